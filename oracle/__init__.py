@@ -1,0 +1,167 @@
+"""CPU oracle for the block-quantised KV decode path (numpy + a plain C library).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product path (the
+CUDA library and its Python binding) never imports, links or calls it, and the two
+share no code: this side works on natural row-major layouts, quantises with the
+plain fp32 rules and attends in fp64.
+
+Definitions restated (sources named per function in ``kvq_oracle.c``):
+  * q8_0 / q4_0 blocks of 32 values with one f16 scale, f16 control arm -- sized by
+    "HAL #582 -- per-layer KV compression study", section 1 (size model table);
+  * exact softmax attention ("logit-identical", same study, sections 3b and 5 P0);
+  * exact merge of split softmax triples (same study, section 5 P2 read path).
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, brute force over codes, exact rational arithmetic, invariants and
+library routines); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvq_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkvq_oracle.so")
+
+TYPES = {"f16": 0, "q8_0": 1, "q4_0": 2}
+QK = 32
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (no fused multiply-add, IEEE semantics)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-std=c11", "-o", _LIB_PATH + ".tmp", _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.kvqo_quantize_rows.argtypes = [i32, vp, i64, i32, vp, vp, i32]
+        L.kvqo_quantize_rows.restype = None
+        L.kvqo_dequantize_rows.argtypes = [i32, vp, vp, i64, i32, vp]
+        L.kvqo_dequantize_rows.restype = None
+        L.kvqo_attention.argtypes = [i32, vp, vp, i32, vp, vp, i32, i64, i64, i32, vp, i32,
+                                     ctypes.c_float, vp, vp, i32]
+        L.kvqo_attention.restype = None
+        L.kvqo_attention_partials.argtypes = [i32, vp, vp, i32, vp, vp, i32, i64, i32, vp, i32,
+                                              ctypes.c_float, vp, i32, vp, vp, vp]
+        L.kvqo_attention_partials.restype = None
+        L.kvqo_combine.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp]
+        L.kvqo_combine.restype = None
+        L.kvqo_code_row_bytes.argtypes = [i32, i32]
+        L.kvqo_code_row_bytes.restype = i64
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def code_dtype(kv_type: str):
+    return {"f16": np.uint16, "q8_0": np.int8, "q4_0": np.uint8}[kv_type]
+
+
+def code_row_len(kv_type: str, D: int) -> int:
+    """Number of code elements per row (f16: D halves, q8_0: D bytes, q4_0: D/2 bytes)."""
+    return {"f16": D, "q8_0": D, "q4_0": D // 2}[kv_type]
+
+
+def quantize(kv_type: str, x: np.ndarray, n_threads: int = 1):
+    """Quantise fp32 rows ``x[..., D]``.  Returns (codes, scales) in natural layout:
+    codes ``[..., code_row_len]`` (f16 bits / int8 / packed uint8), scales f16 bits
+    ``[..., D/32]`` (an empty trailing axis for f16)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    assert D % QK == 0
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    codes = np.empty(x.shape[:-1] + (code_row_len(kv_type, D),), dtype=code_dtype(kv_type))
+    nsc = 0 if kv_type == "f16" else D // QK
+    scales = np.empty(x.shape[:-1] + (nsc,), dtype=np.uint16)
+    lib().kvqo_quantize_rows(TYPES[kv_type], _ptr(x), rows, D, _ptr(codes), _ptr(scales), n_threads)
+    return codes, scales
+
+
+def dequantize(kv_type: str, codes: np.ndarray, scales: np.ndarray, D: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    rows = int(np.prod(codes.shape[:-1])) if codes.ndim > 1 else 1
+    out = np.empty(codes.shape[:-1] + (D,), dtype=np.float64)
+    lib().kvqo_dequantize_rows(TYPES[kv_type], _ptr(codes), _ptr(scales), rows, D, _ptr(out))
+    return out
+
+
+def attention(type_k: str, k_codes, k_scales, type_v: str, v_codes, v_scales, n: int,
+              q: np.ndarray, scale: float, n_threads: int = 1):
+    """Decode attention of one sequence.  ``k_codes [Hkv, cap, row]``, ``k_scales
+    [Hkv, cap, D/32]`` (same for V), ``q [Hq, D]`` fp32; attends over rows ``[0, n)``.
+    Returns (out fp64 [Hq, D], lse fp64 [Hq])."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    Hq, D = q.shape
+    Hkv, cap = k_codes.shape[0], k_codes.shape[1]
+    assert Hq % Hkv == 0 and n <= cap
+    kc, ks = np.ascontiguousarray(k_codes), np.ascontiguousarray(k_scales, dtype=np.uint16)
+    vc, vs = np.ascontiguousarray(v_codes), np.ascontiguousarray(v_scales, dtype=np.uint16)
+    out = np.empty((Hq, D), dtype=np.float64)
+    lse = np.empty((Hq,), dtype=np.float64)
+    lib().kvqo_attention(TYPES[type_k], _ptr(kc), _ptr(ks), TYPES[type_v], _ptr(vc), _ptr(vs),
+                         Hkv, cap, n, D, _ptr(q), Hq, ctypes.c_float(scale), _ptr(out), _ptr(lse),
+                         n_threads)
+    return out, lse
+
+
+def attention_partials(type_k: str, k_codes, k_scales, type_v: str, v_codes, v_scales,
+                       bounds, q: np.ndarray, scale: float):
+    """Unnormalised split triples over key ranges ``[bounds[s], bounds[s+1])``.
+    Returns (o [Hq, S, D], m [Hq, S], l [Hq, S]) in fp64, natural-log units."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    Hq, D = q.shape
+    Hkv, cap = k_codes.shape[0], k_codes.shape[1]
+    b = np.ascontiguousarray(np.asarray(bounds, dtype=np.int64))
+    S = len(b) - 1
+    kc, ks = np.ascontiguousarray(k_codes), np.ascontiguousarray(k_scales, dtype=np.uint16)
+    vc, vs = np.ascontiguousarray(v_codes), np.ascontiguousarray(v_scales, dtype=np.uint16)
+    o = np.empty((Hq, S, D), dtype=np.float64)
+    m = np.empty((Hq, S), dtype=np.float64)
+    l = np.empty((Hq, S), dtype=np.float64)
+    lib().kvqo_attention_partials(TYPES[type_k], _ptr(kc), _ptr(ks), TYPES[type_v], _ptr(vc),
+                                  _ptr(vs), Hkv, cap, D, _ptr(q), Hq, ctypes.c_float(scale),
+                                  _ptr(b), S, _ptr(o), _ptr(m), _ptr(l))
+    return o, m, l
+
+
+def combine(part_o: np.ndarray, part_m: np.ndarray, part_l: np.ndarray):
+    """Merge split triples: ``part_o [R, S, D]``, ``part_m/part_l [R, S]`` -> (out [R, D], lse [R])."""
+    po = np.ascontiguousarray(part_o, dtype=np.float64)
+    pm = np.ascontiguousarray(part_m, dtype=np.float64)
+    pl = np.ascontiguousarray(part_l, dtype=np.float64)
+    R, S, D = po.shape
+    out = np.empty((R, D), dtype=np.float64)
+    lse = np.empty((R,), dtype=np.float64)
+    lib().kvqo_combine(_ptr(po), _ptr(pm), _ptr(pl), R, S, D, _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+if __name__ == "__main__":  # pragma: no cover
+    print(build(force="--force" in sys.argv))
