@@ -1,0 +1,218 @@
+/*
+ * kvq.h -- C ABI of libkvq: a block-quantised KV cache with quantise-on-append and
+ * split-K single-token decode attention for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (problem statement of the spec reading): for each sequence b and
+ * query head hq, with G = Hq / Hkv query heads sharing KV head h = hq / G,
+ *
+ *     s_t   = scale * <q[b,hq,:], k_hat[b,h,t,:]>          for t < len[b]
+ *     out   = sum_t exp(s_t - M) v_hat[b,h,t,:] / sum_t exp(s_t - M),  M = max_t s_t
+ *     lse   = M + log(sum_t exp(s_t - M))
+ *
+ * where k_hat, v_hat are the dequantised cache rows.  Exact softmax attention is what
+ * the pages require a quantised reader to reproduce ("logit-identical", real_frac = 0:
+ * "HAL #582 -- per-layer KV compression study", section 3b finding 2 and section 5 P0).
+ * Storage types are GGML-style blocks of 32 values along the head dimension with one
+ * f16 scale: q8_0 (34 bytes / 32 values), q4_0 (18 bytes / 32 values), and the f16
+ * control arm (same study, section 1 size model: 102 / 54 / 192 KiB per token for the
+ * 48-layer, 8-KV-head, D=128 model).  Asymmetric pairs (q8_0 K / q4_0 V, the study's
+ * default tier, section 4) and symmetric pairs are supported; any (K type, V type)
+ * combination of the three is accepted.
+ *
+ * Quantiser rules (fp32, one rounding per operation):
+ *   q8_0: d = amax/127; q_j = round_half_away(x_j * (1/d)) (0 if d == 0); scale = f16_rne(d)
+ *   q4_0: m = x_k with the largest |x_k| (lowest k on ties); d = m/-8;
+ *         c_j = min(15, trunc(x_j * (1/d) + 8.5)); scale = f16_rne(d);
+ *         a 32-value block packs byte i = c_i | c_{i+16} << 4   (GGML nibble order)
+ *   f16 : x -> binary16, round to nearest even.
+ *   Dequantised values: q8_0 f16(d)*q, q4_0 f16(d)*(c-8), f16 as stored.
+ *
+ * ---------------------------------------------------------------------------------
+ * Memory ownership.  The library allocates NO device memory.  The caller allocates
+ * (with any allocator) the K plane, the V plane, the state block and the decode
+ * workspace, sized by kvq_cache_size / kvq_decode_workspace_size, and keeps them alive
+ * while the cache handle exists.  A handle holds host metadata only (including a host
+ * mirror of the lengths used for capacity checks).  Handles are not thread-safe; all
+ * calls on one cache must be issued to one stream (or externally ordered).
+ *
+ * Asynchrony.  Every call that takes a stream enqueues work on it and returns without
+ * synchronising, except kvq_cache_create, kvq_cache_sync_lengths and
+ * kvq_cache_read_error, which synchronise their stream as documented.  Device pointers must point to
+ * memory of the current CUDA device.  `stream` is a cudaStream_t (NULL = legacy default).
+ *
+ * Errors.  Every entry point returns a kvq_status; nothing aborts, traps or throws.
+ * Argument errors are detected on the host before any launch and leave device memory
+ * untouched.  A launch failure returns KVQ_ERR_CUDA (the CUDA error is not cleared from
+ * the context if it is sticky).  Conditions only the device can see (an append past
+ * capacity after lengths changed behind the host mirror, e.g. in a CUDA-graph replay)
+ * set the state block's error word; kvq_cache_read_error reports it.
+ *
+ * ---------------------------------------------------------------------------------
+ * Cache layout ("fragment-native" tiles).  Rows of one (sequence b, KV head h) are
+ * grouped in tiles of 16 consecutive positions; capacity must be a multiple of 16.
+ * D = 128 * NS (NS = 1 or 2 slices).  Each plane (K and V separately) is
+ *
+ *     [codes region : B][Hkv][capacity/16][NS][code_tile_bytes]
+ *     [scales region: B][Hkv][capacity/16][NS][128]             (absent for f16)
+ *
+ * with code_tile_bytes = 2048 (q8_0), 1024 (q4_0), 4096 (f16) per 16 rows x 128 values,
+ * so the plane size equals the GGML block footprint exactly (bits/value 8.5, 4.5, 16).
+ * Inside a tile, for row kt in [0,16) and value index dd in [0,128) of the slice, with
+ *     n = kt % 8, st = kt / 8, and for "pair" order A/B/C/D:
+ *         kt < 8 : j = kt/2,      pos = kt%2 ? 1 (B) : 0 (A)
+ *         kt >= 8: j = (kt-8)/2,  pos = kt%2 ? 3 (D) : 2 (C)
+ * byte offsets are (b = dd/32, i = dd%32):
+ *   K, q8_0 : b*512 + (4n + (dd%16)/4)*16 + (2st + (i/16))*4 + dd%4
+ *   K, q4_0 : (b/2)*512 + (4n + (i%16)/4)*16 + (2(b%2) + st)*4 + (i%16)%4,
+ *             value in the low nibble if i < 16, else the high nibble
+ *   K, f16  : (2b + st)*512 + (4n + (dd%16)/4)*16 + (i/16)*8 + P(dd%4)*2,
+ *             P(0)=0, P(2)=1, P(1)=2, P(3)=3
+ *   V rows use the pair order; with r = i%16, hv = i/16, n' = r/2:
+ *   V, q8_0 : b*512 + (4n' + j)*16 + ((r%2) + 2hv)*4 + Q(pos),      Q(A,B,C,D) = 0,2,1,3
+ *   V, q4_0 : (b/2)*512 + (4n' + j)*16 + (2(b%2) + r%2)*4 + Q(pos),
+ *             value in the low nibble if i < 16, else the high nibble
+ *   V, f16  : (2b + hv)*512 + (4n' + j)*16 + (r%2)*8 + pos*2
+ *   scales (K or V), for block b of the slice: j*32 + b*8 + pos*2   (f16 bits)
+ * The codes and scales themselves are exactly the GGML q8_0/q4_0 values above; only
+ * their placement differs from GGML's array-of-blocks order.
+ *
+ * State block (int32, 16-byte multiple): [len[B]][append ticket][error word][pad].
+ * Zero it (or set lengths with kvq_cache_set_lengths) before kvq_cache_create.
+ * ---------------------------------------------------------------------------------
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+typedef enum { KVQ_F16 = 0, KVQ_Q8_0 = 1, KVQ_Q4_0 = 2 } kvq_type;
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad descriptor, sizes overflow       */
+    KVQ_ERR_UNSUPPORTED = 2, /* head_dim not 128/256, unknown type, no suitable GPU           */
+    KVQ_ERR_CAPACITY = 3,    /* append would exceed capacity (nothing is written)             */
+    KVQ_ERR_ALIGNMENT = 4,   /* a pointer is not 16-byte aligned                              */
+    KVQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed                          */
+    KVQ_ERR_DEVICE = 6       /* the device error word was set (see kvq_cache_read_error)      */
+} kvq_status;
+
+/* Device error word bits (kvq_cache_read_error). */
+#define KVQ_DEVERR_CAPACITY 0x1 /* an append found len + n_new > capacity on the device     */
+#define KVQ_DEVERR_TIMEOUT 0x2  /* a pipeline wait in a kernel gave up after its time limit */
+
+typedef struct {
+    int32_t batch;      /* B: sequences held by the cache (>= 1)                       */
+    int32_t n_kv_heads; /* Hkv (>= 1)                                                  */
+    int32_t head_dim;   /* D: 128 or 256                                               */
+    int32_t capacity;   /* rows per (sequence, KV head); a positive multiple of 16     */
+    int32_t type_k;     /* kvq_type of the K plane                                     */
+    int32_t type_v;     /* kvq_type of the V plane                                     */
+} kvq_cache_desc;
+
+typedef struct kvq_cache kvq_cache; /* opaque host handle */
+
+/* Bytes the caller must allocate for the K plane, the V plane and the state block.
+ * Pure host arithmetic; no CUDA call. */
+KVQ_API kvq_status kvq_cache_size(const kvq_cache_desc *desc, size_t *k_bytes, size_t *v_bytes,
+                          size_t *state_bytes);
+
+/* Create a handle over caller-owned device memory (all three pointers 16-byte aligned).
+ * Reads the lengths from `state` once to seed the host mirror: the copy is queued on
+ * `stream` (so it follows whatever the caller queued there, e.g. the zero-fill of the
+ * state block) and the call synchronises that stream.  Fails with KVQ_ERR_INVALID_ARG
+ * if a length is outside [0, capacity]. */
+KVQ_API kvq_status kvq_cache_create(const kvq_cache_desc *desc, void *k_mem, void *v_mem, void *state,
+                                    void *stream, kvq_cache **out);
+KVQ_API kvq_status kvq_cache_destroy(kvq_cache *cache);
+
+/* Host mirror of the lengths (B int32).  Exact unless appends ran in a replayed graph. */
+KVQ_API kvq_status kvq_cache_lengths(const kvq_cache *cache, int32_t *h_len);
+/* Set lengths (B int32 host array, each in [0, capacity]); async copy on `stream`. */
+KVQ_API kvq_status kvq_cache_set_lengths(kvq_cache *cache, const int32_t *h_len, void *stream);
+/* Re-read the lengths from the device into the mirror (synchronises `stream`). */
+KVQ_API kvq_status kvq_cache_sync_lengths(kvq_cache *cache, void *stream);
+/* Read and clear the device error word (synchronises `stream`).  *h_err = KVQ_DEVERR_* bits. */
+KVQ_API kvq_status kvq_cache_read_error(kvq_cache *cache, void *stream, int32_t *h_err);
+
+/*
+ * Quantise-on-append (the write path of "HAL #582", section 5 P2: new tokens are
+ * quantised once when they are written).  k and v are fp32 device arrays
+ * [nb][Hkv][n_new][D] (row-major); rows go to positions len[b0+i] .. len[b0+i]+n_new-1
+ * of sequence b0+i, after which len[b0+i] += n_new on the device (in the same launch,
+ * so append + decode can be captured in a CUDA graph).  Positions are read from the
+ * device lengths, not the host mirror.  Returns KVQ_ERR_CAPACITY (nothing written) if
+ * the mirror shows an overflow; an overflow seen only on the device skips that
+ * sequence and sets KVQ_DEVERR_CAPACITY.  n_new == 0 or nb == 0 is a no-op.
+ */
+KVQ_API kvq_status kvq_quantize_append(kvq_cache *cache, const float *k, const float *v, int32_t b0,
+                               int32_t nb, int32_t n_new, void *stream);
+
+/* Number of key splits the decode uses when n_splits == 0 (depends on the GPU, the
+ * cache shape and n_q_heads; not on the lengths, so it is stable under graph replay). */
+KVQ_API kvq_status kvq_decode_auto_splits(const kvq_cache *cache, int32_t n_q_heads, int32_t *n_splits);
+
+/* Workspace bytes for kvq_decode_attention with this n_splits (0 = auto).  The workspace
+ * holds split partials and per-(sequence, KV head) arrival counters; it must be zeroed
+ * once before its first use, and every completed decode leaves the counters at zero. */
+KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache *cache, int32_t n_q_heads, int32_t n_splits,
+                                     size_t *bytes);
+
+/*
+ * Split-K decode attention over the whole cache (all B sequences, lengths read on the
+ * device).  q: fp32 [B][Hq][D]; out: fp32 [B][Hq][D]; lse: fp32 [B][Hq] natural log, or
+ * NULL.  scale multiplies q.k (e.g. 1/sqrt(D)).  Hq must be a multiple of Hkv.  Keys are
+ * split into n_splits contiguous ranges per (sequence, KV head) (0 = auto, else 1..1024);
+ * each range is attended with an online softmax in fp32, and the last range to finish
+ * merges all ranges ("exact online-softmax combine", HAL #582 section 5 P2).  len == 0
+ * gives out = 0 and lse = -inf.  One kernel launch.
+ */
+KVQ_API kvq_status kvq_decode_attention(const kvq_cache *cache, const float *q, int32_t n_q_heads,
+                                float scale, int32_t n_splits, void *workspace, float *out,
+                                float *lse, void *stream);
+
+/*
+ * Same split attention, but writes the unnormalised split triples instead of merging
+ * them: part_o fp32 [B][Hq][n_splits][D] = sum_t exp(s_t - m) v_hat_t over the split,
+ * part_m [B][Hq][n_splits] = max_t s_t (natural units), part_l = sum_t exp(s_t - m).
+ * Empty splits give (o, m, l) = (0, -inf, 0).  n_splits must be given (>= 1).  Split s
+ * of a sequence with T = ceil(len/16) tiles covers tiles [s*c, min(T, (s+1)*c)),
+ * c = ceil(T / min(n_splits, T)).  For merging several caches or key regions, or shards
+ * of one context held on several GPUs, with kvq_combine.
+ */
+KVQ_API kvq_status kvq_decode_partials(const kvq_cache *cache, const float *q, int32_t n_q_heads,
+                               float scale, int32_t n_splits, float *part_o, float *part_m,
+                               float *part_l, void *stream);
+
+/*
+ * Merge split triples: for each of `rows` rows, M = max_s m_s, w_s = exp(m_s - M),
+ * out = sum_s w_s o_s / sum_s w_s l_s, lse = M + log(sum_s w_s l_s) (lse may be NULL).
+ * part_o fp32 [rows][n_splits][head_dim], part_m / part_l fp32 [rows][n_splits],
+ * out fp32 [rows][head_dim].  head_dim a positive multiple of 4; rows with every split
+ * empty give out = 0, lse = -inf.
+ */
+KVQ_API kvq_status kvq_combine(const float *part_o, const float *part_m, const float *part_l,
+                       int32_t rows, int32_t n_splits, int32_t head_dim, float *out, float *lse,
+                       void *stream);
+
+KVQ_API const char *kvq_status_string(kvq_status status);
+KVQ_API int32_t kvq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,349 @@
+// kvq_api.cu -- the C ABI of libkvq (include/kvq.h): argument checks, the host handle,
+// the host mirror of the lengths and the launches.  No device memory is allocated here.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "kvq_internal.cuh"
+
+struct kvq_cache {
+    kvq_cache_desc desc;
+    uint8_t *k_mem, *v_mem;
+    int32_t *state;  // [len B][ticket][error][pad]
+    size_t k_code_bytes, v_code_bytes;
+    int32_t *h_len;  // host mirror
+    int device;
+};
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_type(int32_t t) { return t == KVQ_F16 || t == KVQ_Q8_0 || t == KVQ_Q4_0; }
+
+kvq_status check_desc(const kvq_cache_desc *d) {
+    if (!d) return KVQ_ERR_INVALID_ARG;
+    if (d->batch < 1 || d->n_kv_heads < 1 || d->capacity < 1) return KVQ_ERR_INVALID_ARG;
+    if (d->capacity % kvq::kTileRows != 0) return KVQ_ERR_INVALID_ARG;
+    if (!valid_type(d->type_k) || !valid_type(d->type_v)) return KVQ_ERR_UNSUPPORTED;
+    if (d->head_dim != 128 && d->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+// bytes of the codes region and of the whole plane for one type; false on overflow
+bool plane_bytes(const kvq_cache_desc *d, int type, size_t *codes, size_t *total) {
+    const unsigned long long tiles = static_cast<unsigned long long>(d->batch) * d->n_kv_heads * (d->capacity / 16);
+    const unsigned long long ns = d->head_dim / kvq::kSlice;
+    const unsigned long long per_tile_codes = ns * kvq::code_tile_bytes(type);
+    const unsigned long long per_tile_scales = ns * kvq::scale_tile_bytes(type);
+    if (tiles > (~0ull) / (per_tile_codes + per_tile_scales)) return false;
+    *codes = static_cast<size_t>(tiles * per_tile_codes);
+    *total = static_cast<size_t>(tiles * (per_tile_codes + per_tile_scales));
+    return true;
+}
+
+size_t state_bytes_for(int32_t batch) { return ((static_cast<size_t>(batch) + 2) * 4 + 15) / 16 * 16; }
+
+kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+int auto_splits(const kvq_cache *c, int n_q_heads, int *out) {
+    int ctas = 0, sms = 0;
+    if (kvq::decode_occupancy(c->desc.type_k, c->desc.type_v, c->desc.head_dim, &ctas, &sms) != cudaSuccess)
+        return -1;
+    if (ctas < 1) ctas = 1;
+    const int G = n_q_heads / c->desc.n_kv_heads;
+    const int QG = (G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    const long long units = static_cast<long long>(c->desc.batch) * c->desc.n_kv_heads * QG;
+    // one full wave of CTAs; two waves when sequences may differ in length
+    const long long target = static_cast<long long>(sms) * ctas * (c->desc.batch > 1 ? 2 : 1);
+    long long s = (target + units - 1) / units;
+    const long long max_tiles = c->desc.capacity / kvq::kTileRows;
+    if (s > max_tiles) s = max_tiles;
+    if (s > kvq::kMaxSplits) s = kvq::kMaxSplits;
+    if (s < 1) s = 1;
+    *out = static_cast<int>(s);
+    return 0;
+}
+
+kvq_status check_q_heads(const kvq_cache *c, int32_t n_q_heads) {
+    if (n_q_heads < 1 || n_q_heads % c->desc.n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+    const long long G = n_q_heads / c->desc.n_kv_heads;
+    const long long QG = (G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    if (static_cast<long long>(c->desc.batch) * QG > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (c->desc.n_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+kvq::DecodeParams base_params(const kvq_cache *c, const float *q, int32_t n_q_heads, float scale, int32_t splits) {
+    kvq::DecodeParams p{};
+    p.k_codes = c->k_mem;
+    p.k_scales = c->desc.type_k == KVQ_F16 ? nullptr : c->k_mem + c->k_code_bytes;
+    p.v_codes = c->v_mem;
+    p.v_scales = c->desc.type_v == KVQ_F16 ? nullptr : c->v_mem + c->v_code_bytes;
+    p.len = c->state;
+    p.err = c->state + c->desc.batch + 1;
+    p.q = q;
+    p.B = c->desc.batch;
+    p.Hkv = c->desc.n_kv_heads;
+    p.Hq = n_q_heads;
+    p.G = n_q_heads / c->desc.n_kv_heads;
+    p.QG = (p.G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    p.D = c->desc.head_dim;
+    p.cap_tiles = c->desc.capacity / kvq::kTileRows;
+    p.n_splits = splits;
+    p.scale_log2 = scale * 1.44269504088896340736f;
+    return p;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct WsLayout {
+    size_t counters, counters1, part_m, part_l, part_o, grp_m, grp_l, grp_o, total;
+    int n_groups_max;
+};
+
+WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits) {
+    WsLayout w{};
+    const size_t G = n_q_heads / c->desc.n_kv_heads;
+    const size_t QG = (G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    const size_t rows = static_cast<size_t>(c->desc.batch) * n_q_heads;
+    const size_t units = static_cast<size_t>(c->desc.batch) * c->desc.n_kv_heads * QG;
+    const size_t ng = static_cast<size_t>(kvq::max_merge_groups(splits));
+    w.n_groups_max = static_cast<int>(ng);
+    w.counters = 0;
+    w.counters1 = align256(units * 4);
+    w.part_m = w.counters1 + align256(units * ng * 4);
+    w.part_l = w.part_m + align256(rows * splits * 4);
+    w.part_o = w.part_l + align256(rows * splits * 4);
+    w.grp_m = w.part_o + align256(rows * splits * c->desc.head_dim * 4);
+    w.grp_l = w.grp_m + align256(rows * ng * 4);
+    w.grp_o = w.grp_l + align256(rows * ng * 4);
+    w.total = w.grp_o + align256(rows * ng * c->desc.head_dim * 4);
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kvq_abi_version(void) { return KVQ_ABI_VERSION; }
+
+const char *kvq_status_string(kvq_status s) {
+    switch (s) {
+        case KVQ_OK: return "ok";
+        case KVQ_ERR_INVALID_ARG: return "invalid argument";
+        case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+        case KVQ_ERR_CAPACITY: return "append exceeds cache capacity";
+        case KVQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case KVQ_ERR_CUDA: return "CUDA error";
+        case KVQ_ERR_DEVICE: return "device error word set";
+    }
+    return "unknown status";
+}
+
+kvq_status kvq_cache_size(const kvq_cache_desc *desc, size_t *k_bytes, size_t *v_bytes, size_t *state_bytes) {
+    kvq_status st = check_desc(desc);
+    if (st != KVQ_OK) return st;
+    if (!k_bytes || !v_bytes || !state_bytes) return KVQ_ERR_INVALID_ARG;
+    size_t kc, kt, vc, vt;
+    if (!plane_bytes(desc, desc->type_k, &kc, &kt) || !plane_bytes(desc, desc->type_v, &vc, &vt))
+        return KVQ_ERR_INVALID_ARG;
+    *k_bytes = kt;
+    *v_bytes = vt;
+    *state_bytes = state_bytes_for(desc->batch);
+    return KVQ_OK;
+}
+
+kvq_status kvq_cache_create(const kvq_cache_desc *desc, void *k_mem, void *v_mem, void *state, void *stream,
+                            kvq_cache **out) {
+    kvq_status st = check_desc(desc);
+    if (st != KVQ_OK) return st;
+    if (!k_mem || !v_mem || !state || !out) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k_mem) || !aligned16(v_mem) || !aligned16(state)) return KVQ_ERR_ALIGNMENT;
+    size_t kc, kt, vc, vt;
+    if (!plane_bytes(desc, desc->type_k, &kc, &kt) || !plane_bytes(desc, desc->type_v, &vc, &vt))
+        return KVQ_ERR_INVALID_ARG;
+    kvq_cache *c = new (std::nothrow) kvq_cache;
+    if (!c) return KVQ_ERR_INVALID_ARG;
+    c->h_len = static_cast<int32_t *>(std::calloc(desc->batch, sizeof(int32_t)));
+    if (!c->h_len) {
+        delete c;
+        return KVQ_ERR_INVALID_ARG;
+    }
+    c->desc = *desc;
+    c->k_mem = static_cast<uint8_t *>(k_mem);
+    c->v_mem = static_cast<uint8_t *>(v_mem);
+    c->state = static_cast<int32_t *>(state);
+    c->k_code_bytes = kc;
+    c->v_code_bytes = vc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaMemcpyAsync(c->h_len, state, sizeof(int32_t) * desc->batch, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        std::free(c->h_len);
+        delete c;
+        return KVQ_ERR_CUDA;
+    }
+    for (int i = 0; i < desc->batch; ++i) {
+        if (c->h_len[i] < 0 || c->h_len[i] > desc->capacity) {
+            std::free(c->h_len);
+            delete c;
+            return KVQ_ERR_INVALID_ARG;
+        }
+    }
+    *out = c;
+    return KVQ_OK;
+}
+
+kvq_status kvq_cache_destroy(kvq_cache *cache) {
+    if (!cache) return KVQ_ERR_INVALID_ARG;
+    std::free(cache->h_len);
+    delete cache;
+    return KVQ_OK;
+}
+
+kvq_status kvq_cache_lengths(const kvq_cache *cache, int32_t *h_len) {
+    if (!cache || !h_len) return KVQ_ERR_INVALID_ARG;
+    std::memcpy(h_len, cache->h_len, sizeof(int32_t) * cache->desc.batch);
+    return KVQ_OK;
+}
+
+kvq_status kvq_cache_set_lengths(kvq_cache *cache, const int32_t *h_len, void *stream) {
+    if (!cache || !h_len) return KVQ_ERR_INVALID_ARG;
+    for (int i = 0; i < cache->desc.batch; ++i)
+        if (h_len[i] < 0 || h_len[i] > cache->desc.capacity) return KVQ_ERR_INVALID_ARG;
+    std::memcpy(cache->h_len, h_len, sizeof(int32_t) * cache->desc.batch);
+    // copy from the mirror (which outlives this call), not from the caller's buffer
+    return cuda_status(cudaMemcpyAsync(cache->state, cache->h_len, sizeof(int32_t) * cache->desc.batch,
+                                       cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_cache_sync_lengths(kvq_cache *cache, void *stream) {
+    if (!cache) return KVQ_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(cache->h_len, cache->state, sizeof(int32_t) * cache->desc.batch,
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e);
+}
+
+kvq_status kvq_cache_read_error(kvq_cache *cache, void *stream, int32_t *h_err) {
+    if (!cache || !h_err) return KVQ_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t *err = cache->state + cache->desc.batch + 1;
+    cudaError_t e = cudaMemcpyAsync(h_err, err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e);
+}
+
+kvq_status kvq_quantize_append(kvq_cache *cache, const float *k, const float *v, int32_t b0, int32_t nb,
+                               int32_t n_new, void *stream) {
+    if (!cache) return KVQ_ERR_INVALID_ARG;
+    if (nb < 0 || n_new < 0 || b0 < 0) return KVQ_ERR_INVALID_ARG;
+    if (nb == 0 || n_new == 0) return KVQ_OK;
+    if (b0 + static_cast<long long>(nb) > cache->desc.batch) return KVQ_ERR_INVALID_ARG;
+    if (!k || !v) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_ALIGNMENT;
+    for (int i = 0; i < nb; ++i)
+        if (static_cast<long long>(cache->h_len[b0 + i]) + n_new > cache->desc.capacity) return KVQ_ERR_CAPACITY;
+    const long long warps = static_cast<long long>(nb) * cache->desc.n_kv_heads * n_new * (cache->desc.head_dim / 128);
+    if (warps > (1ll << 31) - 256) return KVQ_ERR_INVALID_ARG;
+    kvq::AppendParams p{};
+    p.k_codes = cache->k_mem;
+    p.k_scales = cache->desc.type_k == KVQ_F16 ? nullptr : cache->k_mem + cache->k_code_bytes;
+    p.v_codes = cache->v_mem;
+    p.v_scales = cache->desc.type_v == KVQ_F16 ? nullptr : cache->v_mem + cache->v_code_bytes;
+    p.len = cache->state;
+    p.ticket = cache->state + cache->desc.batch;
+    p.err = cache->state + cache->desc.batch + 1;
+    p.k = k;
+    p.v = v;
+    p.b0 = b0;
+    p.nb = nb;
+    p.n_new = n_new;
+    p.Hkv = cache->desc.n_kv_heads;
+    p.D = cache->desc.head_dim;
+    p.cap = cache->desc.capacity;
+    p.cap_tiles = cache->desc.capacity / kvq::kTileRows;
+    p.total_warps = static_cast<int>(warps);
+    cudaError_t e = kvq::launch_append(cache->desc.type_k, cache->desc.type_v, p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    for (int i = 0; i < nb; ++i) cache->h_len[b0 + i] += n_new;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_auto_splits(const kvq_cache *cache, int32_t n_q_heads, int32_t *n_splits) {
+    if (!cache || !n_splits) return KVQ_ERR_INVALID_ARG;
+    kvq_status st = check_q_heads(cache, n_q_heads);
+    if (st != KVQ_OK) return st;
+    int s = 0;
+    if (auto_splits(cache, n_q_heads, &s) != 0) return KVQ_ERR_CUDA;
+    *n_splits = s;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_workspace_size(const kvq_cache *cache, int32_t n_q_heads, int32_t n_splits, size_t *bytes) {
+    if (!cache || !bytes) return KVQ_ERR_INVALID_ARG;
+    kvq_status st = check_q_heads(cache, n_q_heads);
+    if (st != KVQ_OK) return st;
+    if (n_splits < 0 || n_splits > kvq::kMaxSplits) return KVQ_ERR_INVALID_ARG;
+    int s = n_splits;
+    if (s == 0 && auto_splits(cache, n_q_heads, &s) != 0) return KVQ_ERR_CUDA;
+    *bytes = ws_layout(cache, n_q_heads, s).total;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(const kvq_cache *cache, const float *q, int32_t n_q_heads, float scale,
+                                int32_t n_splits, void *workspace, float *out, float *lse, void *stream) {
+    if (!cache || !q || !workspace || !out) return KVQ_ERR_INVALID_ARG;
+    kvq_status st = check_q_heads(cache, n_q_heads);
+    if (st != KVQ_OK) return st;
+    if (n_splits < 0 || n_splits > kvq::kMaxSplits) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || (lse && !aligned16(lse)))
+        return KVQ_ERR_ALIGNMENT;
+    int s = n_splits;
+    if (s == 0 && auto_splits(cache, n_q_heads, &s) != 0) return KVQ_ERR_CUDA;
+    const WsLayout w = ws_layout(cache, n_q_heads, s);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s);
+    p.out = out;
+    p.lse = lse;
+    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
+    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
+    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
+    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
+    p.n_groups_max = w.n_groups_max;
+    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
+    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
+    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    return cuda_status(
+        kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_decode_partials(const kvq_cache *cache, const float *q, int32_t n_q_heads, float scale,
+                               int32_t n_splits, float *part_o, float *part_m, float *part_l, void *stream) {
+    if (!cache || !q || !part_o || !part_m || !part_l) return KVQ_ERR_INVALID_ARG;
+    kvq_status st = check_q_heads(cache, n_q_heads);
+    if (st != KVQ_OK) return st;
+    if (n_splits < 1 || n_splits > kvq::kMaxSplits) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(part_o)) return KVQ_ERR_ALIGNMENT;
+    kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, n_splits);
+    p.part_o = part_o;
+    p.part_m = part_m;
+    p.part_l = part_l;
+    return cuda_status(
+        kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, false, static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_combine(const float *part_o, const float *part_m, const float *part_l, int32_t rows,
+                       int32_t n_splits, int32_t head_dim, float *out, float *lse, void *stream) {
+    if (!part_o || !part_m || !part_l || !out) return KVQ_ERR_INVALID_ARG;
+    if (rows < 0 || n_splits < 1 || n_splits > 8192 || head_dim < 4 || head_dim % 4 != 0) return KVQ_ERR_INVALID_ARG;
+    if (rows == 0) return KVQ_OK;
+    if (!aligned16(part_o) || !aligned16(out)) return KVQ_ERR_ALIGNMENT;
+    kvq::CombineParams p{part_o, part_m, part_l, out, lse, rows, n_splits, head_dim};
+    return cuda_status(kvq::launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

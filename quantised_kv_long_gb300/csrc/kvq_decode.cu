@@ -1,0 +1,756 @@
+// kvq_decode.cu -- split-K flash-decode over the block-quantised cache, and the split merge.
+//
+// Method: single-token grouped-query decode attention with the keys of each (sequence,
+// KV head) split into contiguous ranges; each range is attended with an online softmax
+// in fp32 and the ranges are merged exactly ("HAL #582 -- per-layer KV compression
+// study", section 5 P2 read path: "exact online-softmax combine").  The K/V blocks are
+// dequantised in registers while they are read, which is the cure the same study
+// (section 3b, finding 2) gives for a quantised reader that was kernel-bound: throughput
+// has to follow the bytes moved.
+//
+// GB300 mapping (one CTA per (split, KV head, sequence x row-group)):
+//   * warp 0 (producer): 1-D bulk copies (cp.async.bulk, TMA engine) of a run of whole
+//     16-row tiles per stage into a shared-memory ring; completion on mbarriers; every
+//     wait is bounded and reports KVQ_DEVERR_TIMEOUT instead of hanging.
+//   * consumer warps: each owns one tile (and one 128-value slice) per stage.  Tiles are
+//     stored fragment-native (include/kvq.h), so every lane fetches its mma operands
+//     with 16-byte shared loads, converts codes to exact f16 integers with bit tricks
+//     (no I2F), and runs mma.sync m16n8k16 (f16 in, fp32 accumulate).
+//     S = Q K^T: A = [Q_hi ; Q_lo] (M rows 0-7 / 8-15 = up to 8 query heads split into
+//     f16 hi + lo parts, so Q loses nothing), B = K codes (exact), one accumulator per
+//     32-value block, multiplied by the f16 scale afterwards in fp32.
+//     O += P V: the S accumulator layout is the A layout of the next mma, so P never
+//     leaves registers; the V scale of each (row, block) is folded into P, which is
+//     again split into f16 hi + lo rows.
+//   * the CTA merges its warps in shared memory, writes one split triple, and the last
+//     CTA of each (sequence, KV head, row-group) merges all splits (arrival counter).
+#include <math_constants.h>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units): p <= 2^8 between rescales
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// f32 pair -> (f16 hi pair, f16 lo pair) with hi + lo == x to ~2^-22 relative
+__device__ __forceinline__ void split_hi_lo(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    hi = h2_as_u32(h);
+    lo = h2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+}
+
+// 4 int8 codes (bytes x0..x3) -> f16 pairs (x0, x2) and (x1, x3), exact.
+// (byte ^ 0x80) | 0x6400 is the f16 1024 + (code + 128); subtracting 1152 leaves the code.
+__device__ __forceinline__ void cvt_q8(uint32_t w, uint32_t &p02, uint32_t &p13) {
+    const __half2 k1152 = __float2half2_rn(1152.0f);
+    const uint32_t a = (w & 0x00ff00ffu) ^ 0x64806480u;
+    const uint32_t b = ((w >> 8) & 0x00ff00ffu) ^ 0x64806480u;
+    p02 = h2_as_u32(__hsub2(u32_as_h2(a), k1152));
+    p13 = h2_as_u32(__hsub2(u32_as_h2(b), k1152));
+}
+
+// 4 bytes of q4_0 nibbles -> f16 pairs (code - 8): low nibbles of bytes (0,2), (1,3) and
+// high nibbles of bytes (0,2), (1,3).  nibble | 0x6400 is 1024 + c; (c << 4) | 0x6400 is
+// 1024 + 16c, and (1024 + 16c)/16 - 72 = c - 8 exactly.
+__device__ __forceinline__ void cvt_q4(uint32_t w, uint32_t &lo02, uint32_t &lo13, uint32_t &hi02, uint32_t &hi13) {
+    const __half2 k1032 = __float2half2_rn(1032.0f);
+    const __half2 k16th = __float2half2_rn(0.0625f);
+    const __half2 km72 = __float2half2_rn(-72.0f);
+    const uint32_t w8 = w >> 8;
+    lo02 = h2_as_u32(__hsub2(u32_as_h2((w & 0x000f000fu) | 0x64006400u), k1032));
+    lo13 = h2_as_u32(__hsub2(u32_as_h2((w8 & 0x000f000fu) | 0x64006400u), k1032));
+    hi02 = h2_as_u32(__hfma2(u32_as_h2((w & 0x00f000f0u) | 0x64006400u), k16th, km72));
+    hi13 = h2_as_u32(__hfma2(u32_as_h2((w8 & 0x00f000f0u) | 0x64006400u), k16th, km72));
+}
+
+
+constexpr int kDirectMerge = 8;     // up to this many splits are merged in one level
+constexpr int kMaxMergeWidth = 32;  // ceil(sqrt(kMaxSplits)): widest merge of either level
+
+__device__ __forceinline__ int group_size(int ns) {
+    int g = 1;
+    while (g * g < ns) ++g;
+    return g;
+}
+
+// All threads of the CTA call this after writing their results.  Returns true in the
+// CTA that is the target-th to arrive on *counter (it then sees every earlier write).
+__device__ __forceinline__ bool arrive_last(int32_t *counter, int target, int &s_flag) {
+    __threadfence();  // each thread publishes its own writes
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int t = atomicAdd(counter, 1);
+        s_flag = (t == target - 1);
+    }
+    __syncthreads();
+    const bool last = s_flag != 0;
+    if (last) __threadfence();
+    return last;
+}
+
+// Merge NP split triples (o, m, l) of `rows` consecutive query rows starting at row0:
+//   M = max_s m_s, w_s = exp(m_s - M), O = sum_s w_s o_s, L = sum_s w_s l_s.
+// Triples of row r, split s live at (r * stride + s0 + s).  Writes either the normalised
+// output (out = O / L, lse = M + log L) or one unnormalised triple at (r * q_stride + q_s).
+__device__ void merge_rows(const float *po, const float *pm, const float *pl, int stride, int s0, int NP,
+                           size_t row0, int rows, int D, float *scratch, float *out, float *lse, float *qo,
+                           float *qm, float *ql, int q_stride, int q_s) {
+    float *wbuf = scratch;                              // [rows][NP]
+    float *Mbuf = scratch + kMaxRowsPerGroup * kMaxMergeWidth;
+    float *Lbuf = Mbuf + kMaxRowsPerGroup;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int g = warp; g < rows; g += nwarps) {
+        const size_t pr = (row0 + g) * stride + s0;
+        float M = -CUDART_INF_F;
+        for (int s = lane; s < NP; s += 32) M = fmaxf(M, __ldcg(pm + pr + s));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float Ls = 0.f;
+        for (int s = lane; s < NP; s += 32) {
+            const float ms = __ldcg(pm + pr + s);
+            const float w = (M == -CUDART_INF_F || ms == -CUDART_INF_F) ? 0.f : expf(ms - M);
+            wbuf[g * kMaxMergeWidth + s] = w;
+            Ls = fmaf(w, __ldcg(pl + pr + s), Ls);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+        if (lane == 0) {
+            Mbuf[g] = M;
+            Lbuf[g] = Ls;
+        }
+    }
+    __syncthreads();
+    const int DQ = D / 4;
+    for (int idx = threadIdx.x; idx < rows * DQ; idx += blockDim.x) {
+        const int g = idx / DQ, dq = idx % DQ;
+        const float4 *src = reinterpret_cast<const float4 *>(po) + ((row0 + g) * stride + s0) * DQ + dq;
+        const float *w = wbuf + g * kMaxMergeWidth;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < NP; c0 += 8) {
+            // up to eight independent loads in flight per thread, then the weighted sum
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = (c0 + u < NP) ? __ldcg(src + (size_t)(c0 + u) * DQ) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float ws = (c0 + u < NP) ? w[c0 + u] : 0.f;
+                acc.x = fmaf(ws, v[u].x, acc.x);
+                acc.y = fmaf(ws, v[u].y, acc.y);
+                acc.z = fmaf(ws, v[u].z, acc.z);
+                acc.w = fmaf(ws, v[u].w, acc.w);
+            }
+        }
+        const float Ls = Lbuf[g];
+        if (out) {
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            reinterpret_cast<float4 *>(out + (row0 + g) * D)[dq] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (dq == 0 && lse) lse[row0 + g] = Ls > 0.f ? Mbuf[g] + logf(Ls) : -CUDART_INF_F;
+        } else {
+            const size_t dr = (row0 + g) * static_cast<size_t>(q_stride) + q_s;
+            reinterpret_cast<float4 *>(qo + dr * D)[dq] = acc;
+            if (dq == 0) {
+                qm[dr] = Mbuf[g];
+                ql[dr] = Ls;
+            }
+        }
+    }
+}
+
+template <int KT, int VT, int NS>
+struct Cfg {
+    static constexpr int TW = NS == 1 ? 4 : 2;  // tile-warps (one tile per stage each)
+    static constexpr int CW = TW * NS;         // consumer warps
+    static constexpr int THREADS = 32 * (CW + 1);
+    static constexpr int KC = code_tile_bytes(KT) * NS;
+    static constexpr int VC = code_tile_bytes(VT) * NS;
+    static constexpr int KS = scale_tile_bytes(KT) * NS;
+    static constexpr int VS = scale_tile_bytes(VT) * NS;
+    static constexpr int TILE = KC + VC + KS + VS;
+    static constexpr int STAGE = TW * TILE;
+    static constexpr int MIN_CTAS = 2;  // resident CTAs per SM the register/shared budgets aim at
+    static constexpr int STAGES_RAW = 98304 / STAGE;
+    static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 16 ? 16 : STAGES_RAW);
+    static constexpr int RING = STAGES * STAGE;
+    static constexpr int XCHG = NS == 2 ? TW * 2 * 2 * 32 * 16 : 0;
+    static constexpr int BAR_OFF = RING + XCHG;
+    static constexpr int SMEM = BAR_OFF + 2 * STAGES * 8 + 16;
+    static constexpr int D = NS * kSlice;
+    // merge / combine scratch reuses the ring
+    static_assert(TW * kMaxRowsPerGroup * D * 4 + 2 * TW * kMaxRowsPerGroup * 4 <= RING, "merge buffer");
+    static_assert(kMaxRowsPerGroup * (kMaxMergeWidth + 2) * 4 <= RING, "merge scratch");
+};
+
+template <int KT, int VT, int NS>
+__global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
+    using C = Cfg<KT, VT, NS>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_flag;
+    __shared__ int s_timeout;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x, h = blockIdx.y;
+    const int bseq = blockIdx.z / p.QG, qg = blockIdx.z % p.QG;
+    const int cap_rows = p.cap_tiles * kTileRows;
+    int L = __ldcg(p.len + bseq);
+    L = L < 0 ? 0 : (L > cap_rows ? cap_rows : L);
+    const int T = (L + kTileRows - 1) / kTileRows;
+    const int ns = max(1, min(p.n_splits, T));
+    const int tps = T > 0 ? (T + ns - 1) / ns : 0;
+    const int rows = min(kMaxRowsPerGroup, p.G - qg * kMaxRowsPerGroup);
+    const int hq0 = h * p.G + qg * kMaxRowsPerGroup;  // first query head of this CTA
+
+    if (split >= ns) {
+        if (!fused) {  // partials mode: splits beyond ns are empty triples
+            for (int idx = threadIdx.x; idx < rows * (p.D / 4); idx += blockDim.x) {
+                const int g = idx / (p.D / 4), dq = idx % (p.D / 4);
+                const size_t pr = (static_cast<size_t>(bseq) * p.Hq + hq0 + g) * p.n_splits + split;
+                reinterpret_cast<float4 *>(p.part_o + pr * p.D)[dq] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (dq == 0) {
+                    p.part_m[pr] = -CUDART_INF_F;
+                    p.part_l[pr] = 0.f;
+                }
+            }
+        }
+        return;
+    }
+    const int t_begin = min(T, split * tps), t_end = min(T, t_begin + tps);
+    const int n_stage = (t_end - t_begin + C::TW - 1) / C::TW;
+
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, C::CW);
+        }
+        fence_mbar_init();
+        s_timeout = 0;
+    }
+    __syncthreads();
+
+    const size_t bh_tile = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles;
+
+    // per-consumer results kept until the merge
+    float m_run = -CUDART_INF_F, l_acc = 0.f;
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    int tw = 0, sl = 0;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            int issued_use[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) issued_use[i] = -1;
+            bool ok = true;
+            for (int k = 0; k < n_stage && ok; ++k) {
+                const int slot = k % C::STAGES, use = k / C::STAGES;
+                if (use > 0 && !mbar_wait(empty + slot, (use - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const int t0 = t_begin + k * C::TW;
+                const int nt = min(C::TW, t_end - t0);
+                uint8_t *st = smem + slot * C::STAGE;
+                mbar_arrive_expect_tx(full + slot, static_cast<uint32_t>(nt * C::TILE));
+                bulk_g2s(st, p.k_codes + (bh_tile + t0) * C::KC, nt * C::KC, full + slot);
+                bulk_g2s(st + C::TW * C::KC, p.v_codes + (bh_tile + t0) * C::VC, nt * C::VC, full + slot);
+                if constexpr (C::KS > 0)
+                    bulk_g2s(st + C::TW * (C::KC + C::VC), p.k_scales + (bh_tile + t0) * C::KS, nt * C::KS,
+                             full + slot);
+                if constexpr (C::VS > 0)
+                    bulk_g2s(st + C::TW * (C::KC + C::VC + C::KS), p.v_scales + (bh_tile + t0) * C::VS, nt * C::VS,
+                             full + slot);
+                issued_use[slot] = use;
+            }
+            if (!ok) {
+                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
+                s_timeout = 1;
+                // let the copies already issued land before the CTA can exit
+                for (int i = 0; i < C::STAGES; ++i)
+                    if (issued_use[i] >= 0) (void)mbar_wait(full + i, issued_use[i] & 1);
+            }
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const int cw = warp - 1;
+        tw = cw / NS;
+        sl = cw % NS;
+        const int g = lane >> 2, j = lane & 3;
+
+        // Q fragments (scaled to log2 units, split into f16 hi + lo rows)
+        uint32_t qa[8][4];
+        {
+            const bool rv = g < rows;
+            const float *qrow = p.q + (static_cast<size_t>(bseq) * p.Hq + hq0 + (rv ? g : 0)) * p.D + sl * kSlice;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float4 x = rv ? *reinterpret_cast<const float4 *>(qrow + 16 * c + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x.x *= p.scale_log2;
+                x.y *= p.scale_log2;
+                x.z *= p.scale_log2;
+                x.w *= p.scale_log2;
+                split_hi_lo(x.x, x.z, qa[c][0], qa[c][1]);  // k = 2j, 2j+1  <->  d + 0, d + 2
+                split_hi_lo(x.y, x.w, qa[c][2], qa[c][3]);  // k = 2j+8, 2j+9 <-> d + 1, d + 3
+            }
+        }
+        float4 *xchg = reinterpret_cast<float4 *>(smem + C::RING);
+        bool dead = false;
+
+        for (int k = 0; k < n_stage; ++k) {
+            const int slot = k % C::STAGES, use = k / C::STAGES;
+            if (!dead && !mbar_wait(full + slot, use & 1)) {
+                dead = true;
+                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
+                s_timeout = 1;
+            }
+            const int tile = t_begin + k * C::TW + tw;
+            if (tile < t_end) {
+                const int nvalid = min(kTileRows, L - tile * kTileRows);
+                const uint8_t *st = smem + slot * C::STAGE;
+                const uint8_t *kc = st + tw * C::KC + sl * code_tile_bytes(KT);
+                const uint8_t *vc = st + C::TW * C::KC + tw * C::VC + sl * code_tile_bytes(VT);
+                const uint8_t *ks = st + C::TW * (C::KC + C::VC) + tw * C::KS + sl * kScaleTile;
+                const uint8_t *vs = st + C::TW * (C::KC + C::VC + C::KS) + tw * C::VS + sl * kScaleTile;
+
+                // ---- S = Q K^T for keys A=2j, B=2j+1 (S-tile 0) and C=8+2j, D=9+2j (S-tile 1) ----
+                float s0, s1, s2, s3;
+                if constexpr (KT == KVQ_F16) {
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const uint4 w0 = lds128(kc + (2 * b + 0) * 512 + lane * 16);
+                        const uint4 w1 = lds128(kc + (2 * b + 1) * 512 + lane * 16);
+                        mma_16816(acc[0], qa[2 * b], w0.x, w0.y);
+                        mma_16816(acc[0], qa[2 * b + 1], w0.z, w0.w);
+                        mma_16816(acc[1], qa[2 * b], w1.x, w1.y);
+                        mma_16816(acc[1], qa[2 * b + 1], w1.z, w1.w);
+                    }
+                    s0 = acc[0][0] + acc[0][2];
+                    s1 = acc[0][1] + acc[0][3];
+                    s2 = acc[1][0] + acc[1][2];
+                    s3 = acc[1][1] + acc[1][3];
+                } else {
+                    const uint4 sc0 = lds128(ks + j * 32), sc1 = lds128(ks + j * 32 + 16);
+                    const uint32_t kscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
+                    s0 = s1 = s2 = s3 = 0.f;
+                    uint4 wq4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        if constexpr (KT == KVQ_Q8_0) {
+                            const uint4 w = lds128(kc + b * 512 + lane * 16);
+                            uint32_t x0, x1;
+                            cvt_q8(w.x, x0, x1);
+                            mma_16816(acc[0], qa[2 * b], x0, x1);
+                            cvt_q8(w.y, x0, x1);
+                            mma_16816(acc[0], qa[2 * b + 1], x0, x1);
+                            cvt_q8(w.z, x0, x1);
+                            mma_16816(acc[1], qa[2 * b], x0, x1);
+                            cvt_q8(w.w, x0, x1);
+                            mma_16816(acc[1], qa[2 * b + 1], x0, x1);
+                        } else {
+                            if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
+                            const uint32_t w_st0 = (b & 1) ? wq4.z : wq4.x;
+                            const uint32_t w_st1 = (b & 1) ? wq4.w : wq4.y;
+                            uint32_t l02, l13, h02, h13;
+                            cvt_q4(w_st0, l02, l13, h02, h13);
+                            mma_16816(acc[0], qa[2 * b], l02, l13);
+                            mma_16816(acc[0], qa[2 * b + 1], h02, h13);
+                            cvt_q4(w_st1, l02, l13, h02, h13);
+                            mma_16816(acc[1], qa[2 * b], l02, l13);
+                            mma_16816(acc[1], qa[2 * b + 1], h02, h13);
+                        }
+                        const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
+                        const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
+                        s0 = fmaf(dab.x, acc[0][0] + acc[0][2], s0);
+                        s1 = fmaf(dab.y, acc[0][1] + acc[0][3], s1);
+                        s2 = fmaf(dcd.x, acc[1][0] + acc[1][2], s2);
+                        s3 = fmaf(dcd.y, acc[1][1] + acc[1][3], s3);
+                    }
+                }
+                if constexpr (NS == 2) {
+                    // the two slice-warps of this tile add their partial scores
+                    float4 *mine = xchg + ((tw * 2 + (k & 1)) * 2 + sl) * 32;
+                    float4 *other = xchg + ((tw * 2 + (k & 1)) * 2 + (1 - sl)) * 32;
+                    mine[lane] = make_float4(s0, s1, s2, s3);
+                    asm volatile("bar.sync %0, 64;\n" ::"r"(1 + tw) : "memory");
+                    const float4 os = other[lane];
+                    s0 += os.x;
+                    s1 += os.y;
+                    s2 += os.z;
+                    s3 += os.w;
+                }
+                const bool partial = nvalid < kTileRows;
+                bool va = true, vb = true, vcc = true, vd = true;
+                if (partial) {
+                    va = 2 * j < nvalid;
+                    vb = 2 * j + 1 < nvalid;
+                    vcc = 8 + 2 * j < nvalid;
+                    vd = 9 + 2 * j < nvalid;
+                    if (!va) s0 = -CUDART_INF_F;
+                    if (!vb) s1 = -CUDART_INF_F;
+                    if (!vcc) s2 = -CUDART_INF_F;
+                    if (!vd) s3 = -CUDART_INF_F;
+                }
+
+                // ---- online softmax (log2 units), lazy rescale ----
+                // p = exp2(s - m_run) may reach 2^kTau before the running maximum is moved;
+                // the V scales are checked so that p * scale can never overflow f16.
+                float mt = fmaxf(fmaxf(s0, s1), fmaxf(s2, s3));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+                bool exact = false;
+                if constexpr (VT != KVQ_F16) {
+                    const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
+                    // exponent field of any |scale| >= 256 (or inf/nan); an OR may over-report,
+                    // which only costs an exact rescale
+                    const uint32_t e = ((sc0.x | sc0.y | sc0.z) | (sc0.w | sc1.x | sc1.y) | (sc1.z | sc1.w)) & 0x7c007c00u;
+                    exact = __vcmpgeu2(e, 0x5c005c00u) != 0;
+                    // the four lanes of a row must take the same decision: make it warp-wide
+                    exact = __any_sync(0xffffffffu, exact);
+                }
+                const bool need = mt > m_run + (exact ? 0.f : kTau);
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = need ? mt : m_run;
+                    const float alpha = (m_run == -CUDART_INF_F) ? 0.f : ex2(m_run - m_new);
+                    m_run = m_new;
+                    l_acc *= alpha;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        o[i][0] *= alpha;
+                        o[i][1] *= alpha;
+                        o[i][2] *= alpha;
+                        o[i][3] *= alpha;
+                    }
+                }
+                const float p0 = ex2(s0 - m_run), p1 = ex2(s1 - m_run);
+                const float p2 = ex2(s2 - m_run), p3 = ex2(s3 - m_run);
+                l_acc += (p0 + p1) + (p2 + p3);
+
+                // ---- O += P V ----
+                if constexpr (VT == KVQ_F16) {
+                    uint32_t a[4];
+                    split_hi_lo(p0, p1, a[0], a[1]);
+                    split_hi_lo(p2, p3, a[2], a[3]);
+                    const uint32_t mab = (va ? 0x0000ffffu : 0u) | (vb ? 0xffff0000u : 0u);
+                    const uint32_t mcd = (vcc ? 0x0000ffffu : 0u) | (vd ? 0xffff0000u : 0u);
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        uint4 w0 = lds128(vc + (2 * b + 0) * 512 + lane * 16);
+                        uint4 w1 = lds128(vc + (2 * b + 1) * 512 + lane * 16);
+                        if (partial) {  // rows past the length may hold any bits (NaN)
+                            w0.x &= mab;
+                            w0.y &= mcd;
+                            w0.z &= mab;
+                            w0.w &= mcd;
+                            w1.x &= mab;
+                            w1.y &= mcd;
+                            w1.z &= mab;
+                            w1.w &= mcd;
+                        }
+                        mma_16816(o[4 * b + 0], a, w0.x, w0.y);
+                        mma_16816(o[4 * b + 1], a, w0.z, w0.w);
+                        mma_16816(o[4 * b + 2], a, w1.x, w1.y);
+                        mma_16816(o[4 * b + 3], a, w1.z, w1.w);
+                    }
+                } else {
+                    const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
+                    const uint32_t vscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
+                    uint4 wq4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        float2 dab = __half22float2(u32_as_h2(vscale[b][0]));
+                        float2 dcd = __half22float2(u32_as_h2(vscale[b][1]));
+                        if (partial) {  // scales past the length may hold any bits
+                            dab.x = va ? dab.x : 0.f;
+                            dab.y = vb ? dab.y : 0.f;
+                            dcd.x = vcc ? dcd.x : 0.f;
+                            dcd.y = vd ? dcd.y : 0.f;
+                        }
+                        uint32_t a[4];
+                        split_hi_lo(p0 * dab.x, p1 * dab.y, a[0], a[1]);
+                        split_hi_lo(p2 * dcd.x, p3 * dcd.y, a[2], a[3]);
+                        if constexpr (VT == KVQ_Q8_0) {
+                            const uint4 w = lds128(vc + b * 512 + lane * 16);
+                            uint32_t x0, x1;
+                            cvt_q8(w.x, x0, x1);
+                            mma_16816(o[4 * b + 0], a, x0, x1);
+                            cvt_q8(w.y, x0, x1);
+                            mma_16816(o[4 * b + 1], a, x0, x1);
+                            cvt_q8(w.z, x0, x1);
+                            mma_16816(o[4 * b + 2], a, x0, x1);
+                            cvt_q8(w.w, x0, x1);
+                            mma_16816(o[4 * b + 3], a, x0, x1);
+                        } else {
+                            if ((b & 1) == 0) wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
+                            const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x;  // bytes 2n'   of the block
+                            const uint32_t wq1 = (b & 1) ? wq4.w : wq4.y;  // bytes 2n'+1 of the block
+                            uint32_t l02, l13, h02, h13;
+                            cvt_q4(wq0, l02, l13, h02, h13);
+                            mma_16816(o[4 * b + 0], a, l02, l13);
+                            mma_16816(o[4 * b + 2], a, h02, h13);
+                            cvt_q4(wq1, l02, l13, h02, h13);
+                            mma_16816(o[4 * b + 1], a, l02, l13);
+                            mma_16816(o[4 * b + 3], a, h02, h13);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && !dead) mbar_arrive(empty + slot);
+        }
+        // row sums over the four lanes of a row
+        l_acc += __shfl_xor_sync(0xffffffffu, l_acc, 1);
+        l_acc += __shfl_xor_sync(0xffffffffu, l_acc, 2);
+    }
+
+    // ---------------- merge the tile-warps of this CTA ----------------
+    __syncthreads();  // the ring is free from here on
+    constexpr int D = C::D;
+    float *Ob = reinterpret_cast<float *>(smem);                    // [TW][8][D]
+    float *mb = Ob + C::TW * kMaxRowsPerGroup * D;                 // [TW][8]
+    float *lb = mb + C::TW * kMaxRowsPerGroup;                     // [TW][8]
+    if (warp > 0) {
+        const int g = lane >> 2, j = lane & 3;
+        float *orow = Ob + (tw * kMaxRowsPerGroup + g) * D + sl * kSlice;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            // thread holds d = 32b + 4j + {0..3} (ptiles 0,1 of block b) and +16 (ptiles 2,3)
+            const float4 lo4 = make_float4(o[4 * b + 0][0] + o[4 * b + 0][2], o[4 * b + 1][0] + o[4 * b + 1][2],
+                                           o[4 * b + 0][1] + o[4 * b + 0][3], o[4 * b + 1][1] + o[4 * b + 1][3]);
+            const float4 hi4 = make_float4(o[4 * b + 2][0] + o[4 * b + 2][2], o[4 * b + 3][0] + o[4 * b + 3][2],
+                                           o[4 * b + 2][1] + o[4 * b + 2][3], o[4 * b + 3][1] + o[4 * b + 3][3]);
+            *reinterpret_cast<float4 *>(orow + 32 * b + 4 * j) = lo4;
+            *reinterpret_cast<float4 *>(orow + 32 * b + 16 + 4 * j) = hi4;
+        }
+        if (sl == 0 && j == 0) {
+            mb[tw * kMaxRowsPerGroup + g] = m_run;
+            lb[tw * kMaxRowsPerGroup + g] = l_acc;
+        }
+    }
+    __syncthreads();
+    const bool timed_out = s_timeout != 0;
+    const bool single = (ns == 1) && fused;
+    for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
+        const int g = idx / (D / 4), dq = idx % (D / 4);
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int t = 0; t < C::TW; ++t) M = fmaxf(M, mb[t * kMaxRowsPerGroup + g]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lsum = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int t = 0; t < C::TW; ++t) {
+                const float w = ex2(mb[t * kMaxRowsPerGroup + g] - M);  // exp2(-inf) = 0
+                const float4 v = reinterpret_cast<const float4 *>(Ob + (t * kMaxRowsPerGroup + g) * D)[dq];
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+                lsum = fmaf(w, lb[t * kMaxRowsPerGroup + g], lsum);
+            }
+        }
+        const int hq = hq0 + g;
+        if (single) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            reinterpret_cast<float4 *>(p.out + (static_cast<size_t>(bseq) * p.Hq + hq) * D)[dq] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (dq == 0 && p.lse)
+                p.lse[static_cast<size_t>(bseq) * p.Hq + hq] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -CUDART_INF_F;
+        } else {
+            const size_t pr = (static_cast<size_t>(bseq) * p.Hq + hq) * p.n_splits + split;
+            reinterpret_cast<float4 *>(p.part_o + pr * D)[dq] = acc;
+            if (dq == 0) {
+                p.part_m[pr] = M == -CUDART_INF_F ? -CUDART_INF_F : M * kLn2;
+                p.part_l[pr] = lsum;
+            }
+        }
+    }
+    if (!fused || single || timed_out) return;
+
+    // ---------------- merge of the splits of this (sequence, KV head, row group) ----------------
+    // ns <= 8: the last CTA to arrive merges all splits.  Otherwise splits form groups of
+    // ceil(sqrt(ns)); the last arrival of each group merges its group into a group triple
+    // while other CTAs still run, and the last group to finish merges the group triples.
+    const size_t unit = (static_cast<size_t>(bseq) * p.Hkv + h) * p.QG + qg;
+    const size_t row0 = static_cast<size_t>(bseq) * p.Hq + hq0;
+    float *scratch = reinterpret_cast<float *>(smem);
+    if (ns <= kDirectMerge) {
+        if (!arrive_last(p.counters + unit, ns, s_flag)) return;
+        merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, 0, ns, row0, rows, D, scratch, p.out, p.lse, nullptr,
+                   nullptr, nullptr, 0, 0);
+        if (threadIdx.x == 0) p.counters[unit] = 0;
+        return;
+    }
+    const int gs = group_size(ns);
+    const int n_groups = (ns + gs - 1) / gs;
+    const int grp = split / gs;
+    const int gsize = min(gs, ns - grp * gs);
+    int32_t *cnt1 = p.counters1 + unit * p.n_groups_max + grp;
+    if (!arrive_last(cnt1, gsize, s_flag)) return;
+    merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, grp * gs, gsize, row0, rows, D, scratch, nullptr, nullptr,
+               p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, grp);
+    if (threadIdx.x == 0) *cnt1 = 0;
+    if (!arrive_last(p.counters + unit, n_groups, s_flag)) return;
+    merge_rows(p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, 0, n_groups, row0, rows, D, scratch, p.out, p.lse,
+               nullptr, nullptr, nullptr, 0, 0);
+    if (threadIdx.x == 0) p.counters[unit] = 0;
+}
+
+// ---------------- public merge of split triples ----------------
+__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+    extern __shared__ float wsm[];  // [S]
+    __shared__ float s_M, s_L;
+    const int r = blockIdx.x;
+    const float *pm = p.part_m + static_cast<size_t>(r) * p.S;
+    const float *pl = p.part_l + static_cast<size_t>(r) * p.S;
+    if (threadIdx.x < 32) {
+        float M = -CUDART_INF_F;
+        for (int s = threadIdx.x; s < p.S; s += 32) M = fmaxf(M, pm[s]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float Ls = 0.f;
+        for (int s = threadIdx.x; s < p.S; s += 32) {
+            const float w = (M == -CUDART_INF_F || pm[s] == -CUDART_INF_F) ? 0.f : expf(pm[s] - M);
+            wsm[s] = w;
+            Ls = fmaf(w, pl[s], Ls);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+        if (threadIdx.x == 0) {
+            s_M = M;
+            s_L = Ls;
+        }
+    }
+    __syncthreads();
+    const float inv = s_L > 0.f ? 1.f / s_L : 0.f;
+    for (int dq = threadIdx.x; dq < p.D / 4; dq += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < p.S; ++s) {
+            const float w = wsm[s];
+            if (w == 0.f) continue;
+            const float4 v = reinterpret_cast<const float4 *>(p.part_o + (static_cast<size_t>(r) * p.S + s) * p.D)[dq];
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        reinterpret_cast<float4 *>(p.out + static_cast<size_t>(r) * p.D)[dq] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    if (threadIdx.x == 0 && p.lse) p.lse[r] = s_L > 0.f ? s_M + logf(s_L) : -CUDART_INF_F;
+}
+
+constexpr int kMaxDevices = 64;
+
+template <int KT, int VT, int NS>
+cudaError_t configure_t(int dev) {
+    // the dynamic shared-memory opt-in, once per (instance, device)
+    static bool configured[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<KT, VT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<KT, VT, NS>::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <int KT, int VT, int NS>
+cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stream) {
+    using C = Cfg<KT, VT, NS>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = configure_t<KT, VT, NS>(dev);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.n_splits, p.Hkv, p.B * p.QG);
+    decode_kernel<KT, VT, NS><<<grid, C::THREADS, C::SMEM, stream>>>(p, fused ? 1 : 0);
+    return cudaGetLastError();
+}
+
+template <int KT, int VT, int NS>
+cudaError_t occupancy_t(int *ctas) {
+    using C = Cfg<KT, VT, NS>;
+    // resident CTAs per SM, queried once per (instance, device)
+    static int cached[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = configure_t<KT, VT, NS>(dev);
+    if (e != cudaSuccess) return e;
+    if (cached[dev] == 0) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KT, VT, NS>, C::THREADS, C::SMEM);
+        if (e != cudaSuccess) return e;
+        cached[dev] = n > 0 ? n : 1;
+    }
+    *ctas = cached[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+#define KVQ_DISPATCH(KT_, VT_, NS_, CALL)                                  \
+    if (type_k == KT_ && type_v == VT_ && ns == NS_) return CALL<KT_, VT_, NS_>
+#define KVQ_DISPATCH_ALL(CALL, ARGS)                 \
+    KVQ_DISPATCH(KVQ_F16, KVQ_F16, 1, CALL) ARGS;    \
+    KVQ_DISPATCH(KVQ_F16, KVQ_Q8_0, 1, CALL) ARGS;   \
+    KVQ_DISPATCH(KVQ_F16, KVQ_Q4_0, 1, CALL) ARGS;   \
+    KVQ_DISPATCH(KVQ_Q8_0, KVQ_F16, 1, CALL) ARGS;   \
+    KVQ_DISPATCH(KVQ_Q8_0, KVQ_Q8_0, 1, CALL) ARGS;  \
+    KVQ_DISPATCH(KVQ_Q8_0, KVQ_Q4_0, 1, CALL) ARGS;  \
+    KVQ_DISPATCH(KVQ_Q4_0, KVQ_F16, 1, CALL) ARGS;   \
+    KVQ_DISPATCH(KVQ_Q4_0, KVQ_Q8_0, 1, CALL) ARGS;  \
+    KVQ_DISPATCH(KVQ_Q4_0, KVQ_Q4_0, 1, CALL) ARGS;  \
+    KVQ_DISPATCH(KVQ_F16, KVQ_F16, 2, CALL) ARGS;    \
+    KVQ_DISPATCH(KVQ_F16, KVQ_Q8_0, 2, CALL) ARGS;   \
+    KVQ_DISPATCH(KVQ_F16, KVQ_Q4_0, 2, CALL) ARGS;   \
+    KVQ_DISPATCH(KVQ_Q8_0, KVQ_F16, 2, CALL) ARGS;   \
+    KVQ_DISPATCH(KVQ_Q8_0, KVQ_Q8_0, 2, CALL) ARGS;  \
+    KVQ_DISPATCH(KVQ_Q8_0, KVQ_Q4_0, 2, CALL) ARGS;  \
+    KVQ_DISPATCH(KVQ_Q4_0, KVQ_F16, 2, CALL) ARGS;   \
+    KVQ_DISPATCH(KVQ_Q4_0, KVQ_Q8_0, 2, CALL) ARGS;  \
+    KVQ_DISPATCH(KVQ_Q4_0, KVQ_Q4_0, 2, CALL) ARGS;
+
+cudaError_t launch_decode(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream) {
+    const int ns = p.D / kSlice;
+    KVQ_DISPATCH_ALL(launch_decode_t, (p, fused, stream))
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_occupancy(int type_k, int type_v, int D, int *ctas_per_sm, int *n_sms) {
+    static int sm_cache[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (sm_cache[dev] == 0) {
+        e = cudaDeviceGetAttribute(&sm_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    *n_sms = sm_cache[dev];
+    const int ns = D / kSlice;
+    KVQ_DISPATCH_ALL(occupancy_t, (ctas_per_sm))
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
+    const size_t smem = static_cast<size_t>(p.S) * sizeof(float);
+    combine_kernel<<<p.rows, 128, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

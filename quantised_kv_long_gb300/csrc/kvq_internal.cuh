@@ -1,0 +1,150 @@
+// kvq_internal.cuh -- shared definitions of the CUDA path: tile geometry, the
+// fragment-native placement of codes/scales, launch parameter blocks and PTX helpers.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq.h"  // include/ is on the include path
+
+namespace kvq {
+
+constexpr int kTileRows = 16;    // positions per tile
+constexpr int kSlice = 128;      // head-dim values per slice
+constexpr int kBlock = 32;       // values per quantisation block
+constexpr int kScaleTile = 128;  // scale bytes per (tile, slice): 16 rows x 4 blocks x 2 B
+constexpr int kMaxSplits = 1024;
+
+// groups of the two-level split merge: at most ceil(sqrt(n_splits)) groups
+inline int max_merge_groups(int n_splits) {
+    int g = 1;
+    while (g * g < n_splits) ++g;
+    return g + 1;
+}
+constexpr int kMaxRowsPerGroup = 8;  // query heads of one KV head handled per CTA
+
+__host__ __device__ constexpr int code_tile_bytes(int type) {
+    return type == KVQ_Q8_0 ? 2048 : (type == KVQ_Q4_0 ? 1024 : 4096);
+}
+__host__ __device__ constexpr int scale_tile_bytes(int type) { return type == KVQ_F16 ? 0 : kScaleTile; }
+
+// ---- placement inside one (tile, slice); see include/kvq.h for the contract ----
+// pair order of a row inside the 16-row tile: j in [0,4), pos in {A=0,B=1,C=2,D=3}
+__host__ __device__ inline void pair_slot(int kt, int &j, int &pos) {
+    if (kt < 8) {
+        j = kt >> 1;
+        pos = kt & 1;
+    } else {
+        j = (kt - 8) >> 1;
+        pos = 2 + (kt & 1);
+    }
+}
+// byte position of pair member A,B,C,D inside a 4-byte V word (A,C,B,D order)
+__host__ __device__ inline int vword_byte(int pos) { return pos == 0 ? 0 : (pos == 1 ? 2 : (pos == 2 ? 1 : 3)); }
+
+// ---- decode launch parameters ----
+struct DecodeParams {
+    const uint8_t *k_codes, *k_scales, *v_codes, *v_scales;
+    const int32_t *len;   // [B]
+    int32_t *err;         // device error word
+    const float *q;       // [B][Hq][D]
+    float *out, *lse;     // [B][Hq][D], [B][Hq] or nullptr
+    float *part_o, *part_m, *part_l;  // [B][Hq][S][D], [B][Hq][S]
+    int32_t *counters;    // [B][Hkv][QG] (fused mode) or nullptr (partials mode)
+    int32_t *counters1;   // [B][Hkv][QG][n_groups_max]: first-level group arrivals
+    float *grp_o, *grp_m, *grp_l;  // [B][Hq][n_groups_max][D], [B][Hq][n_groups_max]
+    int n_groups_max;
+    int B, Hkv, Hq, G, QG, D;
+    int cap_tiles;
+    int n_splits;
+    float scale_log2;     // scale * log2(e)
+};
+
+struct AppendParams {
+    uint8_t *k_codes, *k_scales, *v_codes, *v_scales;
+    int32_t *len;     // [B]
+    int32_t *ticket;  // one int
+    int32_t *err;
+    const float *k, *v;  // [nb][Hkv][n_new][D]
+    int b0, nb, n_new, Hkv, D, cap, cap_tiles;
+    int total_warps;
+};
+
+struct CombineParams {
+    const float *part_o, *part_m, *part_l;
+    float *out, *lse;
+    int rows, S, D;
+};
+
+// ---- PTX helpers ----
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up after ~kWaitCycles SM clock cycles and returns false.
+constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
+}
+// 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 16-byte shared-memory load (ordinary load: the mbarrier waits carry memory clobbers)
+__device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+}  // namespace kvq
+
+// launchers implemented in the .cu files
+namespace kvq {
+cudaError_t launch_append(int type_k, int type_v, const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_decode(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+cudaError_t decode_occupancy(int type_k, int type_v, int D, int *ctas_per_sm, int *n_sms);
+}  // namespace kvq
