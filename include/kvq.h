@@ -107,7 +107,9 @@ typedef enum {
     KVQ_ERR_CAPACITY = 3,    /* append would exceed capacity (nothing is written)             */
     KVQ_ERR_ALIGNMENT = 4,   /* a pointer is not 16-byte aligned                              */
     KVQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed                          */
-    KVQ_ERR_DEVICE = 6       /* the device error word was set (see kvq_cache_read_error)      */
+    KVQ_ERR_DEVICE = 6,      /* the device error word was set (see kvq_cache_read_error)      */
+    KVQ_ERR_SCRATCH = 7      /* kvq_decode_attention_noalloc: the call needs more scratch than
+                                the library's built-in buffer (KVQ_NOALLOC_SCRATCH_BYTES) has  */
 } kvq_status;
 
 /* Device error word bits (kvq_cache_read_error). */
@@ -207,6 +209,35 @@ KVQ_API kvq_status kvq_decode_partials(const kvq_cache *cache, const float *q, i
 KVQ_API kvq_status kvq_combine(const float *part_o, const float *part_m, const float *part_l,
                        int32_t rows, int32_t n_splits, int32_t head_dim, float *out, float *lse,
                        void *stream);
+
+/*
+ * kvq_decode_attention without a caller-provided workspace.  (The pages have no
+ * counterpart: this entry point exists for callers, not for the method.)
+ *
+ * Some callers cannot allocate device memory at the point where they decode: a plugin
+ * whose host framework hands it only input and output pointers, a serving loop whose
+ * allocator has already reserved every byte of HBM for cache pages, or code that must
+ * not allocate while a CUDA graph is being captured.  This variant takes the same
+ * arguments as kvq_decode_attention minus `workspace`, and uses instead a scratch array
+ * compiled into the library as a file-scope __device__ variable of
+ * KVQ_NOALLOC_SCRATCH_BYTES (8 MiB).  Every GPU on which the library's module is loaded
+ * holds that array until the process exits.  The call itself performs no cudaMalloc,
+ * cudaFree or other allocating call; the caller still passes q, out and lse.
+ *
+ * - The scratch needed is the kvq_decode_workspace_size of the same arguments; larger
+ *   requests return KVQ_ERR_SCRATCH and launch nothing.
+ * - The first call on a device looks up the array's device address for that device
+ *   (cudaGetSymbolAddress, with that device current); make that first call before any
+ *   stream capture.  Later calls only enqueue work.
+ * - All calls share the one array, which keeps the contents of the last call: each call
+ *   clears the arrival counters it relies on (an asynchronous memset on `stream`) before
+ *   its kernel.  Calls that overlap on the GPU (different streams without ordering, or
+ *   several host threads) race on the array and give wrong results.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const float *q, int32_t n_q_heads,
+                                                float scale, int32_t n_splits, float *out, float *lse,
+                                                void *stream);
 
 KVQ_API const char *kvq_status_string(kvq_status status);
 KVQ_API int32_t kvq_abi_version(void);

@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "kvq.h")
 F16, Q8_0, Q4_0 = 0, 1, 2
 TYPE_IDS = {"f16": F16, "q8_0": Q8_0, "q4_0": Q4_0}
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
-          4: "KVQ_ERR_ALIGNMENT", 5: "KVQ_ERR_CUDA", 6: "KVQ_ERR_DEVICE"}
+          4: "KVQ_ERR_ALIGNMENT", 5: "KVQ_ERR_CUDA", 6: "KVQ_ERR_DEVICE", 7: "KVQ_ERR_SCRATCH"}
 DEVERR_CAPACITY, DEVERR_TIMEOUT = 0x1, 0x2
 
 
@@ -56,6 +56,7 @@ def _load():
         "kvq_decode_attention": [vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp],
         "kvq_decode_partials": [vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp],
         "kvq_combine": [vp, vp, vp, i32, i32, i32, vp, vp, vp],
+        "kvq_decode_attention_noalloc": [vp, vp, i32, ctypes.c_float, i32, vp, vp, vp],
     }
     for name, args in sigs.items():
         fn = getattr(L, name)
@@ -202,6 +203,19 @@ class KVCache:
         ws = self.workspace(Hq, n_splits) if workspace is None else workspace
         _check(lib.kvq_decode_attention(self.handle, _ptr(q), Hq, scale, n_splits, _ptr(ws), _ptr(out), _ptr(lse),
                                         _stream(stream)), "kvq_decode_attention")
+        return out, lse
+
+    def decode_noalloc(self, q, scale=None, n_splits=0, out=None, lse=None, stream=None):
+        """Decode through kvq_decode_attention_noalloc: no workspace argument; the library's
+        built-in scratch array is used (see include/kvq.h for its limits)."""
+        assert q.dtype == torch.float32 and q.is_contiguous() and q.dim() == 3
+        B, Hq, D = q.shape
+        assert B == self.batch and D == self.head_dim
+        scale = 1.0 / math.sqrt(D) if scale is None else scale
+        out = torch.empty_like(q) if out is None else out
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+        _check(lib.kvq_decode_attention_noalloc(self.handle, _ptr(q), Hq, scale, n_splits, _ptr(out), _ptr(lse),
+                                                _stream(stream)), "kvq_decode_attention_noalloc")
         return out, lse
 
     def decode_partials(self, q, n_splits, scale=None, stream=None):

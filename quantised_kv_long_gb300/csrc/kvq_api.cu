@@ -2,6 +2,7 @@
 // the host mirror of the lengths and the launches.  No device memory is allocated here.
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "kvq_internal.cuh"
@@ -136,6 +137,7 @@ const char *kvq_status_string(kvq_status s) {
         case KVQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
         case KVQ_ERR_CUDA: return "CUDA error";
         case KVQ_ERR_DEVICE: return "device error word set";
+        case KVQ_ERR_SCRATCH: return "decode needs more scratch than the built-in no-allocation buffer holds";
     }
     return "unknown status";
 }
@@ -344,6 +346,63 @@ kvq_status kvq_combine(const float *part_o, const float *part_m, const float *pa
     if (!aligned16(part_o) || !aligned16(out)) return KVQ_ERR_ALIGNMENT;
     kvq::CombineParams p{part_o, part_m, part_l, out, lse, rows, n_splits, head_dim};
     return cuda_status(kvq::launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+// ---- decode without a caller workspace: scratch compiled into the library ----
+namespace {
+// Shared by every call of kvq_decode_attention_noalloc on a device; see include/kvq.h.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+constexpr int kNoAllocDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_addr[kNoAllocDevices] = {};
+
+// Device address of the scratch array for the current device, looked up once per device.
+kvq_status noalloc_scratch(void **addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocDevices) return KVQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *addr = g_noalloc_addr[dev];
+    return KVQ_OK;
+}
+}  // namespace
+
+kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const float *q, int32_t n_q_heads, float scale,
+                                        int32_t n_splits, float *out, float *lse, void *stream) {
+    if (!cache || !q || !out) return KVQ_ERR_INVALID_ARG;
+    kvq_status st = check_q_heads(cache, n_q_heads);
+    if (st != KVQ_OK) return st;
+    if (n_splits < 0 || n_splits > kvq::kMaxSplits) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return KVQ_ERR_ALIGNMENT;
+    int s = n_splits;
+    if (s == 0 && auto_splits(cache, n_q_heads, &s) != 0) return KVQ_ERR_CUDA;
+    const WsLayout w = ws_layout(cache, n_q_heads, s);
+    if (w.total > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_SCRATCH;
+    void *base = nullptr;
+    st = noalloc_scratch(&base);
+    if (st != KVQ_OK) return st;
+    uint8_t *ws = static_cast<uint8_t *>(base);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the arrival counters of both merge levels must start at zero; the rest is overwritten
+    if (cudaMemsetAsync(ws, 0, w.part_m, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+    kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s);
+    p.out = out;
+    p.lse = lse;
+    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
+    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
+    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
+    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
+    p.n_groups_max = w.n_groups_max;
+    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
+    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
+    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    return cuda_status(kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, cs));
 }
 
 }  // extern "C"
