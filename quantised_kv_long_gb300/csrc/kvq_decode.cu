@@ -104,22 +104,45 @@ __device__ __forceinline__ bool arrive_last(int32_t *counter, int target, int &s
 __device__ void merge_rows(const float *po, const float *pm, const float *pl, int stride, int s0, int NP,
                            size_t row0, int rows, int D, float *scratch, float *out, float *lse, float *qo,
                            float *qm, float *ql, int q_stride, int q_s) {
-    float *wbuf = scratch;                              // [rows][NP]
-    float *Mbuf = scratch + kMaxRowsPerGroup * kMaxMergeWidth;
-    float *Lbuf = Mbuf + kMaxRowsPerGroup;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    // The inputs were written by other CTAs and sit in L2: every phase issues all of its
+    // loads before using any, so a merge costs about three L2 round trips.
+    constexpr int W = kMaxMergeWidth;
+    float *wbuf = scratch;                        // [8][W] weights exp(m_s - M)
+    float *mraw = wbuf + kMaxRowsPerGroup * W;    // [8][W]
+    float *lraw = mraw + kMaxRowsPerGroup * W;    // [8][W]
+    float *Mbuf = lraw + kMaxRowsPerGroup * W;    // [8]
+    float *Lbuf = Mbuf + kMaxRowsPerGroup;        // [8]
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    // (1) all (row, split) maxima and sums, two per thread in flight
+    for (int i0 = tid; i0 < rows * NP; i0 += 2 * nthr) {
+        const int i1 = i0 + nthr;
+        const int g0 = i0 / NP, t0 = i0 % NP, g1 = i1 / NP, t1 = i1 % NP;
+        const bool ok1 = i1 < rows * NP;
+        const float m0 = __ldcg(pm + (row0 + g0) * stride + s0 + t0);
+        const float l0 = __ldcg(pl + (row0 + g0) * stride + s0 + t0);
+        const float m1 = ok1 ? __ldcg(pm + (row0 + g1) * stride + s0 + t1) : 0.f;
+        const float l1 = ok1 ? __ldcg(pl + (row0 + g1) * stride + s0 + t1) : 0.f;
+        mraw[g0 * W + t0] = m0;
+        lraw[g0 * W + t0] = l0;
+        if (ok1) {
+            mraw[g1 * W + t1] = m1;
+            lraw[g1 * W + t1] = l1;
+        }
+    }
+    __syncthreads();
+    // (2) per row: M, weights, L (shared memory only)
     for (int g = warp; g < rows; g += nwarps) {
-        const size_t pr = (row0 + g) * stride + s0;
         float M = -CUDART_INF_F;
-        for (int s = lane; s < NP; s += 32) M = fmaxf(M, __ldcg(pm + pr + s));
+        for (int t = lane; t < NP; t += 32) M = fmaxf(M, mraw[g * W + t]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         float Ls = 0.f;
-        for (int s = lane; s < NP; s += 32) {
-            const float ms = __ldcg(pm + pr + s);
+        for (int t = lane; t < NP; t += 32) {
+            const float ms = mraw[g * W + t];
             const float w = (M == -CUDART_INF_F || ms == -CUDART_INF_F) ? 0.f : expf(ms - M);
-            wbuf[g * kMaxMergeWidth + s] = w;
-            Ls = fmaf(w, __ldcg(pl + pr + s), Ls);
+            wbuf[g * W + t] = w;
+            Ls = fmaf(w, lraw[g * W + t], Ls);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
@@ -129,39 +152,61 @@ __device__ void merge_rows(const float *po, const float *pm, const float *pl, in
         }
     }
     __syncthreads();
+    // (3) weighted sums: two columns per thread, up to 16 splits each, all loads issued first
     const int DQ = D / 4;
-    for (int idx = threadIdx.x; idx < rows * DQ; idx += blockDim.x) {
-        const int g = idx / DQ, dq = idx % DQ;
-        const float4 *src = reinterpret_cast<const float4 *>(po) + ((row0 + g) * stride + s0) * DQ + dq;
-        const float *w = wbuf + g * kMaxMergeWidth;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = 0; c0 < NP; c0 += 8) {
-            // up to eight independent loads in flight per thread, then the weighted sum
-            float4 v[8];
+    const int C = rows * DQ;
+    const float4 *po4 = reinterpret_cast<const float4 *>(po);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = 0; base < C; base += 2 * nthr) {
+        const int c0 = base + tid, c1 = c0 + nthr;
+        const bool v0 = c0 < C, v1 = c1 < C;
+        const int g0 = v0 ? c0 / DQ : 0, q0 = v0 ? c0 % DQ : 0;
+        const int g1 = v1 ? c1 / DQ : 0, q1 = v1 ? c1 % DQ : 0;
+        const float4 *src0 = po4 + ((row0 + g0) * stride + s0) * DQ + q0;
+        const float4 *src1 = po4 + ((row0 + g1) * stride + s0) * DQ + q1;
+        float4 acc0 = z4, acc1 = z4;
+        for (int sc = 0; sc < NP; sc += 16) {
+            float4 a[16], b[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                v[u] = (c0 + u < NP) ? __ldcg(src + (size_t)(c0 + u) * DQ) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = 0; u < 16; ++u) {
+                const bool in = sc + u < NP;
+                a[u] = (v0 && in) ? __ldcg(src0 + (size_t)(sc + u) * DQ) : z4;
+                b[u] = (v1 && in) ? __ldcg(src1 + (size_t)(sc + u) * DQ) : z4;
+            }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float ws = (c0 + u < NP) ? w[c0 + u] : 0.f;
-                acc.x = fmaf(ws, v[u].x, acc.x);
-                acc.y = fmaf(ws, v[u].y, acc.y);
-                acc.z = fmaf(ws, v[u].z, acc.z);
-                acc.w = fmaf(ws, v[u].w, acc.w);
+            for (int u = 0; u < 16; ++u) {
+                const bool in = sc + u < NP;
+                const float w0 = in ? wbuf[g0 * W + sc + u] : 0.f;
+                const float w1 = in ? wbuf[g1 * W + sc + u] : 0.f;
+                acc0.x = fmaf(w0, a[u].x, acc0.x);
+                acc0.y = fmaf(w0, a[u].y, acc0.y);
+                acc0.z = fmaf(w0, a[u].z, acc0.z);
+                acc0.w = fmaf(w0, a[u].w, acc0.w);
+                acc1.x = fmaf(w1, b[u].x, acc1.x);
+                acc1.y = fmaf(w1, b[u].y, acc1.y);
+                acc1.z = fmaf(w1, b[u].z, acc1.z);
+                acc1.w = fmaf(w1, b[u].w, acc1.w);
             }
         }
-        const float Ls = Lbuf[g];
-        if (out) {
-            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-            reinterpret_cast<float4 *>(out + (row0 + g) * D)[dq] =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            if (dq == 0 && lse) lse[row0 + g] = Ls > 0.f ? Mbuf[g] + logf(Ls) : -CUDART_INF_F;
-        } else {
-            const size_t dr = (row0 + g) * static_cast<size_t>(q_stride) + q_s;
-            reinterpret_cast<float4 *>(qo + dr * D)[dq] = acc;
-            if (dq == 0) {
-                qm[dr] = Mbuf[g];
-                ql[dr] = Ls;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const bool v = k == 0 ? v0 : v1;
+            if (!v) continue;
+            const int g = k == 0 ? g0 : g1, dq = k == 0 ? q0 : q1;
+            const float4 acc = k == 0 ? acc0 : acc1;
+            const float Ls = Lbuf[g];
+            if (out) {
+                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                reinterpret_cast<float4 *>(out + (row0 + g) * D)[dq] =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                if (dq == 0 && lse) lse[row0 + g] = Ls > 0.f ? Mbuf[g] + logf(Ls) : -CUDART_INF_F;
+            } else {
+                const size_t dr = (row0 + g) * static_cast<size_t>(q_stride) + q_s;
+                reinterpret_cast<float4 *>(qo + dr * D)[dq] = acc;
+                if (dq == 0) {
+                    qm[dr] = Mbuf[g];
+                    ql[dr] = Ls;
+                }
             }
         }
     }
@@ -169,7 +214,7 @@ __device__ void merge_rows(const float *po, const float *pm, const float *pl, in
 
 template <int KT, int VT, int NS>
 struct Cfg {
-    static constexpr int TW = NS == 1 ? 4 : 2;  // tile-warps (one tile per stage each)
+    static constexpr int TW = NS == 1 ? 4 : 2;  // tile-warps (per 128-value slice)
     static constexpr int CW = TW * NS;         // consumer warps
     static constexpr int THREADS = 32 * (CW + 1);
     static constexpr int KC = code_tile_bytes(KT) * NS;
@@ -177,23 +222,169 @@ struct Cfg {
     static constexpr int KS = scale_tile_bytes(KT) * NS;
     static constexpr int VS = scale_tile_bytes(VT) * NS;
     static constexpr int TILE = KC + VC + KS + VS;
-    static constexpr int STAGE = TW * TILE;
-    static constexpr int MIN_CTAS = 2;  // resident CTAs per SM the register/shared budgets aim at
-    static constexpr int STAGES_RAW = 98304 / STAGE;
+    static constexpr int MIN_CTAS = 2;         // resident CTAs per SM the register/shared budgets aim at
+    static constexpr int RING_BUDGET = 98304;
+    // tiles each warp takes per stage: two (32 keys share one softmax step) when the ring
+    // still holds at least two stages, else one
+    static constexpr int TPW = (2 * 2 * TW * TILE <= RING_BUDGET) ? 2 : 1;
+    static constexpr int TWT = TW * TPW;       // tiles per stage
+    static constexpr int STAGE = TWT * TILE;
+    static constexpr int STAGES_RAW = RING_BUDGET / STAGE;
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 16 ? 16 : STAGES_RAW);
     static constexpr int RING = STAGES * STAGE;
-    static constexpr int XCHG = NS == 2 ? TW * 2 * 2 * 32 * 16 : 0;
+    static constexpr int XCHG = NS == 2 ? TW * 2 * 2 * 32 * 16 * TPW : 0;
     static constexpr int BAR_OFF = RING + XCHG;
     static constexpr int SMEM = BAR_OFF + 2 * STAGES * 8 + 16;
     static constexpr int D = NS * kSlice;
     // merge / combine scratch reuses the ring
     static_assert(TW * kMaxRowsPerGroup * D * 4 + 2 * TW * kMaxRowsPerGroup * 4 <= RING, "merge buffer");
-    static_assert(kMaxRowsPerGroup * (kMaxMergeWidth + 2) * 4 <= RING, "merge scratch");
+    static_assert(kMaxRowsPerGroup * (3 * kMaxMergeWidth + 2) * 4 <= RING, "merge scratch");
 };
+
+// Scores of one tile over this warp's 128-value slice for keys A=2j, B=2j+1 (S-tile 0) and
+// C=8+2j, D=9+2j (S-tile 1), row g = lane/4, in log2 units (Q was prescaled).
+template <int KT>
+__device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks, const uint32_t (&qa)[8][4], int lane,
+                                            int j, float (&s)[4]) {
+    if constexpr (KT == KVQ_F16) {
+        float acc[2][4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint4 w0 = lds128(kc + (2 * b + 0) * 512 + lane * 16);
+            const uint4 w1 = lds128(kc + (2 * b + 1) * 512 + lane * 16);
+            if (b == 0) {
+                mma_16816_z(acc[0], qa[0], w0.x, w0.y);
+                mma_16816_z(acc[1], qa[0], w1.x, w1.y);
+            } else {
+                mma_16816(acc[0], qa[2 * b], w0.x, w0.y);
+                mma_16816(acc[1], qa[2 * b], w1.x, w1.y);
+            }
+            mma_16816(acc[0], qa[2 * b + 1], w0.z, w0.w);
+            mma_16816(acc[1], qa[2 * b + 1], w1.z, w1.w);
+        }
+        s[0] = acc[0][0] + acc[0][2];
+        s[1] = acc[0][1] + acc[0][3];
+        s[2] = acc[1][0] + acc[1][2];
+        s[3] = acc[1][1] + acc[1][3];
+    } else {
+        const uint4 sc0 = lds128(ks + j * 32), sc1 = lds128(ks + j * 32 + 16);
+        const uint32_t kscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
+        s[0] = s[1] = s[2] = s[3] = 0.f;
+        uint4 wq4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float acc[2][4];
+            if constexpr (KT == KVQ_Q8_0) {
+                const uint4 w = lds128(kc + b * 512 + lane * 16);
+                uint32_t x0, x1;
+                cvt_q8(w.x, x0, x1);
+                mma_16816_z(acc[0], qa[2 * b], x0, x1);
+                cvt_q8(w.y, x0, x1);
+                mma_16816(acc[0], qa[2 * b + 1], x0, x1);
+                cvt_q8(w.z, x0, x1);
+                mma_16816_z(acc[1], qa[2 * b], x0, x1);
+                cvt_q8(w.w, x0, x1);
+                mma_16816(acc[1], qa[2 * b + 1], x0, x1);
+            } else {
+                if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
+                const uint32_t w_st0 = (b & 1) ? wq4.z : wq4.x;
+                const uint32_t w_st1 = (b & 1) ? wq4.w : wq4.y;
+                uint32_t l02, l13, h02, h13;
+                cvt_q4(w_st0, l02, l13, h02, h13);
+                mma_16816_z(acc[0], qa[2 * b], l02, l13);
+                mma_16816(acc[0], qa[2 * b + 1], h02, h13);
+                cvt_q4(w_st1, l02, l13, h02, h13);
+                mma_16816_z(acc[1], qa[2 * b], l02, l13);
+                mma_16816(acc[1], qa[2 * b + 1], h02, h13);
+            }
+            const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
+            const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
+            s[0] = fmaf(dab.x, acc[0][0] + acc[0][2], s[0]);
+            s[1] = fmaf(dab.y, acc[0][1] + acc[0][3], s[1]);
+            s[2] = fmaf(dcd.x, acc[1][0] + acc[1][2], s[2]);
+            s[3] = fmaf(dcd.y, acc[1][1] + acc[1][3], s[3]);
+        }
+    }
+}
+
+// O += P V for one tile over this warp's slice.  pk: probabilities of keys A,B,C,D of row g;
+// vmask: which of A,B,C,D are inside the sequence (rows past the length may hold any bits).
+template <int VT>
+__device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, const float (&pk)[4], bool partial,
+                                        const bool (&vmask)[4], int lane, int j, float (&o)[16][4]) {
+    if constexpr (VT == KVQ_F16) {
+        uint32_t a[4];
+        split_hi_lo(pk[0], pk[1], a[0], a[1]);
+        split_hi_lo(pk[2], pk[3], a[2], a[3]);
+        const uint32_t mab = (vmask[0] ? 0x0000ffffu : 0u) | (vmask[1] ? 0xffff0000u : 0u);
+        const uint32_t mcd = (vmask[2] ? 0x0000ffffu : 0u) | (vmask[3] ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            uint4 w0 = lds128(vc + (2 * b + 0) * 512 + lane * 16);
+            uint4 w1 = lds128(vc + (2 * b + 1) * 512 + lane * 16);
+            if (partial) {
+                w0.x &= mab;
+                w0.y &= mcd;
+                w0.z &= mab;
+                w0.w &= mcd;
+                w1.x &= mab;
+                w1.y &= mcd;
+                w1.z &= mab;
+                w1.w &= mcd;
+            }
+            mma_16816(o[4 * b + 0], a, w0.x, w0.y);
+            mma_16816(o[4 * b + 1], a, w0.z, w0.w);
+            mma_16816(o[4 * b + 2], a, w1.x, w1.y);
+            mma_16816(o[4 * b + 3], a, w1.z, w1.w);
+        }
+    } else {
+        const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
+        const uint32_t vscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
+        uint4 wq4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float2 dab = __half22float2(u32_as_h2(vscale[b][0]));
+            float2 dcd = __half22float2(u32_as_h2(vscale[b][1]));
+            if (partial) {
+                dab.x = vmask[0] ? dab.x : 0.f;
+                dab.y = vmask[1] ? dab.y : 0.f;
+                dcd.x = vmask[2] ? dcd.x : 0.f;
+                dcd.y = vmask[3] ? dcd.y : 0.f;
+            }
+            uint32_t a[4];
+            split_hi_lo(pk[0] * dab.x, pk[1] * dab.y, a[0], a[1]);
+            split_hi_lo(pk[2] * dcd.x, pk[3] * dcd.y, a[2], a[3]);
+            if constexpr (VT == KVQ_Q8_0) {
+                const uint4 w = lds128(vc + b * 512 + lane * 16);
+                uint32_t x0, x1;
+                cvt_q8(w.x, x0, x1);
+                mma_16816(o[4 * b + 0], a, x0, x1);
+                cvt_q8(w.y, x0, x1);
+                mma_16816(o[4 * b + 1], a, x0, x1);
+                cvt_q8(w.z, x0, x1);
+                mma_16816(o[4 * b + 2], a, x0, x1);
+                cvt_q8(w.w, x0, x1);
+                mma_16816(o[4 * b + 3], a, x0, x1);
+            } else {
+                if ((b & 1) == 0) wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
+                const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x;  // bytes 2n'   of the block
+                const uint32_t wq1 = (b & 1) ? wq4.w : wq4.y;  // bytes 2n'+1 of the block
+                uint32_t l02, l13, h02, h13;
+                cvt_q4(wq0, l02, l13, h02, h13);
+                mma_16816(o[4 * b + 0], a, l02, l13);
+                mma_16816(o[4 * b + 2], a, h02, h13);
+                cvt_q4(wq1, l02, l13, h02, h13);
+                mma_16816(o[4 * b + 1], a, l02, l13);
+                mma_16816(o[4 * b + 3], a, h02, h13);
+            }
+        }
+    }
+}
 
 template <int KT, int VT, int NS>
 __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
     using C = Cfg<KT, VT, NS>;
+    constexpr int TPW = C::TPW;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_flag;
     __shared__ int s_timeout;
@@ -225,7 +416,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
         return;
     }
     const int t_begin = min(T, split * tps), t_end = min(T, t_begin + tps);
-    const int n_stage = (t_end - t_begin + C::TW - 1) / C::TW;
+    const int n_stage = (t_end - t_begin + C::TWT - 1) / C::TWT;
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
     uint64_t *empty = full + C::STAGES;
@@ -255,25 +446,29 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
 #pragma unroll
             for (int i = 0; i < 16; ++i) issued_use[i] = -1;
             bool ok = true;
-            for (int k = 0; k < n_stage && ok; ++k) {
-                const int slot = k % C::STAGES, use = k / C::STAGES;
+            int slot = 0, use = 0;
+            for (int k = 0; k < n_stage; ++k) {
                 if (use > 0 && !mbar_wait(empty + slot, (use - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                const int t0 = t_begin + k * C::TW;
-                const int nt = min(C::TW, t_end - t0);
+                const int t0 = t_begin + k * C::TWT;
+                const int nt = min(C::TWT, t_end - t0);
                 uint8_t *st = smem + slot * C::STAGE;
                 mbar_arrive_expect_tx(full + slot, static_cast<uint32_t>(nt * C::TILE));
                 bulk_g2s(st, p.k_codes + (bh_tile + t0) * C::KC, nt * C::KC, full + slot);
-                bulk_g2s(st + C::TW * C::KC, p.v_codes + (bh_tile + t0) * C::VC, nt * C::VC, full + slot);
+                bulk_g2s(st + C::TWT * C::KC, p.v_codes + (bh_tile + t0) * C::VC, nt * C::VC, full + slot);
                 if constexpr (C::KS > 0)
-                    bulk_g2s(st + C::TW * (C::KC + C::VC), p.k_scales + (bh_tile + t0) * C::KS, nt * C::KS,
+                    bulk_g2s(st + C::TWT * (C::KC + C::VC), p.k_scales + (bh_tile + t0) * C::KS, nt * C::KS,
                              full + slot);
                 if constexpr (C::VS > 0)
-                    bulk_g2s(st + C::TW * (C::KC + C::VC + C::KS), p.v_scales + (bh_tile + t0) * C::VS, nt * C::VS,
-                             full + slot);
+                    bulk_g2s(st + C::TWT * (C::KC + C::VC + C::KS), p.v_scales + (bh_tile + t0) * C::VS,
+                             nt * C::VS, full + slot);
                 issued_use[slot] = use;
+                if (++slot == C::STAGES) {
+                    slot = 0;
+                    ++use;
+                }
             }
             if (!ok) {
                 atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
@@ -308,119 +503,78 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
         }
         float4 *xchg = reinterpret_cast<float4 *>(smem + C::RING);
         bool dead = false;
+        // keys of this lane inside a tile: A=2j, B=2j+1, C=8+2j, D=9+2j
+        const int kofs[4] = {2 * j, 2 * j + 1, 8 + 2 * j, 9 + 2 * j};
 
+        int slot = 0, use = 0;
         for (int k = 0; k < n_stage; ++k) {
-            const int slot = k % C::STAGES, use = k / C::STAGES;
             if (!dead && !mbar_wait(full + slot, use & 1)) {
                 dead = true;
                 atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
                 s_timeout = 1;
             }
-            const int tile = t_begin + k * C::TW + tw;
-            if (tile < t_end) {
-                const int nvalid = min(kTileRows, L - tile * kTileRows);
+            const int tA = t_begin + (k * C::TW + tw) * TPW;  // first tile of this warp in the stage
+            if (tA < t_end) {
                 const uint8_t *st = smem + slot * C::STAGE;
-                const uint8_t *kc = st + tw * C::KC + sl * code_tile_bytes(KT);
-                const uint8_t *vc = st + C::TW * C::KC + tw * C::VC + sl * code_tile_bytes(VT);
-                const uint8_t *ks = st + C::TW * (C::KC + C::VC) + tw * C::KS + sl * kScaleTile;
-                const uint8_t *vs = st + C::TW * (C::KC + C::VC + C::KS) + tw * C::VS + sl * kScaleTile;
-
-                // ---- S = Q K^T for keys A=2j, B=2j+1 (S-tile 0) and C=8+2j, D=9+2j (S-tile 1) ----
-                float s0, s1, s2, s3;
-                if constexpr (KT == KVQ_F16) {
-                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float sc[TPW][4];
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const uint4 w0 = lds128(kc + (2 * b + 0) * 512 + lane * 16);
-                        const uint4 w1 = lds128(kc + (2 * b + 1) * 512 + lane * 16);
-                        mma_16816(acc[0], qa[2 * b], w0.x, w0.y);
-                        mma_16816(acc[0], qa[2 * b + 1], w0.z, w0.w);
-                        mma_16816(acc[1], qa[2 * b], w1.x, w1.y);
-                        mma_16816(acc[1], qa[2 * b + 1], w1.z, w1.w);
-                    }
-                    s0 = acc[0][0] + acc[0][2];
-                    s1 = acc[0][1] + acc[0][3];
-                    s2 = acc[1][0] + acc[1][2];
-                    s3 = acc[1][1] + acc[1][3];
-                } else {
-                    const uint4 sc0 = lds128(ks + j * 32), sc1 = lds128(ks + j * 32 + 16);
-                    const uint32_t kscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
-                    s0 = s1 = s2 = s3 = 0.f;
-                    uint4 wq4 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                        if constexpr (KT == KVQ_Q8_0) {
-                            const uint4 w = lds128(kc + b * 512 + lane * 16);
-                            uint32_t x0, x1;
-                            cvt_q8(w.x, x0, x1);
-                            mma_16816(acc[0], qa[2 * b], x0, x1);
-                            cvt_q8(w.y, x0, x1);
-                            mma_16816(acc[0], qa[2 * b + 1], x0, x1);
-                            cvt_q8(w.z, x0, x1);
-                            mma_16816(acc[1], qa[2 * b], x0, x1);
-                            cvt_q8(w.w, x0, x1);
-                            mma_16816(acc[1], qa[2 * b + 1], x0, x1);
-                        } else {
-                            if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
-                            const uint32_t w_st0 = (b & 1) ? wq4.z : wq4.x;
-                            const uint32_t w_st1 = (b & 1) ? wq4.w : wq4.y;
-                            uint32_t l02, l13, h02, h13;
-                            cvt_q4(w_st0, l02, l13, h02, h13);
-                            mma_16816(acc[0], qa[2 * b], l02, l13);
-                            mma_16816(acc[0], qa[2 * b + 1], h02, h13);
-                            cvt_q4(w_st1, l02, l13, h02, h13);
-                            mma_16816(acc[1], qa[2 * b], l02, l13);
-                            mma_16816(acc[1], qa[2 * b + 1], h02, h13);
-                        }
-                        const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
-                        const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
-                        s0 = fmaf(dab.x, acc[0][0] + acc[0][2], s0);
-                        s1 = fmaf(dab.y, acc[0][1] + acc[0][3], s1);
-                        s2 = fmaf(dcd.x, acc[1][0] + acc[1][2], s2);
-                        s3 = fmaf(dcd.y, acc[1][1] + acc[1][3], s3);
-                    }
+                for (int t = 0; t < TPW; ++t) {
+                    const int ti = tw * TPW + t;  // tile index inside the stage
+                    tile_scores<KT>(st + ti * C::KC + sl * code_tile_bytes(KT),
+                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * kScaleTile, qa, lane, j, sc[t]);
                 }
                 if constexpr (NS == 2) {
-                    // the two slice-warps of this tile add their partial scores
-                    float4 *mine = xchg + ((tw * 2 + (k & 1)) * 2 + sl) * 32;
-                    float4 *other = xchg + ((tw * 2 + (k & 1)) * 2 + (1 - sl)) * 32;
-                    mine[lane] = make_float4(s0, s1, s2, s3);
+                    // the two slice-warps of this tile pair add their partial scores
+#pragma unroll
+                    for (int t = 0; t < TPW; ++t) {
+                        float4 *mine = xchg + (((tw * 2 + (k & 1)) * 2 + sl) * TPW + t) * 32;
+                        mine[lane] = make_float4(sc[t][0], sc[t][1], sc[t][2], sc[t][3]);
+                    }
                     asm volatile("bar.sync %0, 64;\n" ::"r"(1 + tw) : "memory");
-                    const float4 os = other[lane];
-                    s0 += os.x;
-                    s1 += os.y;
-                    s2 += os.z;
-                    s3 += os.w;
+#pragma unroll
+                    for (int t = 0; t < TPW; ++t) {
+                        const float4 os = xchg[(((tw * 2 + (k & 1)) * 2 + (1 - sl)) * TPW + t) * 32 + lane];
+                        sc[t][0] += os.x;
+                        sc[t][1] += os.y;
+                        sc[t][2] += os.z;
+                        sc[t][3] += os.w;
+                    }
                 }
-                const bool partial = nvalid < kTileRows;
-                bool va = true, vb = true, vcc = true, vd = true;
-                if (partial) {
-                    va = 2 * j < nvalid;
-                    vb = 2 * j + 1 < nvalid;
-                    vcc = 8 + 2 * j < nvalid;
-                    vd = 9 + 2 * j < nvalid;
-                    if (!va) s0 = -CUDART_INF_F;
-                    if (!vb) s1 = -CUDART_INF_F;
-                    if (!vcc) s2 = -CUDART_INF_F;
-                    if (!vd) s3 = -CUDART_INF_F;
+                // rows past the length, and a second tile past this split's range (it belongs
+                // to the next split and was not loaded), are masked out
+                bool partial[TPW], vmask[TPW][4];
+                const int L_split = min(L, t_end * kTileRows);
+#pragma unroll
+                for (int t = 0; t < TPW; ++t) {
+                    const int nvalid = min(kTileRows, max(0, L_split - (tA + t) * kTileRows));
+                    partial[t] = nvalid < kTileRows;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        vmask[t][i] = kofs[i] < nvalid;
+                        if (partial[t] && !vmask[t][i]) sc[t][i] = -CUDART_INF_F;
+                    }
                 }
 
-                // ---- online softmax (log2 units), lazy rescale ----
+                // ---- online softmax (log2 units) over TPW x 16 keys, lazy rescale ----
                 // p = exp2(s - m_run) may reach 2^kTau before the running maximum is moved;
                 // the V scales are checked so that p * scale can never overflow f16.
-                float mt = fmaxf(fmaxf(s0, s1), fmaxf(s2, s3));
+                float mt = -CUDART_INF_F;
+#pragma unroll
+                for (int t = 0; t < TPW; ++t) mt = fmaxf(mt, fmaxf(fmaxf(sc[t][0], sc[t][1]), fmaxf(sc[t][2], sc[t][3])));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
                 bool exact = false;
                 if constexpr (VT != KVQ_F16) {
-                    const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
+                    uint32_t e = 0;
+#pragma unroll
+                    for (int t = 0; t < TPW; ++t) {
+                        const uint8_t *vs = st + C::TWT * (C::KC + C::VC + C::KS) + (tw * TPW + t) * C::VS + sl * kScaleTile;
+                        const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
+                        e |= (sc0.x | sc0.y | sc0.z) | (sc0.w | sc1.x | sc1.y) | (sc1.z | sc1.w);
+                    }
                     // exponent field of any |scale| >= 256 (or inf/nan); an OR may over-report,
-                    // which only costs an exact rescale
-                    const uint32_t e = ((sc0.x | sc0.y | sc0.z) | (sc0.w | sc1.x | sc1.y) | (sc1.z | sc1.w)) & 0x7c007c00u;
-                    exact = __vcmpgeu2(e, 0x5c005c00u) != 0;
-                    // the four lanes of a row must take the same decision: make it warp-wide
-                    exact = __any_sync(0xffffffffu, exact);
+                    // which only costs an exact rescale.  The four lanes of a row must agree.
+                    exact = __any_sync(0xffffffffu, __vcmpgeu2(e & 0x7c007c00u, 0x5c005c00u) != 0);
                 }
                 const bool need = mt > m_run + (exact ? 0.f : kTau);
                 if (__any_sync(0xffffffffu, need)) {
@@ -436,81 +590,29 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                         o[i][3] *= alpha;
                     }
                 }
-                const float p0 = ex2(s0 - m_run), p1 = ex2(s1 - m_run);
-                const float p2 = ex2(s2 - m_run), p3 = ex2(s3 - m_run);
-                l_acc += (p0 + p1) + (p2 + p3);
+                float pk[TPW][4];
+#pragma unroll
+                for (int t = 0; t < TPW; ++t) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) pk[t][i] = ex2(sc[t][i] - m_run);
+                    l_acc += (pk[t][0] + pk[t][1]) + (pk[t][2] + pk[t][3]);
+                }
 
                 // ---- O += P V ----
-                if constexpr (VT == KVQ_F16) {
-                    uint32_t a[4];
-                    split_hi_lo(p0, p1, a[0], a[1]);
-                    split_hi_lo(p2, p3, a[2], a[3]);
-                    const uint32_t mab = (va ? 0x0000ffffu : 0u) | (vb ? 0xffff0000u : 0u);
-                    const uint32_t mcd = (vcc ? 0x0000ffffu : 0u) | (vd ? 0xffff0000u : 0u);
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        uint4 w0 = lds128(vc + (2 * b + 0) * 512 + lane * 16);
-                        uint4 w1 = lds128(vc + (2 * b + 1) * 512 + lane * 16);
-                        if (partial) {  // rows past the length may hold any bits (NaN)
-                            w0.x &= mab;
-                            w0.y &= mcd;
-                            w0.z &= mab;
-                            w0.w &= mcd;
-                            w1.x &= mab;
-                            w1.y &= mcd;
-                            w1.z &= mab;
-                            w1.w &= mcd;
-                        }
-                        mma_16816(o[4 * b + 0], a, w0.x, w0.y);
-                        mma_16816(o[4 * b + 1], a, w0.z, w0.w);
-                        mma_16816(o[4 * b + 2], a, w1.x, w1.y);
-                        mma_16816(o[4 * b + 3], a, w1.z, w1.w);
-                    }
-                } else {
-                    const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
-                    const uint32_t vscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
-                    uint4 wq4 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        float2 dab = __half22float2(u32_as_h2(vscale[b][0]));
-                        float2 dcd = __half22float2(u32_as_h2(vscale[b][1]));
-                        if (partial) {  // scales past the length may hold any bits
-                            dab.x = va ? dab.x : 0.f;
-                            dab.y = vb ? dab.y : 0.f;
-                            dcd.x = vcc ? dcd.x : 0.f;
-                            dcd.y = vd ? dcd.y : 0.f;
-                        }
-                        uint32_t a[4];
-                        split_hi_lo(p0 * dab.x, p1 * dab.y, a[0], a[1]);
-                        split_hi_lo(p2 * dcd.x, p3 * dcd.y, a[2], a[3]);
-                        if constexpr (VT == KVQ_Q8_0) {
-                            const uint4 w = lds128(vc + b * 512 + lane * 16);
-                            uint32_t x0, x1;
-                            cvt_q8(w.x, x0, x1);
-                            mma_16816(o[4 * b + 0], a, x0, x1);
-                            cvt_q8(w.y, x0, x1);
-                            mma_16816(o[4 * b + 1], a, x0, x1);
-                            cvt_q8(w.z, x0, x1);
-                            mma_16816(o[4 * b + 2], a, x0, x1);
-                            cvt_q8(w.w, x0, x1);
-                            mma_16816(o[4 * b + 3], a, x0, x1);
-                        } else {
-                            if ((b & 1) == 0) wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
-                            const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x;  // bytes 2n'   of the block
-                            const uint32_t wq1 = (b & 1) ? wq4.w : wq4.y;  // bytes 2n'+1 of the block
-                            uint32_t l02, l13, h02, h13;
-                            cvt_q4(wq0, l02, l13, h02, h13);
-                            mma_16816(o[4 * b + 0], a, l02, l13);
-                            mma_16816(o[4 * b + 2], a, h02, h13);
-                            cvt_q4(wq1, l02, l13, h02, h13);
-                            mma_16816(o[4 * b + 1], a, l02, l13);
-                            mma_16816(o[4 * b + 3], a, h02, h13);
-                        }
-                    }
+                for (int t = 0; t < TPW; ++t) {
+                    const int ti = tw * TPW + t;
+                    tile_pv<VT>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
+                                st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t], partial[t],
+                                vmask[t], lane, j, o);
                 }
             }
             __syncwarp();
             if (lane == 0 && !dead) mbar_arrive(empty + slot);
+            if (++slot == C::STAGES) {
+                slot = 0;
+                ++use;
+            }
         }
         // row sums over the four lanes of a row
         l_acc += __shfl_xor_sync(0xffffffffu, l_acc, 1);
