@@ -2,8 +2,8 @@
 """Decode-attention benchmark over the block-quantised KV cache (one JSON line on stdout).
 
 A step is one pass of the whole hot path over one batch: for every layer, quantise-on-
-append of the new K/V row of each sequence, then split-K decode attention with its fused
-split merge.  Each step is one CUDA-graph replay (2 kernels per layer).  Inputs are
+append of the new K/V row of each sequence, then split-K decode attention with its split
+merge, all in one kernel per layer (kvq_append_decode).  Each step is one CUDA-graph replay.  Inputs are
 seeded synthetic tensors shaped like the pages' models (see synthetic.py); caches are
 filled and resident in HBM before the timed region starts.
 
@@ -181,11 +181,11 @@ class Cell:
     def launch_step(self, events=None):
         """Enqueue one step (append + decode per layer) on self.stream."""
         for layer, c in enumerate(self.caches):
-            c.append(self.knew[layer], self.vnew[layer], stream=self.stream)
             if events is not None:
                 events[layer][0].record(self.stream)
-            c.decode(self.q[layer], scale=self.wl.scale, n_splits=self.splits, out=self.out[layer],
-                     lse=self.lse[layer], workspace=self.ws, stream=self.stream)
+            c.append_decode(self.knew[layer], self.vnew[layer], self.q[layer], scale=self.wl.scale,
+                            n_splits=self.splits, out=self.out[layer], lse=self.lse[layer], workspace=self.ws,
+                            stream=self.stream)
             if events is not None:
                 events[layer][1].record(self.stream)
 
@@ -538,7 +538,7 @@ def main():
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": (achieved / peak) if achieved else None, "traffic": traffic_from_profiles(wl),
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6800 GB/s", "kernel": "decode_kernel (split-K decode + fused split merge)",
+            else "fallback 6800 GB/s", "kernel": "decode_kernel, fused-append mode (1-row quantise-append + split-K decode + split merge)",
             "bytes_per_launch": step_kv_bytes(wl, [wl.lengths[0]]) / wl.layers,
             "per_unit": f"{row_bytes(wl):.0f} B per (position, layer): Hkv*D*(bpv_K+bpv_V)"}
     e2e = head.pop("e2e")
@@ -551,10 +551,11 @@ def main():
                    "kv": f"{wl.type_k}/{wl.type_v}", "steps_per_s": head["steps_per_s"],
                    "pct_hbm_peak": head["pct_hbm_peak"], "splits": head["splits"],
                    "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",
-                   "step": "per layer: 1-row quantise-append + split-K decode with fused merge; one CUDA graph",
+                   "step": "per layer: one kernel = 1-row quantise-append + split-K decode + split merge; "
+                           "the layers of a step form one CUDA graph",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 2 * wl.layers * args.steps, "clocks": clocks,
+        "gpu_launches": wl.layers * args.steps, "clocks": clocks,
         "sweep": sweep, "chunk_quantise": chunk,
     }
     print(json.dumps(line), flush=True)

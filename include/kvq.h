@@ -187,6 +187,22 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_cache *cache, const float *q, 
                                 float *lse, void *stream);
 
 /*
+ * One decode step of the hot path in one launch: quantise-on-append of one new K/V row per
+ * sequence (k_new, v_new: fp32 [B][Hkv][D]) at position len[b], then split-K decode
+ * attention over len[b] + 1 rows (the new row included), then len[b] += 1 on the device.
+ * Arguments and workspace as kvq_decode_attention.  The CTA whose key range holds the new
+ * row quantises it (same rules and layout as kvq_quantize_append) before reading that
+ * tile, so the row is written exactly once; when more than 8 query heads share a KV head
+ * the call falls back to kvq_quantize_append followed by kvq_decode_attention.  Returns
+ * KVQ_ERR_CAPACITY (nothing launched) if the host mirror shows a full sequence; a full
+ * sequence seen only on the device is attended without the new row, not advanced, and
+ * sets KVQ_DEVERR_CAPACITY.
+ */
+KVQ_API kvq_status kvq_append_decode(kvq_cache *cache, const float *k_new, const float *v_new, const float *q,
+                                     int32_t n_q_heads, float scale, int32_t n_splits, void *workspace,
+                                     float *out, float *lse, void *stream);
+
+/*
  * Same split attention, but writes the unnormalised split triples instead of merging
  * them: part_o fp32 [B][Hq][n_splits][D] = sum_t exp(s_t - m) v_hat_t over the split,
  * part_m [B][Hq][n_splits] = max_t s_t (natural units), part_l = sum_t exp(s_t - m).

@@ -57,6 +57,7 @@ def _load():
         "kvq_decode_partials": [vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp],
         "kvq_combine": [vp, vp, vp, i32, i32, i32, vp, vp, vp],
         "kvq_decode_attention_noalloc": [vp, vp, i32, ctypes.c_float, i32, vp, vp, vp],
+        "kvq_append_decode": [vp, vp, vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp],
     }
     for name, args in sigs.items():
         fn = getattr(L, name)
@@ -203,6 +204,23 @@ class KVCache:
         ws = self.workspace(Hq, n_splits) if workspace is None else workspace
         _check(lib.kvq_decode_attention(self.handle, _ptr(q), Hq, scale, n_splits, _ptr(ws), _ptr(out), _ptr(lse),
                                         _stream(stream)), "kvq_decode_attention")
+        return out, lse
+
+    def append_decode(self, k_new, v_new, q, scale=None, n_splits=0, out=None, lse=None, workspace=None,
+                      stream=None):
+        """One decode step: quantise-append k_new, v_new fp32 [B, Hkv, 1, D] (one row per
+        sequence), then attend q fp32 [B, Hq, D] over the cache including them."""
+        for t in (k_new, v_new, q):
+            assert t.dtype == torch.float32 and t.is_contiguous()
+        assert k_new.shape == v_new.shape and k_new.numel() == self.batch * self.n_kv_heads * self.head_dim
+        B, Hq, D = q.shape
+        assert B == self.batch and D == self.head_dim
+        scale = 1.0 / math.sqrt(D) if scale is None else scale
+        out = torch.empty_like(q) if out is None else out
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+        ws = self.workspace(Hq, n_splits) if workspace is None else workspace
+        _check(lib.kvq_append_decode(self.handle, _ptr(k_new), _ptr(v_new), _ptr(q), Hq, scale, n_splits, _ptr(ws),
+                                     _ptr(out), _ptr(lse), _stream(stream)), "kvq_append_decode")
         return out, lse
 
     def decode_noalloc(self, q, scale=None, n_splits=0, out=None, lse=None, stream=None):

@@ -323,6 +323,51 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const float *q, int32_t 
         kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, static_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_append_decode(kvq_cache *cache, const float *k_new, const float *v_new, const float *q,
+                             int32_t n_q_heads, float scale, int32_t n_splits, void *workspace, float *out, float *lse,
+                             void *stream) {
+    if (!cache || !k_new || !v_new || !q || !workspace || !out) return KVQ_ERR_INVALID_ARG;
+    kvq_status st = check_q_heads(cache, n_q_heads);
+    if (st != KVQ_OK) return st;
+    if (n_splits < 0 || n_splits > kvq::kMaxSplits) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out) || !aligned16(workspace) ||
+        (lse && !aligned16(lse)))
+        return KVQ_ERR_ALIGNMENT;
+    for (int i = 0; i < cache->desc.batch; ++i)
+        if (static_cast<long long>(cache->h_len[i]) + 1 > cache->desc.capacity) return KVQ_ERR_CAPACITY;
+    const int G = n_q_heads / cache->desc.n_kv_heads;
+    if (G > kvq::kMaxRowsPerGroup) {
+        // several CTAs per KV head would read the new row: write it first, then attend
+        st = kvq_quantize_append(cache, k_new, v_new, 0, cache->desc.batch, 1, stream);
+        if (st != KVQ_OK) return st;
+        return kvq_decode_attention(cache, q, n_q_heads, scale, n_splits, workspace, out, lse, stream);
+    }
+    int s = n_splits;
+    if (s == 0 && auto_splits(cache, n_q_heads, &s) != 0) return KVQ_ERR_CUDA;
+    const WsLayout w = ws_layout(cache, n_q_heads, s);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s);
+    p.out = out;
+    p.lse = lse;
+    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
+    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
+    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
+    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
+    p.n_groups_max = w.n_groups_max;
+    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
+    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
+    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.ticket = cache->state + cache->desc.batch;
+    cudaError_t e =
+        kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    for (int i = 0; i < cache->desc.batch; ++i) cache->h_len[i] += 1;
+    return KVQ_OK;
+}
+
 kvq_status kvq_decode_partials(const kvq_cache *cache, const float *q, int32_t n_q_heads, float scale,
                                int32_t n_splits, float *part_o, float *part_m, float *part_l, void *stream) {
     if (!cache || !q || !part_o || !part_m || !part_l) return KVQ_ERR_INVALID_ARG;

@@ -212,6 +212,25 @@ __device__ void merge_rows(const float *po, const float *pm, const float *pl, in
     }
 }
 
+// Fused append: every CTA of the grid arrives once, after it has read the lengths; the
+// last one advances len[b] by one for each sequence that had room (else it reports
+// KVQ_DEVERR_CAPACITY) and resets the ticket.  Called by one thread per CTA.
+__device__ __noinline__ void grid_ticket(const DecodeParams &p, int cap_rows) {
+    __threadfence();
+    const int total = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
+    if (atomicAdd(p.ticket, 1) != total - 1) return;
+    __threadfence();
+    int32_t *len = const_cast<int32_t *>(p.len);
+    for (int b = 0; b < p.B; ++b) {
+        const int Lb = __ldcg(len + b);
+        if (Lb >= 0 && Lb + 1 <= cap_rows)
+            len[b] = Lb + 1;
+        else
+            atomicOr(p.err, KVQ_DEVERR_CAPACITY);
+    }
+    *p.ticket = 0;
+}
+
 template <int KT, int VT, int NS>
 struct Cfg {
     static constexpr int TW = NS == 1 ? 4 : 2;  // tile-warps (per 128-value slice)
@@ -393,8 +412,12 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     const int split = blockIdx.x, h = blockIdx.y;
     const int bseq = blockIdx.z / p.QG, qg = blockIdx.z % p.QG;
     const int cap_rows = p.cap_tiles * kTileRows;
-    int L = __ldcg(p.len + bseq);
-    L = L < 0 ? 0 : (L > cap_rows ? cap_rows : L);
+    int L_old = __ldcg(p.len + bseq);
+    L_old = L_old < 0 ? 0 : (L_old > cap_rows ? cap_rows : L_old);
+    // fused append: the new row lands at position L_old and is attended to
+    const bool appending = p.k_new != nullptr;
+    const bool do_app = appending && L_old + 1 <= cap_rows;
+    const int L = do_app ? L_old + 1 : L_old;
     const int T = (L + kTileRows - 1) / kTileRows;
     const int ns = max(1, min(p.n_splits, T));
     const int tps = T > 0 ? (T + ns - 1) / ns : 0;
@@ -402,6 +425,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     const int hq0 = h * p.G + qg * kMaxRowsPerGroup;  // first query head of this CTA
 
     if (split >= ns) {
+        if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
         if (!fused) {  // partials mode: splits beyond ns are empty triples
             for (int idx = threadIdx.x; idx < rows * (p.D / 4); idx += blockDim.x) {
                 const int g = idx / (p.D / 4), dq = idx % (p.D / 4);
@@ -441,17 +465,41 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
 
     if (warp == 0) {
         // ---------------- producer ----------------
-        if (lane == 0) {
-            int issued_use[16];
+        // In fused-append mode the CTA whose split holds the last tile first writes the new
+        // row of its KV head into that tile (all 32 lanes quantise), then copies it in.
+        const bool owner = do_app && t_begin < T && t_end == T;
+        const int app_stage = owner ? (T - 1 - t_begin) / C::TWT : -1;
+        int issued_use[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) issued_use[i] = -1;
-            bool ok = true;
-            int slot = 0, use = 0;
-            for (int k = 0; k < n_stage; ++k) {
-                if (use > 0 && !mbar_wait(empty + slot, (use - 1) & 1)) {
-                    ok = false;
-                    break;
+        for (int i = 0; i < 16; ++i) issued_use[i] = -1;
+        bool ok = true;
+        int slot = 0, use = 0;
+        for (int k = 0; k < n_stage; ++k) {
+            bool ok_k = true;
+            if (lane == 0 && use > 0) ok_k = mbar_wait(empty + slot, (use - 1) & 1);
+            if (!__shfl_sync(0xffffffffu, ok_k ? 1 : 0, 0)) {
+                ok = false;
+                break;
+            }
+            if (k == app_stage) {
+                const size_t tile = bh_tile + (L_old >> 4);
+                const int kt = L_old & 15;
+                const float *kx = p.k_new + (static_cast<size_t>(bseq) * p.Hkv + h) * p.D;
+                const float *vx = p.v_new + (static_cast<size_t>(bseq) * p.Hkv + h) * p.D;
+#pragma unroll
+                for (int s2 = 0; s2 < NS; ++s2) {
+                    quantize_store<KT, false>(kx + s2 * kSlice + 4 * lane,
+                                              const_cast<uint8_t *>(p.k_codes) + tile * C::KC + s2 * code_tile_bytes(KT),
+                                              const_cast<uint8_t *>(p.k_scales) + tile * C::KS + s2 * kScaleTile, kt, lane);
+                    quantize_store<VT, true>(vx + s2 * kSlice + 4 * lane,
+                                             const_cast<uint8_t *>(p.v_codes) + tile * C::VC + s2 * code_tile_bytes(VT),
+                                             const_cast<uint8_t *>(p.v_scales) + tile * C::VS + s2 * kScaleTile, kt, lane);
                 }
+                // order these generic-proxy stores before the bulk copy (async proxy) that reads them
+                asm volatile("fence.proxy.async.global;\n" ::: "memory");
+                __syncwarp();
+            }
+            if (lane == 0) {
                 const int t0 = t_begin + k * C::TWT;
                 const int nt = min(C::TWT, t_end - t0);
                 uint8_t *st = smem + slot * C::STAGE;
@@ -465,18 +513,19 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                     bulk_g2s(st + C::TWT * (C::KC + C::VC + C::KS), p.v_scales + (bh_tile + t0) * C::VS,
                              nt * C::VS, full + slot);
                 issued_use[slot] = use;
-                if (++slot == C::STAGES) {
-                    slot = 0;
-                    ++use;
-                }
             }
-            if (!ok) {
-                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
-                s_timeout = 1;
-                // let the copies already issued land before the CTA can exit
-                for (int i = 0; i < C::STAGES; ++i)
-                    if (issued_use[i] >= 0) (void)mbar_wait(full + i, issued_use[i] & 1);
+            __syncwarp();
+            if (++slot == C::STAGES) {
+                slot = 0;
+                ++use;
             }
+        }
+        if (!ok && lane == 0) {
+            atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
+            s_timeout = 1;
+            // let the copies already issued land before the CTA can exit
+            for (int i = 0; i < C::STAGES; ++i)
+                if (issued_use[i] >= 0) (void)mbar_wait(full + i, issued_use[i] & 1);
         }
     } else {
         // ---------------- consumers ----------------
@@ -621,6 +670,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
 
     // ---------------- merge the tile-warps of this CTA ----------------
     __syncthreads();  // the ring is free from here on
+    if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
     constexpr int D = C::D;
     float *Ob = reinterpret_cast<float *>(smem);                    // [TW][8][D]
     float *mb = Ob + C::TW * kMaxRowsPerGroup * D;                 // [TW][8]

@@ -384,3 +384,102 @@ def test_full_size_sampled(kvq, which):
         err = np.abs(out[b, hq].cpu().numpy() - ref[0]).max()
         assert err <= TOL, (b, hq, err)
         assert abs(float(lse[b, hq]) - ref_lse[0]) <= TOL
+
+
+@pytest.mark.parametrize("tk,tv", [("q8_0", "q8_0"), ("q8_0", "q4_0"), ("q4_0", "q4_0"), ("f16", "f16"), ("f16", "q4_0")])
+@pytest.mark.parametrize("D,G", [(128, 5), (256, 8), (128, 12)])
+def test_append_decode_fused_steps(kvq, tk, tv, D, G):
+    """kvq_append_decode: one launch appends one row per sequence and attends over it.
+    Codes of every row (old and appended) are bit-exact; outputs match the oracle."""
+    H = 2
+    lens = [300, 17, 48]
+    B = len(lens)
+    wl = syn.Workload("fused", 1, B, H * G, H, D, tk, tv, tuple(lens), seed=G + D)
+    steps = 3
+    cap = 320
+    cache = kvq.KVCache(B, H, D, cap, tk, tv)
+    Ks = [torch.stack([syn.kv_rows(wl, syn.KIND_K, 0, b, h, 0, lens[b] + steps) for h in range(H)]) for b in range(B)]
+    Vs = [torch.stack([syn.kv_rows(wl, syn.KIND_V, 0, b, h, 0, lens[b] + steps) for h in range(H)]) for b in range(B)]
+    for b in range(B):
+        cache.append(Ks[b][None, :, :lens[b]].contiguous(), Vs[b][None, :, :lens[b]].contiguous(), b0=b)
+    for step in range(steps):
+        kn = torch.stack([Ks[b][:, lens[b] + step] for b in range(B)])[:, :, None].contiguous()
+        vn = torch.stack([Vs[b][:, lens[b] + step] for b in range(B)])[:, :, None].contiguous()
+        q = syn.queries(wl, 0, step=step)
+        out, lse = cache.append_decode(kn, vn, q, scale=wl.scale)
+        torch.cuda.synchronize()
+        assert cache.lengths() == [n + step + 1 for n in lens]
+        qh = q.cpu().numpy()
+        for b in range(B):
+            n = lens[b] + step + 1
+            kc, ks = oracle.quantize(tk, Ks[b][:, :n].cpu().numpy())
+            vc, vs = oracle.quantize(tv, Vs[b][:, :n].cpu().numpy())
+            ref, ref_lse = oracle.attention(tk, kc, ks, tv, vc, vs, n, qh[b], wl.scale)
+            assert np.abs(out[b].cpu().numpy() - ref).max() <= TOL, (step, b)
+            assert np.abs(lse[b].cpu().numpy() - ref_lse).max() <= TOL
+    assert cache.sync_lengths() == [n + steps for n in lens]
+    assert cache.read_error() == 0
+    kc, ksc, vc, vsc = read_natural(cache)
+    for b in range(B):
+        n = lens[b] + steps
+        ok_c, ok_s = oracle.quantize(tk, Ks[b][:, :n].cpu().numpy())
+        ov_c, ov_s = oracle.quantize(tv, Vs[b][:, :n].cpu().numpy())
+        assert np.array_equal(kc[b, :, :n], ok_c) and np.array_equal(ksc[b, :, :n], ok_s)
+        assert np.array_equal(vc[b, :, :n], ov_c) and np.array_equal(vsc[b, :, :n], ov_s)
+
+
+def test_append_decode_capacity(kvq):
+    H, D, G = 2, 128, 4
+    cache = kvq.KVCache(2, H, D, 32, "q8_0", "q4_0")
+    x = torch.randn((1, H, 32, D), device="cuda")
+    cache.append(x, x, b0=0)                               # sequence 0 is full
+    cache.append(x[:, :, :5].contiguous(), x[:, :, :5].contiguous(), b0=1)
+    kn = torch.randn((2, H, 1, D), device="cuda")
+    q = torch.randn((2, H * G, D), device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        cache.append_decode(kn, kn, q)
+    assert e.value.status == 3
+    assert cache.sync_lengths() == [32, 5]
+    # full only on the device: that sequence is attended without the new row and not advanced
+    cache.state[0] = 31
+    cache.sync_lengths()
+    cache.state[0] = 32
+    out, _ = cache.append_decode(kn, kn, q)
+    torch.cuda.synchronize()
+    assert cache.read_error() == kvq.DEVERR_CAPACITY
+    assert cache.sync_lengths() == [32, 6]
+
+
+def test_append_decode_graph_replay(kvq):
+    H, D, G = 2, 256, 8
+    wl = syn.Workload("gf", 1, 1, H * G, H, D, "q8_0", "q8_0", (200,), seed=8)
+    cache = kvq.KVCache(1, H, D, 224, "q8_0", "q8_0")
+    K = torch.stack([syn.kv_rows(wl, syn.KIND_K, 0, 0, h, 0, 204) for h in range(H)])[None].contiguous()
+    V = torch.stack([syn.kv_rows(wl, syn.KIND_V, 0, 0, h, 0, 204) for h in range(H)])[None].contiguous()
+    cache.append(K[:, :, :200].contiguous(), V[:, :, :200].contiguous())
+    q = syn.queries(wl, 0)
+    kn = torch.empty((1, H, 1, D), device="cuda")
+    vn = torch.empty((1, H, 1, D), device="cuda")
+    S = cache.auto_splits(H * G)
+    ws = cache.workspace(H * G, S)
+    out = torch.empty_like(q)
+    lse = torch.empty((1, H * G), device="cuda")
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        cache.append_decode(kn, vn, q, n_splits=S, out=out, lse=lse, workspace=ws, stream=st)
+    torch.cuda.synchronize()
+    assert cache.sync_lengths() == [200]
+    qh = q.cpu().numpy()
+    for step in range(4):
+        kn.copy_(K[:, :, 200 + step:201 + step])
+        vn.copy_(V[:, :, 200 + step:201 + step])
+        g.replay()
+        torch.cuda.synchronize()
+        n = 201 + step
+        assert cache.sync_lengths() == [n]
+        kc, ks = oracle.quantize("q8_0", K[0, :, :n].cpu().numpy())
+        vc, vs = oracle.quantize("q8_0", V[0, :, :n].cpu().numpy())
+        ref, _ = oracle.attention("q8_0", kc, ks, "q8_0", vc, vs, n, qh[0], wl.scale)
+        assert np.abs(out[0].cpu().numpy() - ref).max() <= TOL
