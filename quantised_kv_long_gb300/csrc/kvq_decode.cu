@@ -233,7 +233,7 @@ __device__ __noinline__ void grid_ticket(const DecodeParams &p, int cap_rows) {
 
 template <int KT, int VT, int NS>
 struct Cfg {
-    static constexpr int TW = NS == 1 ? 4 : 2;  // tile-warps (per 128-value slice)
+    static constexpr int TW = NS == 1 ? 8 : 4;  // tile-warps (per 128-value slice)
     static constexpr int CW = TW * NS;         // consumer warps
     static constexpr int THREADS = 32 * (CW + 1);
     static constexpr int KC = code_tile_bytes(KT) * NS;
@@ -241,8 +241,8 @@ struct Cfg {
     static constexpr int KS = scale_tile_bytes(KT) * NS;
     static constexpr int VS = scale_tile_bytes(VT) * NS;
     static constexpr int TILE = KC + VC + KS + VS;
-    static constexpr int MIN_CTAS = 2;         // resident CTAs per SM the register/shared budgets aim at
-    static constexpr int RING_BUDGET = 98304;
+    static constexpr int MIN_CTAS = 1;         // one CTA per SM: 8 consumer warps + 1 producer
+    static constexpr int RING_BUDGET = 196608;
     // tiles each warp takes per stage: two (32 keys share one softmax step) when the ring
     // still holds at least two stages, else one
     static constexpr int TPW = (2 * 2 * TW * TILE <= RING_BUDGET) ? 2 : 1;
@@ -328,8 +328,8 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
 
 // O += P V for one tile over this warp's slice.  pk: probabilities of keys A,B,C,D of row g;
 // vmask: which of A,B,C,D are inside the sequence (rows past the length may hold any bits).
-template <int VT>
-__device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, const float (&pk)[4], bool partial,
+template <int VT, bool PARTIAL>
+__device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, const float (&pk)[4],
                                         const bool (&vmask)[4], int lane, int j, float (&o)[16][4]) {
     if constexpr (VT == KVQ_F16) {
         uint32_t a[4];
@@ -341,7 +341,7 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
         for (int b = 0; b < 4; ++b) {
             uint4 w0 = lds128(vc + (2 * b + 0) * 512 + lane * 16);
             uint4 w1 = lds128(vc + (2 * b + 1) * 512 + lane * 16);
-            if (partial) {
+            if constexpr (PARTIAL) {
                 w0.x &= mab;
                 w0.y &= mcd;
                 w0.z &= mab;
@@ -364,7 +364,7 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
         for (int b = 0; b < 4; ++b) {
             float2 dab = __half22float2(u32_as_h2(vscale[b][0]));
             float2 dcd = __half22float2(u32_as_h2(vscale[b][1]));
-            if (partial) {
+            if constexpr (PARTIAL) {  // scales past the length may hold any bits
                 dab.x = vmask[0] ? dab.x : 0.f;
                 dab.y = vmask[1] ? dab.y : 0.f;
                 dcd.x = vmask[2] ? dcd.x : 0.f;
@@ -412,6 +412,11 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     const int split = blockIdx.x, h = blockIdx.y;
     const int bseq = blockIdx.z / p.QG, qg = blockIdx.z % p.QG;
     const int cap_rows = p.cap_tiles * kTileRows;
+    // Programmatic dependent launch: let the next kernel of the stream get scheduled as SMs
+    // free up, then wait for every earlier kernel (lengths, queries, new rows and cache
+    // tiles may all have been written by it) before touching global memory.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     int L_old = __ldcg(p.len + bseq);
     L_old = L_old < 0 ? 0 : (L_old > cap_rows ? cap_rows : L_old);
     // fused append: the new row lands at position L_old and is attended to
@@ -591,17 +596,24 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 }
                 // rows past the length, and a second tile past this split's range (it belongs
                 // to the next split and was not loaded), are masked out
-                bool partial[TPW], vmask[TPW][4];
+                bool vmask[TPW][4];
                 const int L_split = min(L, t_end * kTileRows);
+                const bool any_partial = (tA + TPW) * kTileRows > L_split;  // warp-uniform
+                if (any_partial) {
 #pragma unroll
-                for (int t = 0; t < TPW; ++t) {
-                    const int nvalid = min(kTileRows, max(0, L_split - (tA + t) * kTileRows));
-                    partial[t] = nvalid < kTileRows;
+                    for (int t = 0; t < TPW; ++t) {
+                        const int nvalid = min(kTileRows, max(0, L_split - (tA + t) * kTileRows));
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        vmask[t][i] = kofs[i] < nvalid;
-                        if (partial[t] && !vmask[t][i]) sc[t][i] = -CUDART_INF_F;
+                        for (int i = 0; i < 4; ++i) {
+                            vmask[t][i] = kofs[i] < nvalid;
+                            if (!vmask[t][i]) sc[t][i] = -CUDART_INF_F;
+                        }
                     }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < TPW; ++t)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) vmask[t][i] = true;
                 }
 
                 // ---- online softmax (log2 units) over TPW x 16 keys, lazy rescale ----
@@ -647,13 +659,23 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                     l_acc += (pk[t][0] + pk[t][1]) + (pk[t][2] + pk[t][3]);
                 }
 
-                // ---- O += P V ----
+                // ---- O += P V (masking code only for the rare tile that crosses the end) ----
+                if (!any_partial) {
 #pragma unroll
-                for (int t = 0; t < TPW; ++t) {
-                    const int ti = tw * TPW + t;
-                    tile_pv<VT>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
-                                st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t], partial[t],
-                                vmask[t], lane, j, o);
+                    for (int t = 0; t < TPW; ++t) {
+                        const int ti = tw * TPW + t;
+                        tile_pv<VT, false>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
+                                           st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t],
+                                           vmask[t], lane, j, o);
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < TPW; ++t) {
+                        const int ti = tw * TPW + t;
+                        tile_pv<VT, true>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
+                                          st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t],
+                                          vmask[t], lane, j, o);
+                    }
                 }
             }
             __syncwarp();
@@ -829,9 +851,17 @@ cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stre
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = configure_t<KT, VT, NS>(dev);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.n_splits, p.Hkv, p.B * p.QG);
-    decode_kernel<KT, VT, NS><<<grid, C::THREADS, C::SMEM, stream>>>(p, fused ? 1 : 0);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B * p.QG);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<KT, VT, NS>, p, fused ? 1 : 0);
 }
 
 template <int KT, int VT, int NS>
