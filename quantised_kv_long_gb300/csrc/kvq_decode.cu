@@ -357,22 +357,35 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
             mma_16816(o[4 * b + 3], a, w1.z, w1.w);
         }
     } else {
+        // P' = p x scale per (key, block) as f16 hi + lo: p is split once per tile
+        // (p = ph + pl), then per block  hi = ph*d,  err = fma(ph, d, -hi) (exact: the
+        // rounding error of an f16 product), lo = fma(pl, d, err)  -- three packed f16 ops
+        // per key pair, about 2^-21 relative.  The scale half2 words already pair keys
+        // (A,B) and (C,D), matching the A-fragment pairs.
+        uint32_t ph_ab, pl_ab, ph_cd, pl_cd;
+        split_hi_lo(pk[0], pk[1], ph_ab, pl_ab);
+        split_hi_lo(pk[2], pk[3], ph_cd, pl_cd);
         const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
         const uint32_t vscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
+        uint32_t mab = 0xffffffffu, mcd = 0xffffffffu;
+        if constexpr (PARTIAL) {  // scales past the length may hold any bits
+            mab = (vmask[0] ? 0x0000ffffu : 0u) | (vmask[1] ? 0xffff0000u : 0u);
+            mcd = (vmask[2] ? 0x0000ffffu : 0u) | (vmask[3] ? 0xffff0000u : 0u);
+        }
         uint4 wq4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            float2 dab = __half22float2(u32_as_h2(vscale[b][0]));
-            float2 dcd = __half22float2(u32_as_h2(vscale[b][1]));
-            if constexpr (PARTIAL) {  // scales past the length may hold any bits
-                dab.x = vmask[0] ? dab.x : 0.f;
-                dab.y = vmask[1] ? dab.y : 0.f;
-                dcd.x = vmask[2] ? dcd.x : 0.f;
-                dcd.y = vmask[3] ? dcd.y : 0.f;
-            }
+            const __half2 dab = u32_as_h2(vscale[b][0] & mab);
+            const __half2 dcd = u32_as_h2(vscale[b][1] & mcd);
+            const __half2 hab = __hmul2(u32_as_h2(ph_ab), dab);
+            const __half2 hcd = __hmul2(u32_as_h2(ph_cd), dcd);
+            const __half2 eab = __hfma2(u32_as_h2(ph_ab), dab, __hneg2(hab));
+            const __half2 ecd = __hfma2(u32_as_h2(ph_cd), dcd, __hneg2(hcd));
             uint32_t a[4];
-            split_hi_lo(pk[0] * dab.x, pk[1] * dab.y, a[0], a[1]);
-            split_hi_lo(pk[2] * dcd.x, pk[3] * dcd.y, a[2], a[3]);
+            a[0] = h2_as_u32(hab);
+            a[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), dab, eab));
+            a[2] = h2_as_u32(hcd);
+            a[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), dcd, ecd));
             if constexpr (VT == KVQ_Q8_0) {
                 const uint4 w = lds128(vc + b * 512 + lane * 16);
                 uint32_t x0, x1;
