@@ -73,7 +73,9 @@ __device__ __forceinline__ void cvt_q4(uint32_t w, uint32_t &lo02, uint32_t &lo1
 }
 
 
-constexpr int kDirectMerge = 8;     // up to this many splits are merged in one level
+// Split triples of one row group up to this size are merged in one level (one CTA reads
+// them all); larger sets use two levels so that no single CTA reads too much.
+constexpr int kDirectMergeBytes = 96 * 1024;
 constexpr int kMaxMergeWidth = 32;  // ceil(sqrt(kMaxSplits)): widest merge of either level
 
 __device__ __forceinline__ int group_size(int ns) {
@@ -101,111 +103,87 @@ __device__ __forceinline__ bool arrive_last(int32_t *counter, int target, int &s
 //   M = max_s m_s, w_s = exp(m_s - M), O = sum_s w_s o_s, L = sum_s w_s l_s.
 // Triples of row r, split s live at (r * stride + s0 + s).  Writes either the normalised
 // output (out = O / L, lse = M + log L) or one unnormalised triple at (r * q_stride + q_s).
+// The inputs were written by other CTAs and sit in L2.  Each thread owns two output
+// columns and merges up to kMergeChunk splits per L2 round trip, loading m, l and o
+// together and keeping a running maximum (rescaling when it grows), so a merge of up to
+// kMergeChunk splits costs one round trip and needs no shared memory or barrier.
+constexpr int kMergeChunk = 10;
 __device__ void merge_rows(const float *po, const float *pm, const float *pl, int stride, int s0, int NP,
-                           size_t row0, int rows, int D, float *scratch, float *out, float *lse, float *qo,
-                           float *qm, float *ql, int q_stride, int q_s) {
-    // The inputs were written by other CTAs and sit in L2: every phase issues all of its
-    // loads before using any, so a merge costs about three L2 round trips.
-    constexpr int W = kMaxMergeWidth;
-    float *wbuf = scratch;                        // [8][W] weights exp(m_s - M)
-    float *mraw = wbuf + kMaxRowsPerGroup * W;    // [8][W]
-    float *lraw = mraw + kMaxRowsPerGroup * W;    // [8][W]
-    float *Mbuf = lraw + kMaxRowsPerGroup * W;    // [8]
-    float *Lbuf = Mbuf + kMaxRowsPerGroup;        // [8]
+                           size_t row0, int rows, int D, float *out, float *lse, float *qo, float *qm, float *ql,
+                           int q_stride, int q_s) {
     const int tid = threadIdx.x, nthr = blockDim.x;
-    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
-    // (1) all (row, split) maxima and sums, two per thread in flight
-    for (int i0 = tid; i0 < rows * NP; i0 += 2 * nthr) {
-        const int i1 = i0 + nthr;
-        const int g0 = i0 / NP, t0 = i0 % NP, g1 = i1 / NP, t1 = i1 % NP;
-        const bool ok1 = i1 < rows * NP;
-        const float m0 = __ldcg(pm + (row0 + g0) * stride + s0 + t0);
-        const float l0 = __ldcg(pl + (row0 + g0) * stride + s0 + t0);
-        const float m1 = ok1 ? __ldcg(pm + (row0 + g1) * stride + s0 + t1) : 0.f;
-        const float l1 = ok1 ? __ldcg(pl + (row0 + g1) * stride + s0 + t1) : 0.f;
-        mraw[g0 * W + t0] = m0;
-        lraw[g0 * W + t0] = l0;
-        if (ok1) {
-            mraw[g1 * W + t1] = m1;
-            lraw[g1 * W + t1] = l1;
-        }
-    }
-    __syncthreads();
-    // (2) per row: M, weights, L (shared memory only)
-    for (int g = warp; g < rows; g += nwarps) {
-        float M = -CUDART_INF_F;
-        for (int t = lane; t < NP; t += 32) M = fmaxf(M, mraw[g * W + t]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float Ls = 0.f;
-        for (int t = lane; t < NP; t += 32) {
-            const float ms = mraw[g * W + t];
-            const float w = (M == -CUDART_INF_F || ms == -CUDART_INF_F) ? 0.f : expf(ms - M);
-            wbuf[g * W + t] = w;
-            Ls = fmaf(w, lraw[g * W + t], Ls);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
-        if (lane == 0) {
-            Mbuf[g] = M;
-            Lbuf[g] = Ls;
-        }
-    }
-    __syncthreads();
-    // (3) weighted sums: two columns per thread, up to 16 splits each, all loads issued first
     const int DQ = D / 4;
     const int C = rows * DQ;
     const float4 *po4 = reinterpret_cast<const float4 *>(po);
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int base = 0; base < C; base += 2 * nthr) {
-        const int c0 = base + tid, c1 = c0 + nthr;
-        const bool v0 = c0 < C, v1 = c1 < C;
-        const int g0 = v0 ? c0 / DQ : 0, q0 = v0 ? c0 % DQ : 0;
-        const int g1 = v1 ? c1 / DQ : 0, q1 = v1 ? c1 % DQ : 0;
-        const float4 *src0 = po4 + ((row0 + g0) * stride + s0) * DQ + q0;
-        const float4 *src1 = po4 + ((row0 + g1) * stride + s0) * DQ + q1;
-        float4 acc0 = z4, acc1 = z4;
-        for (int sc = 0; sc < NP; sc += 16) {
-            float4 a[16], b[16];
+        int col[2], g[2], dq[2];
+        bool v[2];
+        float M[2], L[2];
+        float4 A[2];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const bool in = sc + u < NP;
-                a[u] = (v0 && in) ? __ldcg(src0 + (size_t)(sc + u) * DQ) : z4;
-                b[u] = (v1 && in) ? __ldcg(src1 + (size_t)(sc + u) * DQ) : z4;
+        for (int k = 0; k < 2; ++k) {
+            col[k] = base + tid + k * nthr;
+            v[k] = col[k] < C;
+            g[k] = v[k] ? col[k] / DQ : 0;
+            dq[k] = v[k] ? col[k] % DQ : 0;
+            M[k] = -CUDART_INF_F;
+            L[k] = 0.f;
+            A[k] = z4;
+        }
+        for (int sc = 0; sc < NP; sc += kMergeChunk) {
+            float mm[2][kMergeChunk], ll[2][kMergeChunk];
+            float4 oo[2][kMergeChunk];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const size_t pr = (row0 + g[k]) * stride + s0 + sc;
+#pragma unroll
+                for (int u = 0; u < kMergeChunk; ++u) {
+                    const bool in = v[k] && (sc + u < NP);
+                    mm[k][u] = in ? __ldcg(pm + pr + u) : -CUDART_INF_F;
+                    ll[k][u] = in ? __ldcg(pl + pr + u) : 0.f;
+                    oo[k][u] = in ? __ldcg(po4 + (pr + u) * DQ + dq[k]) : z4;
+                }
             }
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const bool in = sc + u < NP;
-                const float w0 = in ? wbuf[g0 * W + sc + u] : 0.f;
-                const float w1 = in ? wbuf[g1 * W + sc + u] : 0.f;
-                acc0.x = fmaf(w0, a[u].x, acc0.x);
-                acc0.y = fmaf(w0, a[u].y, acc0.y);
-                acc0.z = fmaf(w0, a[u].z, acc0.z);
-                acc0.w = fmaf(w0, a[u].w, acc0.w);
-                acc1.x = fmaf(w1, b[u].x, acc1.x);
-                acc1.y = fmaf(w1, b[u].y, acc1.y);
-                acc1.z = fmaf(w1, b[u].z, acc1.z);
-                acc1.w = fmaf(w1, b[u].w, acc1.w);
+            for (int k = 0; k < 2; ++k) {
+                float cm = -CUDART_INF_F;
+#pragma unroll
+                for (int u = 0; u < kMergeChunk; ++u) cm = fmaxf(cm, mm[k][u]);
+                const float Mn = fmaxf(M[k], cm);
+                if (Mn == -CUDART_INF_F) continue;  // nothing but empty splits so far
+                const float a = M[k] == -CUDART_INF_F ? 0.f : expf(M[k] - Mn);
+                A[k].x *= a;
+                A[k].y *= a;
+                A[k].z *= a;
+                A[k].w *= a;
+                L[k] *= a;
+#pragma unroll
+                for (int u = 0; u < kMergeChunk; ++u) {
+                    const float w = mm[k][u] == -CUDART_INF_F ? 0.f : expf(mm[k][u] - Mn);
+                    A[k].x = fmaf(w, oo[k][u].x, A[k].x);
+                    A[k].y = fmaf(w, oo[k][u].y, A[k].y);
+                    A[k].z = fmaf(w, oo[k][u].z, A[k].z);
+                    A[k].w = fmaf(w, oo[k][u].w, A[k].w);
+                    L[k] = fmaf(w, ll[k][u], L[k]);
+                }
+                M[k] = Mn;
             }
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const bool v = k == 0 ? v0 : v1;
-            if (!v) continue;
-            const int g = k == 0 ? g0 : g1, dq = k == 0 ? q0 : q1;
-            const float4 acc = k == 0 ? acc0 : acc1;
-            const float Ls = Lbuf[g];
+            if (!v[k]) continue;
             if (out) {
-                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-                reinterpret_cast<float4 *>(out + (row0 + g) * D)[dq] =
-                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                if (dq == 0 && lse) lse[row0 + g] = Ls > 0.f ? Mbuf[g] + logf(Ls) : -CUDART_INF_F;
+                const float inv = L[k] > 0.f ? 1.f / L[k] : 0.f;
+                reinterpret_cast<float4 *>(out + (row0 + g[k]) * D)[dq[k]] =
+                    make_float4(A[k].x * inv, A[k].y * inv, A[k].z * inv, A[k].w * inv);
+                if (dq[k] == 0 && lse) lse[row0 + g[k]] = L[k] > 0.f ? M[k] + logf(L[k]) : -CUDART_INF_F;
             } else {
-                const size_t dr = (row0 + g) * static_cast<size_t>(q_stride) + q_s;
-                reinterpret_cast<float4 *>(qo + dr * D)[dq] = acc;
-                if (dq == 0) {
-                    qm[dr] = Mbuf[g];
-                    ql[dr] = Ls;
+                const size_t dr = (row0 + g[k]) * static_cast<size_t>(q_stride) + q_s;
+                reinterpret_cast<float4 *>(qo + dr * D)[dq[k]] = A[k];
+                if (dq[k] == 0) {
+                    qm[dr] = M[k];
+                    ql[dr] = L[k];
                 }
             }
         }
@@ -257,7 +235,6 @@ struct Cfg {
     static constexpr int D = NS * kSlice;
     // merge / combine scratch reuses the ring
     static_assert(TW * kMaxRowsPerGroup * D * 4 + 2 * TW * kMaxRowsPerGroup * 4 <= RING, "merge buffer");
-    static_assert(kMaxRowsPerGroup * (3 * kMaxMergeWidth + 2) * 4 <= RING, "merge scratch");
 };
 
 // Scores of one tile over this warp's 128-value slice for keys A=2j, B=2j+1 (S-tile 0) and
@@ -769,16 +746,15 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     if (!fused || single || timed_out) return;
 
     // ---------------- merge of the splits of this (sequence, KV head, row group) ----------------
-    // ns <= 8: the last CTA to arrive merges all splits.  Otherwise splits form groups of
-    // ceil(sqrt(ns)); the last arrival of each group merges its group into a group triple
-    // while other CTAs still run, and the last group to finish merges the group triples.
+    // Small sets of split triples: the last CTA to arrive merges them all.  Otherwise splits
+    // form groups of ceil(sqrt(ns)); the last arrival of each group merges its group into a
+    // group triple while other CTAs still run, and the last group merges the group triples.
     const size_t unit = (static_cast<size_t>(bseq) * p.Hkv + h) * p.QG + qg;
     const size_t row0 = static_cast<size_t>(bseq) * p.Hq + hq0;
-    float *scratch = reinterpret_cast<float *>(smem);
-    if (ns <= kDirectMerge) {
+    if (static_cast<long long>(ns) * rows * (D + 2) * 4 <= kDirectMergeBytes) {
         if (!arrive_last(p.counters + unit, ns, s_flag)) return;
-        merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, 0, ns, row0, rows, D, scratch, p.out, p.lse, nullptr,
-                   nullptr, nullptr, 0, 0);
+        merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, 0, ns, row0, rows, D, p.out, p.lse, nullptr, nullptr,
+                   nullptr, 0, 0);
         if (threadIdx.x == 0) p.counters[unit] = 0;
         return;
     }
@@ -788,12 +764,12 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     const int gsize = min(gs, ns - grp * gs);
     int32_t *cnt1 = p.counters1 + unit * p.n_groups_max + grp;
     if (!arrive_last(cnt1, gsize, s_flag)) return;
-    merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, grp * gs, gsize, row0, rows, D, scratch, nullptr, nullptr,
-               p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, grp);
+    merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, grp * gs, gsize, row0, rows, D, nullptr, nullptr, p.grp_o,
+               p.grp_m, p.grp_l, p.n_groups_max, grp);
     if (threadIdx.x == 0) *cnt1 = 0;
     if (!arrive_last(p.counters + unit, n_groups, s_flag)) return;
-    merge_rows(p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, 0, n_groups, row0, rows, D, scratch, p.out, p.lse,
-               nullptr, nullptr, nullptr, 0, 0);
+    merge_rows(p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, 0, n_groups, row0, rows, D, p.out, p.lse, nullptr,
+               nullptr, nullptr, 0, 0);
     if (threadIdx.x == 0) p.counters[unit] = 0;
 }
 
