@@ -40,6 +40,15 @@
  * kvq_cache_read_error, which synchronise their stream as documented.  Device pointers must point to
  * memory of the current CUDA device.  `stream` is a cudaStream_t (NULL = legacy default).
  *
+ * Early reads.  The decode kernels are launched with programmatic dependent launch: a
+ * launch may start while the previous kernel of its stream is still finishing.  Queries,
+ * new rows, outputs and the workspace are touched only once that kernel has completed.
+ * The cache's lengths and tiles are read before then whenever the library's own record
+ * shows that the previous library launch on the stream did not write this cache (the
+ * library notes, per stream, which cache each of its launches writes).  So after
+ * kvq_cache_create the K plane, V plane and state block must be written only through
+ * this library; a kernel of the caller's that writes them breaks that record.
+ *
  * Errors.  Every entry point returns a kvq_status; nothing aborts, traps or throws.
  * Argument errors are detected on the host before any launch and leave device memory
  * untouched.  A launch failure returns KVQ_ERR_CUDA (the CUDA error is not cleared from

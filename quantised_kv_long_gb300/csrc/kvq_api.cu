@@ -122,6 +122,47 @@ WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits) {
     return w;
 }
 
+// ---- per-stream record of which cache each library launch writes ----
+// A decode launch reads its cache's lengths and tiles before the previous kernel of the
+// stream has finished (DecodeParams::early) unless the library's previous launch on that
+// stream wrote the cache.  After kvq_cache_create only this library writes cache memory,
+// so the record covers every writer.  A fixed table of streams; once an entry has been
+// evicted, streams without an entry are treated as unknown (no early reads).
+struct StreamRec {
+    cudaStream_t stream;
+    const kvq_cache *wrote;  // cache written by the latest library launch on the stream
+};
+constexpr int kTrackSlots = 64;
+std::mutex g_track_mu;
+StreamRec g_track[kTrackSlots];
+int g_track_n = 0, g_track_next = 0;
+bool g_track_lost = false;
+
+// Called just before the library enqueues work on `stream` that reads cache `reads`
+// (nullptr: none) and writes cache `writes` (nullptr: none).  Returns whether the reads
+// may start before the previous kernel of the stream completes.
+bool track_launch(cudaStream_t stream, const kvq_cache *reads, const kvq_cache *writes) {
+    std::lock_guard<std::mutex> lock(g_track_mu);
+    int i = 0;
+    while (i < g_track_n && g_track[i].stream != stream) ++i;
+    bool early;
+    if (i < g_track_n) {
+        early = g_track[i].wrote != reads;
+    } else {
+        early = !g_track_lost;
+        if (g_track_n < kTrackSlots) {
+            i = g_track_n++;
+        } else {
+            i = g_track_next;
+            g_track_next = (g_track_next + 1) % kTrackSlots;
+            g_track_lost = true;
+        }
+        g_track[i].stream = stream;
+    }
+    g_track[i].wrote = writes;
+    return early && reads != nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -192,6 +233,7 @@ kvq_status kvq_cache_create(const kvq_cache_desc *desc, void *k_mem, void *v_mem
             return KVQ_ERR_INVALID_ARG;
         }
     }
+    track_launch(s, nullptr, c);
     *out = c;
     return KVQ_OK;
 }
@@ -215,6 +257,7 @@ kvq_status kvq_cache_set_lengths(kvq_cache *cache, const int32_t *h_len, void *s
         if (h_len[i] < 0 || h_len[i] > cache->desc.capacity) return KVQ_ERR_INVALID_ARG;
     std::memcpy(cache->h_len, h_len, sizeof(int32_t) * cache->desc.batch);
     // copy from the mirror (which outlives this call), not from the caller's buffer
+    track_launch(static_cast<cudaStream_t>(stream), nullptr, cache);
     return cuda_status(cudaMemcpyAsync(cache->state, cache->h_len, sizeof(int32_t) * cache->desc.batch,
                                        cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
 }
@@ -268,6 +311,7 @@ kvq_status kvq_quantize_append(kvq_cache *cache, const float *k, const float *v,
     p.cap = cache->desc.capacity;
     p.cap_tiles = cache->desc.capacity / kvq::kTileRows;
     p.total_warps = static_cast<int>(warps);
+    track_launch(static_cast<cudaStream_t>(stream), nullptr, cache);
     cudaError_t e = kvq::launch_append(cache->desc.type_k, cache->desc.type_v, p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
     for (int i = 0; i < nb; ++i) cache->h_len[b0 + i] += n_new;
@@ -319,6 +363,7 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const float *q, int32_t 
     p.part_m = reinterpret_cast<float *>(ws + w.part_m);
     p.part_l = reinterpret_cast<float *>(ws + w.part_l);
     p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    p.early = track_launch(static_cast<cudaStream_t>(stream), cache, nullptr) ? 1 : 0;
     return cuda_status(
         kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, static_cast<cudaStream_t>(stream)));
 }
@@ -361,6 +406,7 @@ kvq_status kvq_append_decode(kvq_cache *cache, const float *k_new, const float *
     p.k_new = k_new;
     p.v_new = v_new;
     p.ticket = cache->state + cache->desc.batch;
+    p.early = track_launch(static_cast<cudaStream_t>(stream), cache, cache) ? 1 : 0;
     cudaError_t e =
         kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return KVQ_ERR_CUDA;
@@ -379,6 +425,7 @@ kvq_status kvq_decode_partials(const kvq_cache *cache, const float *q, int32_t n
     p.part_o = part_o;
     p.part_m = part_m;
     p.part_l = part_l;
+    p.early = track_launch(static_cast<cudaStream_t>(stream), cache, nullptr) ? 1 : 0;
     return cuda_status(
         kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, false, static_cast<cudaStream_t>(stream)));
 }
@@ -390,6 +437,7 @@ kvq_status kvq_combine(const float *part_o, const float *part_m, const float *pa
     if (rows == 0) return KVQ_OK;
     if (!aligned16(part_o) || !aligned16(out)) return KVQ_ERR_ALIGNMENT;
     kvq::CombineParams p{part_o, part_m, part_l, out, lse, rows, n_splits, head_dim};
+    track_launch(static_cast<cudaStream_t>(stream), nullptr, nullptr);
     return cuda_status(kvq::launch_combine(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -447,6 +495,7 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const float *q, 
     p.part_m = reinterpret_cast<float *>(ws + w.part_m);
     p.part_l = reinterpret_cast<float *>(ws + w.part_l);
     p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    p.early = track_launch(cs, cache, nullptr) ? 1 : 0;
     return cuda_status(kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, cs));
 }
 

@@ -390,6 +390,40 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
     }
 }
 
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// Cache tiles this CTA starts with, pulled into L2 while the previous kernel of the stream
+// drains (called before the programmatic-launch wait).  Only a hint: the length read here
+// may be one append behind and the tiles may still be written; L2 is the coherence point,
+// so later reads see every write either way.  Capped per CTA so that the prefetched set of
+// all CTAs stays well inside L2.
+constexpr int kPrefetchBytes = 384 * 1024;
+template <class C>
+__device__ __noinline__ void prefetch_split(const DecodeParams &p, int bseq, int h, int split, int cap_rows,
+                                            int skip_tiles) {
+    int L = *reinterpret_cast<const volatile int32_t *>(p.len + bseq);
+    if (p.k_new != nullptr) ++L;
+    L = L < 0 ? 0 : (L > cap_rows ? cap_rows : L);
+    const int T = (L + kTileRows - 1) / kTileRows;
+    const int ns = max(1, min(p.n_splits, T));
+    if (split >= ns || T == 0) return;
+    const int tps = (T + ns - 1) / ns;
+    const int t0 = min(T, split * tps + skip_tiles), t1 = min(T, split * tps + tps);
+    const int nt = min(t1 - t0, kPrefetchBytes / C::TILE - skip_tiles);
+    if (nt <= 0) return;
+    const size_t bt = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + t0;
+    constexpr int kChunk = 32768;
+    auto pf = [](const uint8_t *base, size_t bytes) {
+        for (size_t o = 0; o < bytes; o += kChunk)
+            bulk_prefetch_l2(base + o, static_cast<uint32_t>(min(static_cast<size_t>(kChunk), bytes - o)));
+    };
+    pf(p.k_codes + bt * C::KC, static_cast<size_t>(nt) * C::KC);
+    pf(p.v_codes + bt * C::VC, static_cast<size_t>(nt) * C::VC);
+    if constexpr (C::KS > 0) pf(p.k_scales + bt * C::KS, static_cast<size_t>(nt) * C::KS);
+    if constexpr (C::VS > 0) pf(p.v_scales + bt * C::VS, static_cast<size_t>(nt) * C::VS);
+}
+
 template <int KT, int VT, int NS>
 __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
     using C = Cfg<KT, VT, NS>;
@@ -402,11 +436,29 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     const int split = blockIdx.x, h = blockIdx.y;
     const int bseq = blockIdx.z / p.QG, qg = blockIdx.z % p.QG;
     const int cap_rows = p.cap_tiles * kTileRows;
-    // Programmatic dependent launch: let the next kernel of the stream get scheduled as SMs
-    // free up, then wait for every earlier kernel (lengths, queries, new rows and cache
-    // tiles may all have been written by it) before touching global memory.
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    if (threadIdx.x == 0) {  // shared memory only: may run before the wait below
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, C::CW);
+        }
+        fence_mbar_init();
+        s_timeout = 0;
+    }
+    __syncthreads();
+    // Programmatic dependent launch.  Global memory that the previous kernel of the stream
+    // may write (queries, new rows, outputs, workspace, and in general the cache) is read
+    // only after griddepcontrol.wait.  With p.early set the host has established that the
+    // previous kernel does not write this cache, so its lengths and tiles are final already:
+    // the lengths are read at once and the producer fills the ring before the wait.  Every
+    // CTA releases its dependents only after its own wait, so while a kernel runs its
+    // pre-wait part at most one earlier kernel of the stream can still be running.
+    const bool early = p.early != 0;
+    if (!early) {
+        if (threadIdx.x == 0) prefetch_split<C>(p, bseq, h, split, cap_rows, 0);
+        grid_dep_wait();
+    }
     int L_old = __ldcg(p.len + bseq);
     L_old = L_old < 0 ? 0 : (L_old > cap_rows ? cap_rows : L_old);
     // fused append: the new row lands at position L_old and is attended to
@@ -420,6 +472,8 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     const int hq0 = h * p.G + qg * kMaxRowsPerGroup;  // first query head of this CTA
 
     if (split >= ns) {
+        if (early) grid_dep_wait();
+        grid_dep_launch();
         if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
         if (!fused) {  // partials mode: splits beyond ns are empty triples
             for (int idx = threadIdx.x; idx < rows * (p.D / 4); idx += blockDim.x) {
@@ -436,18 +490,6 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     }
     const int t_begin = min(T, split * tps), t_end = min(T, t_begin + tps);
     const int n_stage = (t_end - t_begin + C::TWT - 1) / C::TWT;
-
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *empty = full + C::STAGES;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(full + i, 1);
-            mbar_init(empty + i, C::CW);
-        }
-        fence_mbar_init();
-        s_timeout = 0;
-    }
-    __syncthreads();
 
     const size_t bh_tile = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles;
 
@@ -467,9 +509,38 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
         int issued_use[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) issued_use[i] = -1;
+        // one stage: up to TWT tiles of K codes, V codes, K scales, V scales (lane 0 only)
+        auto issue = [&](int k, int slot, int use) {
+            const int t0 = t_begin + k * C::TWT;
+            const int nt = min(C::TWT, t_end - t0);
+            uint8_t *st = smem + slot * C::STAGE;
+            mbar_arrive_expect_tx(full + slot, static_cast<uint32_t>(nt * C::TILE));
+            bulk_g2s(st, p.k_codes + (bh_tile + t0) * C::KC, nt * C::KC, full + slot);
+            bulk_g2s(st + C::TWT * C::KC, p.v_codes + (bh_tile + t0) * C::VC, nt * C::VC, full + slot);
+            if constexpr (C::KS > 0)
+                bulk_g2s(st + C::TWT * (C::KC + C::VC), p.k_scales + (bh_tile + t0) * C::KS, nt * C::KS, full + slot);
+            if constexpr (C::VS > 0)
+                bulk_g2s(st + C::TWT * (C::KC + C::VC + C::KS), p.v_scales + (bh_tile + t0) * C::VS, nt * C::VS,
+                         full + slot);
+            issued_use[slot] = use;
+        };
+        // early mode: fill the ring before the wait, up to (not including) the stage that
+        // holds the row this kernel appends
+        int k0 = 0;
+        if (early) {
+            k0 = min(n_stage, C::STAGES);
+            if (app_stage >= 0) k0 = min(k0, app_stage);
+            if (lane == 0) {
+                for (int k = 0; k < k0; ++k) issue(k, k, 0);
+                prefetch_split<C>(p, bseq, h, split, cap_rows, k0 * C::TWT);
+            }
+            __syncwarp();
+            grid_dep_wait();
+        }
+        grid_dep_launch();
         bool ok = true;
-        int slot = 0, use = 0;
-        for (int k = 0; k < n_stage; ++k) {
+        int slot = k0 == C::STAGES ? 0 : k0, use = k0 == C::STAGES ? 1 : 0;
+        for (int k = k0; k < n_stage; ++k) {
             bool ok_k = true;
             if (lane == 0 && use > 0) ok_k = mbar_wait(empty + slot, (use - 1) & 1);
             if (!__shfl_sync(0xffffffffu, ok_k ? 1 : 0, 0)) {
@@ -494,27 +565,15 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 asm volatile("fence.proxy.async.global;\n" ::: "memory");
                 __syncwarp();
             }
-            if (lane == 0) {
-                const int t0 = t_begin + k * C::TWT;
-                const int nt = min(C::TWT, t_end - t0);
-                uint8_t *st = smem + slot * C::STAGE;
-                mbar_arrive_expect_tx(full + slot, static_cast<uint32_t>(nt * C::TILE));
-                bulk_g2s(st, p.k_codes + (bh_tile + t0) * C::KC, nt * C::KC, full + slot);
-                bulk_g2s(st + C::TWT * C::KC, p.v_codes + (bh_tile + t0) * C::VC, nt * C::VC, full + slot);
-                if constexpr (C::KS > 0)
-                    bulk_g2s(st + C::TWT * (C::KC + C::VC), p.k_scales + (bh_tile + t0) * C::KS, nt * C::KS,
-                             full + slot);
-                if constexpr (C::VS > 0)
-                    bulk_g2s(st + C::TWT * (C::KC + C::VC + C::KS), p.v_scales + (bh_tile + t0) * C::VS,
-                             nt * C::VS, full + slot);
-                issued_use[slot] = use;
-            }
+            if (lane == 0) issue(k, slot, use);
             __syncwarp();
             if (++slot == C::STAGES) {
                 slot = 0;
                 ++use;
             }
         }
+        // the length advance of a fused append, off the consumers' critical path
+        if (appending && lane == 0) grid_ticket(p, cap_rows);
         if (!ok && lane == 0) {
             atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
             s_timeout = 1;
@@ -524,6 +583,8 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
         }
     } else {
         // ---------------- consumers ----------------
+        if (early) grid_dep_wait();
+        grid_dep_launch();
         const int cw = warp - 1;
         tw = cw / NS;
         sl = cw % NS;
@@ -682,7 +743,6 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
 
     // ---------------- merge the tile-warps of this CTA ----------------
     __syncthreads();  // the ring is free from here on
-    if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
     constexpr int D = C::D;
     float *Ob = reinterpret_cast<float *>(smem);                    // [TW][8][D]
     float *mb = Ob + C::TW * kMaxRowsPerGroup * D;                 // [TW][8]

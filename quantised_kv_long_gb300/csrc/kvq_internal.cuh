@@ -62,6 +62,9 @@ struct DecodeParams {
     // fused quantise-on-append of one row per sequence (nullptr: attend only)
     const float *k_new, *v_new;  // [B][Hkv][D]
     int32_t *ticket;             // grid arrival ticket (state block); the last CTA advances len[]
+    // 1: the previous kernel of the stream does not write this cache, so lengths and tiles
+    // may be read before the programmatic-launch wait (set by the host, see kvq_api.cu)
+    int early;
 };
 
 struct AppendParams {
@@ -143,6 +146,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Hint: pull [src, src + bytes) into L2 (bytes % 16 == 0, src 16-byte aligned).  No data
+// reaches the SM and nothing waits on it; L2 stays coherent with later writes.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // 16-byte shared-memory load (ordinary load: the mbarrier waits carry memory clobbers)

@@ -483,3 +483,84 @@ def test_append_decode_graph_replay(kvq):
         vc, vs = oracle.quantize("q8_0", V[0, :, :n].cpu().numpy())
         ref, _ = oracle.attention("q8_0", kc, ks, "q8_0", vc, vs, n, qh[0], wl.scale)
         assert np.abs(out[0].cpu().numpy() - ref).max() <= TOL
+
+
+@pytest.mark.parametrize("order", ["layers", "same_cache", "mixed"])
+def test_back_to_back_launches_without_sync(kvq, order):
+    """Launches queued back to back with no synchronisation in between, as a model's decode
+    step issues them.  A decode launch may start while the previous kernel of the stream is
+    still running and then reads its cache's lengths and tiles early unless that kernel
+    wrote the cache; these orders cover both cases (other caches before it, the same cache
+    before it, a bulk append of the same cache just before it, a plain decode between)."""
+    H, D, G, tk, tv = 2, 128, 5, "q8_0", "q4_0"
+    lens = [700, 333]
+    B = len(lens)
+    n_layers = 1 if order == "same_cache" else 3
+    steps = 6 if order == "same_cache" else 4
+    wl = syn.Workload("b2b", n_layers, B, H * G, H, D, tk, tv, tuple(lens), seed=77)
+    cap = 736
+    caches = [kvq.KVCache(B, H, D, cap, tk, tv) for _ in range(n_layers)]
+    rows = {}
+    for l in range(n_layers):
+        for kind in (syn.KIND_K, syn.KIND_V):
+            rows[l, kind] = [torch.stack([syn.kv_rows(wl, kind, l, b, h, 0, lens[b] + steps + 1) for h in range(H)])
+                             for b in range(B)]
+    ops = []
+    if order == "mixed":
+        # layer 0 is filled right before its first fused step; layer 1 gets a plain decode
+        # between fused steps; layer 2 follows a bulk append of itself
+        ops += [("prefill", 1), ("prefill", 2)]
+        for s in range(steps):
+            if s == 0:
+                ops.append(("prefill", 0))
+            ops += [("step", 0, s), ("decode", 1), ("step", 1, s), ("step", 2, s)]
+    else:
+        ops += [("prefill", l) for l in range(n_layers)]
+        ops += [("step", l, s) for s in range(steps) for l in range(n_layers)]
+    # every input is made before the first launch, so that the library's launches follow
+    # one another on the stream with no other kernel between them
+    n_now = [list(lens) for _ in range(n_layers)]
+    plan = []
+    for i, op in enumerate(ops):
+        l = op[1]
+        if op[0] == "prefill":
+            plan.append((op[0], l, [rows[l, syn.KIND_K][b][None, :, :lens[b]].contiguous() for b in range(B)],
+                         [rows[l, syn.KIND_V][b][None, :, :lens[b]].contiguous() for b in range(B)], None))
+            continue
+        q = syn.queries(wl, l, step=i)
+        kn = vn = None
+        if op[0] == "step":
+            kn = torch.stack([rows[l, syn.KIND_K][b][:, n_now[l][b]] for b in range(B)])[:, :, None].contiguous()
+            vn = torch.stack([rows[l, syn.KIND_V][b][:, n_now[l][b]] for b in range(B)])[:, :, None].contiguous()
+            n_now[l] = [n + 1 for n in n_now[l]]
+        plan.append((op[0], l, kn, vn, q, list(n_now[l]),
+                     torch.empty_like(q), torch.empty((B, H * G), device="cuda")))
+    ws = caches[0].workspace(H * G, 0)  # one workspace shared by every launch
+    torch.cuda.synchronize()
+    expect = []
+    for item in plan:
+        kind, l = item[0], item[1]
+        c = caches[l]
+        if kind == "prefill":
+            for b in range(B):
+                c.append(item[2][b], item[3][b], b0=b)
+            continue
+        _, _, kn, vn, q, ns, out, lse = item
+        if kind == "step":
+            c.append_decode(kn, vn, q, scale=wl.scale, out=out, lse=lse, workspace=ws)
+        else:
+            c.decode(q, scale=wl.scale, out=out, lse=lse, workspace=ws)
+        expect.append((l, ns, q, out, lse))
+    torch.cuda.synchronize()
+    for l in range(n_layers):
+        assert caches[l].sync_lengths() == n_now[l]
+        assert caches[l].read_error() == 0
+    for l, ns, q, out, lse in expect:
+        qh = q.cpu().numpy()
+        for b in range(B):
+            n = ns[b]
+            kc, ks = oracle.quantize(tk, rows[l, syn.KIND_K][b][:, :n].cpu().numpy())
+            vc, vs = oracle.quantize(tv, rows[l, syn.KIND_V][b][:, :n].cpu().numpy())
+            ref, ref_lse = oracle.attention(tk, kc, ks, tv, vc, vs, n, qh[b], wl.scale)
+            assert np.abs(out[b].cpu().numpy() - ref).max() <= TOL, (l, n, b)
+            assert np.abs(lse[b].cpu().numpy() - ref_lse).max() <= TOL
