@@ -2,7 +2,7 @@
  * kvq.h -- C ABI of libkvq: a block-quantised KV cache with quantise-on-append and
  * split-K single-token decode attention for one NVIDIA GB300 (sm_103a).
  *
- * The operation (problem statement of the spec reading): for each sequence b and
+ * The operation: for each sequence b and
  * query head hq, with G = Hq / Hkv query heads sharing KV head h = hq / G,
  *
  *     s_t   = scale * <q[b,hq,:], k_hat[b,h,t,:]>          for t < len[b]
@@ -82,8 +82,10 @@
  *             value in the low nibble if i < 16, else the high nibble
  *   V, f16  : (2b + hv)*512 + (4n' + j)*16 + (r%2)*8 + pos*2
  *   scales (K or V), for block b of the slice: j*32 + b*8 + pos*2   (f16 bits)
- * The codes and scales themselves are exactly the GGML q8_0/q4_0 values above; only
- * their placement differs from GGML's array-of-blocks order.
+ * The codes and scales are the GGML q8_0/q4_0 values above; only their placement
+ * differs from GGML's array-of-blocks order, and a q8_0 code q is stored as a
+ * sign-magnitude byte (q < 0 ? 0x80 | -q : q), which a permute and a mask turn into the
+ * f16 subnormal q * 2^-24 that the decode kernel feeds to the tensor cores.
  *
  * State block (int32, 16-byte multiple): [len[B]][append ticket][error word][pad].
  * Zero it (or set lengths with kvq_cache_set_lengths) before kvq_cache_create.
@@ -99,7 +101,7 @@
 extern "C" {
 #endif
 
-#define KVQ_ABI_VERSION 1
+#define KVQ_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define KVQ_API __attribute__((visibility("default")))

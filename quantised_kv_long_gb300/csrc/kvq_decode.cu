@@ -48,30 +48,43 @@ __device__ __forceinline__ void split_hi_lo(float x0, float x1, uint32_t &hi, ui
     lo = h2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
 }
 
-// 4 int8 codes (bytes x0..x3) -> f16 pairs (x0, x2) and (x1, x3), exact.
-// (byte ^ 0x80) | 0x6400 is the f16 1024 + (code + 128); subtracting 1152 leaves the code.
-__device__ __forceinline__ void cvt_q8(uint32_t w, uint32_t &p02, uint32_t &p13) {
-    const __half2 k1152 = __float2half2_rn(1152.0f);
-    const uint32_t a = (w & 0x00ff00ffu) ^ 0x64806480u;
-    const uint32_t b = ((w >> 8) & 0x00ff00ffu) ^ 0x64806480u;
-    p02 = h2_as_u32(__hsub2(u32_as_h2(a), k1152));
-    p13 = h2_as_u32(__hsub2(u32_as_h2(b), k1152));
+// ---- codes as f16 subnormals ----
+// Code words become mma operands with a permute and a mask.  A q8_0 code is stored as a
+// sign-magnitude byte (bit 7 sign, bits 0..6 |q|); placing the magnitude in the low bits
+// of an f16 half and the sign in bit 15 gives the subnormal q * 2^-24.  A q4_0 low nibble
+// c in the low bits is c * 2^-24 and a high nibble (bits 4..7) is 16c * 2^-24; the offset
+// 8 times the sum of the other operand is removed afterwards.  mma.sync multiplies f16
+// subnormals exactly, so the accumulators hold exact dot products in units of 2^-24 (or
+// 2^-20), and the unit is folded into one final multiply.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t prmt(uint32_t a) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;\n" : "=r"(d) : "r"(a), "n"(SEL));
+    return d;
 }
+// bytes 0, 2 / 1, 3 of a word of q8_0 codes as two f16 halves: byte, then its sign
+// replicated (selector nibble with bit 3 set), masked to sign bit and magnitude
+__device__ __forceinline__ uint32_t q8_02(uint32_t w) { return prmt<0xA280u>(w) & 0x807f807fu; }
+__device__ __forceinline__ uint32_t q8_13(uint32_t w) { return prmt<0xB391u>(w) & 0x807f807fu; }
+constexpr uint32_t kNibLo = 0x000f000fu, kNibHi = 0x00f000f0u;
+constexpr float kTwo24 = 16777216.0f, kTwo20 = 1048576.0f;
+constexpr float kQ4Offset = 8.0f;  // q4_0 value = scale * (c - 8)
 
-// 4 bytes of q4_0 nibbles -> f16 pairs (code - 8): low nibbles of bytes (0,2), (1,3) and
-// high nibbles of bytes (0,2), (1,3).  nibble | 0x6400 is 1024 + c; (c << 4) | 0x6400 is
-// 1024 + 16c, and (1024 + 16c)/16 - 72 = c - 8 exactly.
-__device__ __forceinline__ void cvt_q4(uint32_t w, uint32_t &lo02, uint32_t &lo13, uint32_t &hi02, uint32_t &hi13) {
-    const __half2 k1032 = __float2half2_rn(1032.0f);
-    const __half2 k16th = __float2half2_rn(0.0625f);
-    const __half2 km72 = __float2half2_rn(-72.0f);
-    const uint32_t w8 = w >> 8;
-    lo02 = h2_as_u32(__hsub2(u32_as_h2((w & 0x000f000fu) | 0x64006400u), k1032));
-    lo13 = h2_as_u32(__hsub2(u32_as_h2((w8 & 0x000f000fu) | 0x64006400u), k1032));
-    hi02 = h2_as_u32(__hfma2(u32_as_h2((w & 0x00f000f0u) | 0x64006400u), k16th, km72));
-    hi13 = h2_as_u32(__hfma2(u32_as_h2((w8 & 0x00f000f0u) | 0x64006400u), k16th, km72));
+// packed fp32 pair arithmetic (one instruction per pair)
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n add.rn.f32x2 rd, ra, rb;\n"
+        " mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
-
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
 
 // Split triples of one row group up to this size are merged in one level (one CTA reads
 // them all); larger sets use two levels so that no single CTA reads too much.
@@ -231,7 +244,9 @@ struct Cfg {
     static constexpr int RING = STAGES * STAGE;
     static constexpr int XCHG = NS == 2 ? TW * 2 * 2 * 32 * 16 * TPW : 0;
     static constexpr int BAR_OFF = RING + XCHG;
-    static constexpr int SMEM = BAR_OFF + 2 * STAGES * 8 + 16;
+    // per consumer warp: the K code-offset corrections of its 8 rows x 4 blocks
+    static constexpr int KCOR_OFF = (BAR_OFF + 2 * STAGES * 8 + 15) / 16 * 16;
+    static constexpr int SMEM = KCOR_OFF + CW * 128 + 16;
     static constexpr int D = NS * kSlice;
     // merge / combine scratch reuses the ring
     static_assert(TW * kMaxRowsPerGroup * D * 4 + 2 * TW * kMaxRowsPerGroup * 4 <= RING, "merge buffer");
@@ -240,8 +255,8 @@ struct Cfg {
 // Scores of one tile over this warp's 128-value slice for keys A=2j, B=2j+1 (S-tile 0) and
 // C=8+2j, D=9+2j (S-tile 1), row g = lane/4, in log2 units (Q was prescaled).
 template <int KT>
-__device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks, const uint32_t (&qa)[8][4], int lane,
-                                            int j, float (&s)[4]) {
+__device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks, const uint32_t (&qa)[8][4],
+                                            const uint8_t *kcor, int lane, int j, float (&s)[4]) {
     if constexpr (KT == KVQ_F16) {
         float acc[2][4];
 #pragma unroll
@@ -263,43 +278,56 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
         s[2] = acc[1][0] + acc[1][2];
         s[3] = acc[1][1] + acc[1][3];
     } else {
+        // accumulators hold sum q * code in units of 2^-24 (q8_0) or, with the low-nibble
+        // chunk of Q prescaled by 16, sum q * c in units of 2^-20 (q4_0), where
+        // kcorr[b] = -8 * sum_b q in the same unit turns c into the code value c - 8
+        float kcorr[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (KT == KVQ_Q4_0) {
+            const float4 kc4 = *reinterpret_cast<const float4 *>(kcor);
+            kcorr[0] = kc4.x;
+            kcorr[1] = kc4.y;
+            kcorr[2] = kc4.z;
+            kcorr[3] = kc4.w;
+        }
         const uint4 sc0 = lds128(ks + j * 32), sc1 = lds128(ks + j * 32 + 16);
         const uint32_t kscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
-        s[0] = s[1] = s[2] = s[3] = 0.f;
+        float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
         uint4 wq4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             float acc[2][4];
             if constexpr (KT == KVQ_Q8_0) {
                 const uint4 w = lds128(kc + b * 512 + lane * 16);
-                uint32_t x0, x1;
-                cvt_q8(w.x, x0, x1);
-                mma_16816_z(acc[0], qa[2 * b], x0, x1);
-                cvt_q8(w.y, x0, x1);
-                mma_16816(acc[0], qa[2 * b + 1], x0, x1);
-                cvt_q8(w.z, x0, x1);
-                mma_16816_z(acc[1], qa[2 * b], x0, x1);
-                cvt_q8(w.w, x0, x1);
-                mma_16816(acc[1], qa[2 * b + 1], x0, x1);
+                mma_16816_z(acc[0], qa[2 * b], q8_02(w.x), q8_13(w.x));
+                mma_16816(acc[0], qa[2 * b + 1], q8_02(w.y), q8_13(w.y));
+                mma_16816_z(acc[1], qa[2 * b], q8_02(w.z), q8_13(w.z));
+                mma_16816(acc[1], qa[2 * b + 1], q8_02(w.w), q8_13(w.w));
             } else {
                 if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
-                const uint32_t w_st0 = (b & 1) ? wq4.z : wq4.x;
-                const uint32_t w_st1 = (b & 1) ? wq4.w : wq4.y;
-                uint32_t l02, l13, h02, h13;
-                cvt_q4(w_st0, l02, l13, h02, h13);
-                mma_16816_z(acc[0], qa[2 * b], l02, l13);
-                mma_16816(acc[0], qa[2 * b + 1], h02, h13);
-                cvt_q4(w_st1, l02, l13, h02, h13);
-                mma_16816_z(acc[1], qa[2 * b], l02, l13);
-                mma_16816(acc[1], qa[2 * b + 1], h02, h13);
+                const uint32_t w0 = (b & 1) ? wq4.z : wq4.x, w0s = w0 >> 8;
+                const uint32_t w1 = (b & 1) ? wq4.w : wq4.y, w1s = w1 >> 8;
+                mma_16816_z(acc[0], qa[2 * b], w0 & kNibLo, w0s & kNibLo);
+                mma_16816(acc[0], qa[2 * b + 1], w0 & kNibHi, w0s & kNibHi);
+                mma_16816_z(acc[1], qa[2 * b], w1 & kNibLo, w1s & kNibLo);
+                mma_16816(acc[1], qa[2 * b + 1], w1 & kNibHi, w1s & kNibHi);
             }
             const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
             const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
-            s[0] = fmaf(dab.x, acc[0][0] + acc[0][2], s[0]);
-            s[1] = fmaf(dab.y, acc[0][1] + acc[0][3], s[1]);
-            s[2] = fmaf(dcd.x, acc[1][0] + acc[1][2], s[2]);
-            s[3] = fmaf(dcd.y, acc[1][1] + acc[1][3], s[3]);
+            float2 t01 = add2(make_float2(acc[0][0], acc[0][1]), make_float2(acc[0][2], acc[0][3]));
+            float2 t23 = add2(make_float2(acc[1][0], acc[1][1]), make_float2(acc[1][2], acc[1][3]));
+            if constexpr (KT == KVQ_Q4_0) {
+                const float2 cb = make_float2(kcorr[b], kcorr[b]);
+                t01 = add2(t01, cb);
+                t23 = add2(t23, cb);
+            }
+            s01 = fma2(dab, t01, s01);
+            s23 = fma2(dcd, t23, s23);
         }
+        constexpr float unit = KT == KVQ_Q8_0 ? kTwo24 : kTwo20;
+        s[0] = s01.x * unit;
+        s[1] = s01.y * unit;
+        s[2] = s23.x * unit;
+        s[3] = s23.y * unit;
     }
 }
 
@@ -307,7 +335,8 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
 // vmask: which of A,B,C,D are inside the sequence (rows past the length may hold any bits).
 template <int VT, bool PARTIAL>
 __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, const float (&pk)[4],
-                                        const bool (&vmask)[4], int lane, int j, float (&o)[16][4]) {
+                                        const bool (&vmask)[4], int lane, int j, float (&o)[16][4],
+                                        uint32_t magic) {
     if constexpr (VT == KVQ_F16) {
         uint32_t a[4];
         split_hi_lo(pk[0], pk[1], a[0], a[1]);
@@ -363,28 +392,29 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
             a[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), dab, eab));
             a[2] = h2_as_u32(hcd);
             a[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), dcd, ecd));
+            // o accumulates sum P' * code in units of 2^-24 (q4_0 high nibbles: 16c); for
+            // q4_0, corr column b accumulates sum P' of block b (B = 1.0 in column b), which
+            // removes the code offset 8 at the end
             if constexpr (VT == KVQ_Q8_0) {
                 const uint4 w = lds128(vc + b * 512 + lane * 16);
-                uint32_t x0, x1;
-                cvt_q8(w.x, x0, x1);
-                mma_16816(o[4 * b + 0], a, x0, x1);
-                cvt_q8(w.y, x0, x1);
-                mma_16816(o[4 * b + 1], a, x0, x1);
-                cvt_q8(w.z, x0, x1);
-                mma_16816(o[4 * b + 2], a, x0, x1);
-                cvt_q8(w.w, x0, x1);
-                mma_16816(o[4 * b + 3], a, x0, x1);
+                mma_16816(o[4 * b + 0], a, q8_02(w.x), q8_13(w.x));
+                mma_16816(o[4 * b + 1], a, q8_02(w.y), q8_13(w.y));
+                mma_16816(o[4 * b + 2], a, q8_02(w.z), q8_13(w.z));
+                mma_16816(o[4 * b + 3], a, q8_02(w.w), q8_13(w.w));
             } else {
+                // q4_0 V: exact f16 values c - 8 by the magic-number route (nibble | 0x6400 is
+                // 1024 + c; the high nibble gives 1024 + 16c, scaled by 1/16 and less 72)
                 if ((b & 1) == 0) wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
-                const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x;  // bytes 2n'   of the block
-                const uint32_t wq1 = (b & 1) ? wq4.w : wq4.y;  // bytes 2n'+1 of the block
-                uint32_t l02, l13, h02, h13;
-                cvt_q4(wq0, l02, l13, h02, h13);
-                mma_16816(o[4 * b + 0], a, l02, l13);
-                mma_16816(o[4 * b + 2], a, h02, h13);
-                cvt_q4(wq1, l02, l13, h02, h13);
-                mma_16816(o[4 * b + 1], a, l02, l13);
-                mma_16816(o[4 * b + 3], a, h02, h13);
+                const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x, wq0s = wq0 >> 8;  // bytes 2n'   of the block
+                const uint32_t wq1 = (b & 1) ? wq4.w : wq4.y, wq1s = wq1 >> 8;  // bytes 2n'+1 of the block
+                const __half2 k1032 = __float2half2_rn(1032.0f), k16th = __float2half2_rn(0.0625f),
+                              km72 = __float2half2_rn(-72.0f);
+                auto lo = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2((x & kNibLo) | magic), k1032)); };
+                auto hi = [&](uint32_t x) { return h2_as_u32(__hfma2(u32_as_h2((x & kNibHi) | magic), k16th, km72)); };
+                mma_16816(o[4 * b + 0], a, lo(wq0), lo(wq0s));
+                mma_16816(o[4 * b + 2], a, hi(wq0), hi(wq0s));
+                mma_16816(o[4 * b + 1], a, lo(wq1), lo(wq1s));
+                mma_16816(o[4 * b + 3], a, hi(wq1), hi(wq1s));
             }
         }
     }
@@ -590,9 +620,14 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
         sl = cw % NS;
         const int g = lane >> 2, j = lane & 3;
 
-        // Q fragments (scaled to log2 units, split into f16 hi + lo rows)
+        // Q fragments (scaled to log2 units, split into f16 hi + lo rows).  For q4_0 keys the
+        // low-nibble chunk of each block is prescaled by 16 (exact) to match the high
+        // nibbles, which arrive as 16c, and kcorr[b] = -8 times the block's sum of q in the
+        // accumulator unit is kept for each row.
         uint32_t qa[8][4];
+        uint8_t *kcor_row = smem + C::KCOR_OFF + cw * 128 + g * 16;
         {
+            float kcorr[4] = {0.f, 0.f, 0.f, 0.f};
             const bool rv = g < rows;
             const float *qrow = p.q + (static_cast<size_t>(bseq) * p.Hq + hq0 + (rv ? g : 0)) * p.D + sl * kSlice;
 #pragma unroll
@@ -602,10 +637,27 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 x.y *= p.scale_log2;
                 x.z *= p.scale_log2;
                 x.w *= p.scale_log2;
-                split_hi_lo(x.x, x.z, qa[c][0], qa[c][1]);  // k = 2j, 2j+1  <->  d + 0, d + 2
-                split_hi_lo(x.y, x.w, qa[c][2], qa[c][3]);  // k = 2j+8, 2j+9 <-> d + 1, d + 3
+                kcorr[c >> 1] += (x.x + x.y) + (x.z + x.w);
+                const float f = (KT == KVQ_Q4_0 && (c & 1) == 0) ? 16.f : 1.f;
+                split_hi_lo(x.x * f, x.z * f, qa[c][0], qa[c][1]);  // k = 2j, 2j+1  <->  d + 0, d + 2
+                split_hi_lo(x.y * f, x.w * f, qa[c][2], qa[c][3]);  // k = 2j+8, 2j+9 <-> d + 1, d + 3
+            }
+            if constexpr (KT == KVQ_Q4_0) {
+                constexpr float kf = -kQ4Offset / kTwo20;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    kcorr[b] += __shfl_xor_sync(0xffffffffu, kcorr[b], 1);
+                    kcorr[b] += __shfl_xor_sync(0xffffffffu, kcorr[b], 2);
+                    kcorr[b] *= kf;
+                }
+                // kept in shared memory (one row of 4 per lane group) instead of registers
+                if (j == 0)
+                    *reinterpret_cast<float4 *>(kcor_row) = make_float4(kcorr[0], kcorr[1], kcorr[2], kcorr[3]);
+                __syncwarp();
             }
         }
+        uint32_t magic;  // 0x64006400 in a register, so each nibble mask-and-or is one instruction
+        asm volatile("mov.b32 %0, 0x64006400;\n" : "=r"(magic));
         float4 *xchg = reinterpret_cast<float4 *>(smem + C::RING);
         bool dead = false;
         // keys of this lane inside a tile: A=2j, B=2j+1, C=8+2j, D=9+2j
@@ -626,7 +678,8 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 for (int t = 0; t < TPW; ++t) {
                     const int ti = tw * TPW + t;  // tile index inside the stage
                     tile_scores<KT>(st + ti * C::KC + sl * code_tile_bytes(KT),
-                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * kScaleTile, qa, lane, j, sc[t]);
+                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * kScaleTile, qa, kcor_row, lane,
+                                    j, sc[t]);
                 }
                 if constexpr (NS == 2) {
                     // the two slice-warps of this tile pair add their partial scores
@@ -717,7 +770,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                         const int ti = tw * TPW + t;
                         tile_pv<VT, false>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
                                            st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t],
-                                           vmask[t], lane, j, o);
+                                           vmask[t], lane, j, o, magic);
                     }
                 } else {
 #pragma unroll
@@ -725,7 +778,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                         const int ti = tw * TPW + t;
                         tile_pv<VT, true>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
                                           st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t],
-                                          vmask[t], lane, j, o);
+                                          vmask[t], lane, j, o, magic);
                     }
                 }
             }
@@ -734,6 +787,16 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
             if (++slot == C::STAGES) {
                 slot = 0;
                 ++use;
+            }
+        }
+        // q8_0 V: o to real units
+        if constexpr (VT == KVQ_Q8_0) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] = (o[i][0] + o[i][2]) * kTwo24;
+                o[i][1] = (o[i][1] + o[i][3]) * kTwo24;
+                o[i][2] = 0.f;
+                o[i][3] = 0.f;
             }
         }
         // row sums over the four lanes of a row

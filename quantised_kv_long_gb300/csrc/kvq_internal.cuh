@@ -211,7 +211,10 @@ __device__ __forceinline__ void quantize_store(const float *x, uint8_t *codes, u
         const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
         int c[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) c[e] = static_cast<int>(round_half_away(__fmul_rn(xs[e], id)));
+        for (int e = 0; e < 4; ++e) {  // stored as a sign-magnitude byte
+            const int q = static_cast<int>(round_half_away(__fmul_rn(xs[e], id)));
+            c[e] = q < 0 ? (0x80 | -q) : q;
+        }
         if constexpr (!IS_V) {
             const int jd = (dd0 & 15) >> 2, hd = i0 >> 4;
             const uint32_t w = (uint32_t(c[0]) & 0xffu) | ((uint32_t(c[1]) & 0xffu) << 8) |

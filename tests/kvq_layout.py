@@ -75,7 +75,10 @@ def decode_plane(codes_plane: np.ndarray, scales_plane: np.ndarray, kv_type: str
         return codes, scales
     byte = raw[..., off]
     if kv_type == "q8_0":
-        codes = byte.view(np.int8).transpose(0, 1, 2, 4, 3, 5).reshape(B, Hkv, cap, D)
+        # stored as a sign-magnitude byte
+        mag = (byte & np.uint8(0x7F)).astype(np.int16)
+        q = np.where(byte & np.uint8(0x80), -mag, mag).astype(np.int8)
+        codes = q.transpose(0, 1, 2, 4, 3, 5).reshape(B, Hkv, cap, D)
     else:
         c = np.where(nib == 1, byte >> 4, byte & 0x0F).astype(np.uint8)   # [B,Hkv,T,NS,16,128]
         c = c.transpose(0, 1, 2, 4, 3, 5).reshape(B, Hkv, cap, D // 32, 32)
