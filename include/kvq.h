@@ -109,7 +109,14 @@ extern "C" {
 #define KVQ_API
 #endif
 
-typedef enum { KVQ_F16 = 0, KVQ_Q8_0 = 1, KVQ_Q4_0 = 2 } kvq_type;
+typedef enum {
+    KVQ_F16 = 0,
+    KVQ_Q8_0 = 1,
+    KVQ_Q4_0 = 2,
+    /* storage cost only (kvq_block_bytes, kvq_select_tier); caches of these types are
+       KVQ_ERR_UNSUPPORTED */
+    KVQ_Q5_1 = 5
+} kvq_type;
 
 typedef enum {
     KVQ_OK = 0,
@@ -265,6 +272,37 @@ KVQ_API kvq_status kvq_combine(const float *part_o, const float *part_m, const f
 KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const float *q, int32_t n_q_heads,
                                                 float scale, int32_t n_splits, float *out, float *lse,
                                                 void *stream);
+
+/*
+ * Storage cost of one 32-value block of a type, in bytes: f16 64, q8_0 34, q4_0 18,
+ * q5_1 24 (two f16 scales, 32 fifth bits, 16 bytes of nibbles).  0 for an unknown type.
+ * "HAL #582 -- per-layer KV compression study", section 1 and section 5 P1 (the P1
+ * validation prices q5_1 K + q4_0 V at 2016 MiB for 32768 cells of the 14B shape).
+ */
+KVQ_API int32_t kvq_block_bytes(kvq_type type);
+
+/*
+ * Automatic KV tier at start-up, "HAL #582 -- per-layer KV compression study", section 5
+ * P1: given the number of cache cells (all sequences), the model shape and the byte
+ * budget for the KV cache, walk the ladder
+ *     rung 0 f16/f16,  1 q8_0/q8_0,  2 q8_0 K/q4_0 V,  3 q5_1 K/q4_0 V (floor)
+ * and choose the first (least compressing) rung whose whole cache,
+ *     cells * n_layers * n_kv_heads * head_dim / 32 * (block_bytes(K) + block_bytes(V)),
+ * is at most the budget; when none is, choose the floor and report fits = 0 (the caller
+ * then spills or shortens the context).  The budget arithmetic itself (free memory,
+ * memory already resident, reserve) is the caller's.  Host-only; no GPU call.
+ * Errors: KVQ_ERR_INVALID_ARG for a null out, cells < 0, a non-positive shape, a
+ * head_dim not a multiple of 32, or a size that overflows 64 bits.
+ */
+typedef struct {
+    int32_t rung;     /* 0..3 as above                                             */
+    kvq_type type_k;  /* chosen K type                                             */
+    kvq_type type_v;  /* chosen V type                                             */
+    int32_t fits;     /* 1 if bytes <= budget_bytes                                */
+    uint64_t bytes;   /* whole-cache bytes of the chosen rung                      */
+} kvq_tier_choice;
+KVQ_API kvq_status kvq_select_tier(int64_t cells, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                                   uint64_t budget_bytes, kvq_tier_choice *out);
 
 KVQ_API const char *kvq_status_string(kvq_status status);
 KVQ_API int32_t kvq_abi_version(void);

@@ -159,6 +159,31 @@ def combine(part_o: np.ndarray, part_m: np.ndarray, part_l: np.ndarray):
     return out, lse
 
 
+# Bytes of one 32-value block.  f16, q8_0, q4_0 from the size model table of "HAL #582 --
+# per-layer KV compression study", section 1 (192 / 102 / 54 KiB per token of the 14B
+# shape); q5_1 from the section 5 P1 validation (q5_1 K + q4_0 V = 2016 MiB at 32768
+# cells, i.e. 63 KiB per token, of which q4_0 V is 27).
+BLOCK_BYTES = {"f16": 64, "q8_0": 34, "q4_0": 18, "q5_1": 24}
+TIER_LADDER = [("f16", "f16"), ("q8_0", "q8_0"), ("q8_0", "q4_0"), ("q5_1", "q4_0")]
+
+
+def kv_cache_bytes(cells: int, n_layers: int, n_kv_heads: int, head_dim: int, type_k: str, type_v: str) -> int:
+    """Whole-cache bytes: every cell stores head_dim values per KV head per layer, for K and V."""
+    blocks = cells * n_layers * n_kv_heads * (head_dim // QK)
+    return blocks * (BLOCK_BYTES[type_k] + BLOCK_BYTES[type_v])
+
+
+def select_tier(cells: int, n_layers: int, n_kv_heads: int, head_dim: int, budget_bytes: int) -> dict:
+    """Automatic KV tier (same study, section 5 P1): walk the ladder f16 -> q8/q8 -> q8K/q4V ->
+    q5_1K/q4V and take the first (least compressing) rung whose whole cache fits the budget;
+    if none fits, take the last rung and report that it does not fit."""
+    for rung, (tk, tv) in enumerate(TIER_LADDER):
+        size = kv_cache_bytes(cells, n_layers, n_kv_heads, head_dim, tk, tv)
+        last = rung == len(TIER_LADDER) - 1
+        if size <= budget_bytes or last:
+            return {"rung": rung, "type_k": tk, "type_v": tv, "fits": size <= budget_bytes, "bytes": size}
+
+
 def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
 

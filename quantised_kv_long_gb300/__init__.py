@@ -19,7 +19,9 @@ LIB_PATH = os.path.join(_HERE, "libkvq.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "kvq.h")
 
 F16, Q8_0, Q4_0 = 0, 1, 2
-TYPE_IDS = {"f16": F16, "q8_0": Q8_0, "q4_0": Q4_0}
+Q5_1 = 5  # storage cost only (block_bytes, select_tier)
+TYPE_IDS = {"f16": F16, "q8_0": Q8_0, "q4_0": Q4_0, "q5_1": Q5_1}
+TYPE_NAMES = {v: k for k, v in TYPE_IDS.items()}
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
           4: "KVQ_ERR_ALIGNMENT", 5: "KVQ_ERR_CUDA", 6: "KVQ_ERR_DEVICE", 7: "KVQ_ERR_SCRATCH"}
 DEVERR_CAPACITY, DEVERR_TIMEOUT = 0x1, 0x2
@@ -29,6 +31,11 @@ class KvqError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
         super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+class TierChoice(ctypes.Structure):
+    _fields_ = [("rung", ctypes.c_int32), ("type_k", ctypes.c_int32), ("type_v", ctypes.c_int32),
+                ("fits", ctypes.c_int32), ("bytes", ctypes.c_uint64)]
 
 
 class Desc(ctypes.Structure):
@@ -63,6 +70,10 @@ def _load():
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    L.kvq_select_tier.argtypes = [ctypes.c_int64, i32, i32, i32, ctypes.c_uint64, ctypes.POINTER(TierChoice)]
+    L.kvq_select_tier.restype = ctypes.c_int
+    L.kvq_block_bytes.argtypes = [ctypes.c_int]
+    L.kvq_block_bytes.restype = ctypes.c_int32
     L.kvq_status_string.argtypes = [ctypes.c_int]
     L.kvq_status_string.restype = ctypes.c_char_p
     L.kvq_abi_version.argtypes = []
@@ -102,6 +113,20 @@ def cache_size(batch, n_kv_heads, head_dim, capacity, type_k, type_v):
     _check(lib.kvq_cache_size(ctypes.byref(d), ctypes.byref(kb), ctypes.byref(vb), ctypes.byref(sb)),
            "kvq_cache_size")
     return kb.value, vb.value, sb.value
+
+
+def block_bytes(kv_type) -> int:
+    """Bytes of one 32-value block of a storage type (kvq_block_bytes)."""
+    return int(lib.kvq_block_bytes(_tid(kv_type)))
+
+
+def select_tier(cells, n_layers, n_kv_heads, head_dim, budget_bytes) -> dict:
+    """KV tier ladder choice (kvq_select_tier): rung, K/V type names, fits, whole-cache bytes."""
+    c = TierChoice()
+    _check(lib.kvq_select_tier(cells, n_layers, n_kv_heads, head_dim, budget_bytes, ctypes.byref(c)),
+           "kvq_select_tier")
+    return {"rung": c.rung, "type_k": TYPE_NAMES[c.type_k], "type_v": TYPE_NAMES[c.type_v], "fits": bool(c.fits),
+            "bytes": int(c.bytes)}
 
 
 def _tid(t):

@@ -183,6 +183,42 @@ const char *kvq_status_string(kvq_status s) {
     return "unknown status";
 }
 
+int32_t kvq_block_bytes(kvq_type type) {
+    switch (type) {
+        case KVQ_F16: return 64;
+        case KVQ_Q8_0: return 34;
+        case KVQ_Q4_0: return 18;
+        case KVQ_Q5_1: return 24;
+    }
+    return 0;
+}
+
+kvq_status kvq_select_tier(int64_t cells, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                           uint64_t budget_bytes, kvq_tier_choice *out) {
+    if (!out || cells < 0 || n_layers < 1 || n_kv_heads < 1 || head_dim < 32 || head_dim % 32 != 0)
+        return KVQ_ERR_INVALID_ARG;
+    static const kvq_type ladder[4][2] = {
+        {KVQ_F16, KVQ_F16}, {KVQ_Q8_0, KVQ_Q8_0}, {KVQ_Q8_0, KVQ_Q4_0}, {KVQ_Q5_1, KVQ_Q4_0}};
+    // blocks per cell over all layers and heads, then bytes per rung (overflow-checked)
+    const unsigned __int128 blocks = static_cast<unsigned __int128>(cells) * static_cast<uint64_t>(n_layers) *
+                                     static_cast<uint64_t>(n_kv_heads) * static_cast<uint64_t>(head_dim / 32);
+    for (int r = 0; r < 4; ++r) {
+        const unsigned __int128 b =
+            blocks * static_cast<uint64_t>(kvq_block_bytes(ladder[r][0]) + kvq_block_bytes(ladder[r][1]));
+        if (b > static_cast<unsigned __int128>(~0ull)) return KVQ_ERR_INVALID_ARG;
+        const bool fits = static_cast<uint64_t>(b) <= budget_bytes;
+        if (fits || r == 3) {
+            out->rung = r;
+            out->type_k = ladder[r][0];
+            out->type_v = ladder[r][1];
+            out->fits = fits ? 1 : 0;
+            out->bytes = static_cast<uint64_t>(b);
+            return KVQ_OK;
+        }
+    }
+    return KVQ_ERR_INVALID_ARG;  // not reached
+}
+
 kvq_status kvq_cache_size(const kvq_cache_desc *desc, size_t *k_bytes, size_t *v_bytes, size_t *state_bytes) {
     kvq_status st = check_desc(desc);
     if (st != KVQ_OK) return st;

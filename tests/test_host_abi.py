@@ -103,3 +103,27 @@ def test_null_pointers_rejected_without_cuda():
 
 def test_layout_is_a_bijection():
     kvq_layout.check_bijective()
+
+
+def test_block_bytes():
+    assert [kvq.block_bytes(t) for t in ("f16", "q8_0", "q4_0", "q5_1")] == [64, 34, 18, 24]
+    assert kvq.lib.kvq_block_bytes(9) == 0
+
+
+def test_select_tier_matches_oracle():
+    import oracle
+    shapes = [(32768, 48, 8, 128), (65536, 10, 2, 256), (262144, 48, 8, 128), (1, 1, 1, 32), (0, 4, 4, 64)]
+    for cells, L, H, D in shapes:
+        sizes = [oracle.kv_cache_bytes(cells, L, H, D, tk, tv) for tk, tv in oracle.TIER_LADDER]
+        budgets = {0, 1} | {s + d for s in sizes for d in (-1, 0, 1) if s + d >= 0}
+        for budget in sorted(budgets):
+            assert kvq.select_tier(cells, L, H, D, budget) == oracle.select_tier(cells, L, H, D, budget), \
+                (cells, L, H, D, budget)
+
+
+def test_select_tier_rejects_bad_arguments():
+    c = kvq.TierChoice()
+    for args in [(-1, 48, 8, 128), (1, 0, 8, 128), (1, 48, 0, 128), (1, 48, 8, 100), (1, 48, 8, 0),
+                 (1 << 62, 1 << 20, 1 << 10, 1 << 20)]:
+        assert kvq.lib.kvq_select_tier(*args, 1 << 30, ctypes.byref(c)) == 1, args
+    assert kvq.lib.kvq_select_tier(1, 48, 8, 128, 1 << 30, None) == 1

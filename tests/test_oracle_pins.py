@@ -432,3 +432,48 @@ def test_partials_and_combine():
     assert np.isneginf(m).all() and (l == 0).all() and (o == 0).all()
     out, lse = oracle.combine(o, m, l)
     assert (out == 0).all() and np.isneginf(lse).all()
+
+
+# ---------------------------------------------------------------------------------------
+# automatic KV tier ("HAL #582 -- per-layer KV compression study", section 5 P1)
+# ---------------------------------------------------------------------------------------
+def _tier_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "tier_ladder.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                c = [x.strip() for x in line.split("|")]
+                rows.append((int(c[0]), int(c[1]), int(c[2]), int(c[3]), int(c[4]), c[5], c[6], int(c[7])))
+    return rows
+
+
+@pytest.mark.parametrize("row", _tier_rows())
+def test_tier_ladder_worked_example(row):
+    """The page's validation: each budget picks the printed rung, at the printed size."""
+    cells, L, H, D, budget_mib, tk, tv, kv_mib = row
+    t = oracle.select_tier(cells, L, H, D, budget_mib << 20)
+    assert (t["type_k"], t["type_v"]) == (tk, tv)
+    assert t["fits"] and t["bytes"] == kv_mib << 20
+
+
+def test_tier_ladder_properties():
+    L, H, D, cells = 48, 8, 128, 32768
+    sizes = [oracle.kv_cache_bytes(cells, L, H, D, tk, tv) for tk, tv in oracle.TIER_LADDER]
+    assert sizes == sorted(sizes, reverse=True)            # each rung compresses more
+    assert sizes[0] == 6144 << 20                           # f16: 192 KiB/token (section 1)
+    # f16 whenever it fits, including exactly at the budget
+    assert oracle.select_tier(cells, L, H, D, sizes[0])["rung"] == 0
+    # one byte short of a rung moves one rung down
+    for r in range(3):
+        assert oracle.select_tier(cells, L, H, D, sizes[r] - 1)["rung"] == r + 1
+    # nothing fits: the floor, flagged
+    t = oracle.select_tier(cells, L, H, D, sizes[3] - 1)
+    assert t["rung"] == 3 and not t["fits"]
+    # monotone: a larger budget never picks a more compressing rung
+    prev = 3
+    for budget in range(0, sizes[0] + (64 << 20), 97 << 20):
+        r = oracle.select_tier(cells, L, H, D, budget)["rung"]
+        assert r <= prev
+        prev = r
+    # no cells cost nothing
+    assert oracle.select_tier(0, L, H, D, 0) == {"rung": 0, "type_k": "f16", "type_v": "f16", "fits": True, "bytes": 0}
