@@ -332,6 +332,80 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
     return res
 
 
+def run_window_cell(kvq, torch, wl, window, steps, warmup, peak):
+    """Position-axis mixed cache (f16 window of the last `window` tokens + quantised tail):
+    one step = for every layer, kvq_window_append (1 row, evicting the oldest window row
+    into the tail) + kvq_window_decode (window and tail decodes + exact merge); the layers
+    of a step form one CUDA graph."""
+    stream = torch.cuda.Stream()
+    L, B = wl.layers, wl.batch
+    ctx = wl.lengths[0]
+    extra = 1 + warmup + steps + 8
+    caches = []
+    with torch.cuda.stream(stream):
+        for layer in range(L):
+            c = kvq.WindowedCache(B, wl.n_kv_heads, wl.head_dim, window, ((ctx - window + extra + 15) // 16) * 16,
+                                  wl.type_k, wl.type_v, stream=stream)
+            for b in range(B):
+                K = torch.stack([syn.kv_rows(wl, syn.KIND_K, layer, b, h, 0, ctx) for h in range(wl.n_kv_heads)])
+                V = torch.stack([syn.kv_rows(wl, syn.KIND_V, layer, b, h, 0, ctx) for h in range(wl.n_kv_heads)])
+                c.tail.append(K[None, :, :ctx - window].contiguous(), V[None, :, :ctx - window].contiguous(), b0=b,
+                              stream=stream)
+                c.window.append(K[None, :, ctx - window:].contiguous(), V[None, :, ctx - window:].contiguous(), b0=b,
+                                stream=stream)
+                del K, V
+            caches.append(c)
+        q = torch.stack([syn.queries(wl, layer) for layer in range(L)]).contiguous()
+        news = [syn.new_rows(wl, layer, 0) for layer in range(L)]
+        knew = torch.stack([k[:, :, 0] for k, _ in news]).contiguous()
+        vnew = torch.stack([v[:, :, 0] for _, v in news]).contiguous()
+        out = torch.empty_like(q)
+        lse = torch.empty((L, B, wl.n_q_heads), device=q.device)
+        ws = caches[0].workspace(wl.n_q_heads)
+    torch.cuda.synchronize()
+
+    def step():
+        for layer, c in enumerate(caches):
+            c.append(knew[layer], vnew[layer], stream=stream)
+            c.decode(q[layer], scale=wl.scale, out=out[layer], lse=lse[layer], workspace=ws, stream=stream)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    D, H = wl.head_dim, wl.n_kv_heads
+    bpv = {"f16": 2.0, "q8_0": 34 / 32, "q4_0": 18 / 32}
+    n_tail = ctx - window + 1 + warmup + steps / 2.0  # mean tail length over the timed steps
+    bytes_step = L * B * H * D * (window * 4.0 + n_tail * (bpv[wl.type_k] + bpv[wl.type_v]))
+    err = any(c.window.read_error() or c.tail.read_error() for c in caches)
+    res = {"workload": f"hybrid-{L}L-window{window}-f16+{wl.type_k}-{wl.type_v}-ctx{ctx}", "layers": L, "batch": B,
+           "n_q_heads": wl.n_q_heads, "n_kv_heads": H, "head_dim": D, "kv": f"f16 window + {wl.type_k}/{wl.type_v} tail",
+           "ctx": ctx, "window": window, "steps_per_s": 1000.0 / ms, "ms_per_step": ms,
+           "kv_gbs": bytes_step / (ms * 1e-3) / 1e9, "kv_bytes_per_step": bytes_step,
+           "pct_hbm_peak": 100.0 * bytes_step / (ms * 1e-3) / 1e9 / peak,
+           "step": "per layer: window append (evict oldest into tail) + window decode + tail decode + merge"}
+    if err:
+        res["device_error"] = True
+    del g
+    caches.clear()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def chunk_quantise(kvq, torch, wl, reps=20, warmup=3):
     """The 4096-row prefill-chunk quantise of one layer: fp32 K,V [1,Hkv,4096,D] -> cache."""
     n = 4096
@@ -534,6 +608,8 @@ def main():
             r = run_cell(kvq, torch, w, args.sweep_steps, max(3, min(args.warmup, 5)), peak)
             r.pop("_wall")
             sweep.append(r)
+        sweep.append(run_window_cell(kvq, torch, syn.hybrid(65536, "q8_0", "q8_0"), 4096, args.sweep_steps,
+                                     max(3, min(args.warmup, 5)), peak))
         chunk = chunk_quantise(kvq, torch, syn.multi_session())
     else:
         chunk = None

@@ -245,6 +245,37 @@ KVQ_API kvq_status kvq_combine(const float *part_o, const float *part_m, const f
                        void *stream);
 
 /*
+ * Position-axis mixed cache: an f16 window of the most recent tokens in front of a
+ * quantised tail, "HAL #582 -- per-layer KV compression study", section 5 P2.  Two caches
+ * of one shape (batch, n_kv_heads, head_dim) make the pair: `window` must be f16/f16, its
+ * capacity W is the window length; `tail` has any K/V types and holds the older tokens.
+ *
+ * kvq_window_append: one new row per sequence, k and v fp32 [B][Hkv][D] (device, 16-byte
+ * aligned).  The window is a ring (attention does not depend on key order): the new row
+ * goes to slot (tail_len + window_len) mod W.  While the window is filling, window_len
+ * grows; once it is full, the row in that slot is the oldest one: it is read back from
+ * the window, quantised once into the tail at tail_len (the write path's
+ * quantise-on-eviction; the tail quantises the window's f16 values), and then
+ * overwritten, and tail_len grows.  Both lengths advance on the device, so the call can
+ * be captured in a CUDA graph; the host mirrors advance too.  KVQ_ERR_CAPACITY (nothing
+ * written) when a full window would evict into a full tail; KVQ_ERR_UNSUPPORTED when the
+ * window is not f16/f16; KVQ_ERR_INVALID_ARG for mismatched shapes or the same cache twice.
+ *
+ * kvq_window_decode: decode attention of q [B][Hq][D] over the union of both regions
+ * (window_len + tail_len rows per sequence), written like kvq_decode_attention.  Each
+ * region runs its own typed decode into one set of split triples in `workspace`
+ * (kvq_window_workspace_size bytes; no zeroing needed), and kvq_combine's exact merge
+ * forms the result (the read path of section 5 P2).
+ */
+KVQ_API kvq_status kvq_window_append(kvq_cache *window, kvq_cache *tail, const float *k, const float *v,
+                                     void *stream);
+KVQ_API kvq_status kvq_window_workspace_size(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads,
+                                             size_t *bytes);
+KVQ_API kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *tail, const float *q,
+                                     int32_t n_q_heads, float scale, void *workspace, float *out, float *lse,
+                                     void *stream);
+
+/*
  * kvq_decode_attention without a caller-provided workspace.  (The pages have no
  * counterpart: this entry point exists for callers, not for the method.)
  *

@@ -65,6 +65,9 @@ def _load():
         "kvq_combine": [vp, vp, vp, i32, i32, i32, vp, vp, vp],
         "kvq_decode_attention_noalloc": [vp, vp, i32, ctypes.c_float, i32, vp, vp, vp],
         "kvq_append_decode": [vp, vp, vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp],
+        "kvq_window_append": [vp, vp, vp, vp, vp],
+        "kvq_window_workspace_size": [vp, vp, i32, ctypes.POINTER(sz)],
+        "kvq_window_decode": [vp, vp, vp, i32, ctypes.c_float, vp, vp, vp, vp],
     }
     for name, args in sigs.items():
         fn = getattr(L, name)
@@ -113,6 +116,50 @@ def cache_size(batch, n_kv_heads, head_dim, capacity, type_k, type_v):
     _check(lib.kvq_cache_size(ctypes.byref(d), ctypes.byref(kb), ctypes.byref(vb), ctypes.byref(sb)),
            "kvq_cache_size")
     return kb.value, vb.value, sb.value
+
+
+class WindowedCache:
+    """A rolling f16 window of the most recent `window` tokens in front of a quantised tail
+    (kvq_window_append / kvq_window_decode).  `window` must be a multiple of 16."""
+
+    def __init__(self, batch, n_kv_heads, head_dim, window, tail_capacity, type_k="q8_0", type_v="q8_0",
+                 device=None, stream=None):
+        self.window = KVCache(batch, n_kv_heads, head_dim, window, "f16", "f16", device=device, stream=stream)
+        self.tail = KVCache(batch, n_kv_heads, head_dim, tail_capacity, type_k, type_v, device=device, stream=stream)
+        self.batch, self.n_kv_heads, self.head_dim = batch, n_kv_heads, head_dim
+
+    def append(self, k, v, stream=None):
+        """One new row per sequence: k, v fp32 [B, Hkv, D] (or [B, Hkv, 1, D])."""
+        for t in (k, v):
+            assert t.dtype == torch.float32 and t.is_contiguous()
+            assert t.numel() == self.batch * self.n_kv_heads * self.head_dim
+        _check(lib.kvq_window_append(self.window.handle, self.tail.handle, _ptr(k), _ptr(v), _stream(stream)),
+               "kvq_window_append")
+
+    def workspace_bytes(self, n_q_heads) -> int:
+        b = ctypes.c_size_t()
+        _check(lib.kvq_window_workspace_size(self.window.handle, self.tail.handle, n_q_heads, ctypes.byref(b)),
+               "kvq_window_workspace_size")
+        return b.value
+
+    def workspace(self, n_q_heads):
+        return torch.empty(self.workspace_bytes(n_q_heads), dtype=torch.uint8, device=self.window.device)
+
+    def decode(self, q, scale=None, out=None, lse=None, workspace=None, stream=None):
+        assert q.dtype == torch.float32 and q.is_contiguous() and q.dim() == 3
+        B, Hq, D = q.shape
+        assert B == self.batch and D == self.head_dim
+        scale = 1.0 / math.sqrt(D) if scale is None else scale
+        out = torch.empty_like(q) if out is None else out
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+        ws = self.workspace(Hq) if workspace is None else workspace
+        _check(lib.kvq_window_decode(self.window.handle, self.tail.handle, _ptr(q), Hq, scale, _ptr(ws), _ptr(out),
+                                     _ptr(lse), _stream(stream)), "kvq_window_decode")
+        return out, lse
+
+    def lengths(self):
+        """(window lengths, tail lengths) from the host mirrors."""
+        return self.window.lengths(), self.tail.lengths()
 
 
 def block_bytes(kv_type) -> int:

@@ -91,6 +91,8 @@ kvq::DecodeParams base_params(const kvq_cache *c, const float *q, int32_t n_q_he
     p.D = c->desc.head_dim;
     p.cap_tiles = c->desc.capacity / kvq::kTileRows;
     p.n_splits = splits;
+    p.part_stride = splits;
+    p.part_base = 0;
     p.scale_log2 = scale * 1.44269504088896340736f;
     return p;
 }
@@ -130,7 +132,7 @@ WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits) {
 // evicted, streams without an entry are treated as unknown (no early reads).
 struct StreamRec {
     cudaStream_t stream;
-    const kvq_cache *wrote;  // cache written by the latest library launch on the stream
+    const kvq_cache *wrote[2];  // caches written by the latest library launch on the stream
 };
 constexpr int kTrackSlots = 64;
 std::mutex g_track_mu;
@@ -139,15 +141,16 @@ int g_track_n = 0, g_track_next = 0;
 bool g_track_lost = false;
 
 // Called just before the library enqueues work on `stream` that reads cache `reads`
-// (nullptr: none) and writes cache `writes` (nullptr: none).  Returns whether the reads
-// may start before the previous kernel of the stream completes.
-bool track_launch(cudaStream_t stream, const kvq_cache *reads, const kvq_cache *writes) {
+// (nullptr: none) and writes caches `w0`, `w1` (nullptr: none).  Returns whether the
+// reads may start before the previous kernel of the stream completes.
+bool track_launch(cudaStream_t stream, const kvq_cache *reads, const kvq_cache *w0,
+                  const kvq_cache *w1 = nullptr) {
     std::lock_guard<std::mutex> lock(g_track_mu);
     int i = 0;
     while (i < g_track_n && g_track[i].stream != stream) ++i;
     bool early;
     if (i < g_track_n) {
-        early = g_track[i].wrote != reads;
+        early = g_track[i].wrote[0] != reads && g_track[i].wrote[1] != reads;
     } else {
         early = !g_track_lost;
         if (g_track_n < kTrackSlots) {
@@ -159,7 +162,8 @@ bool track_launch(cudaStream_t stream, const kvq_cache *reads, const kvq_cache *
         }
         g_track[i].stream = stream;
     }
-    g_track[i].wrote = writes;
+    g_track[i].wrote[0] = w0;
+    g_track[i].wrote[1] = w1;
     return early && reads != nullptr;
 }
 
@@ -475,6 +479,114 @@ kvq_status kvq_combine(const float *part_o, const float *part_m, const float *pa
     kvq::CombineParams p{part_o, part_m, part_l, out, lse, rows, n_splits, head_dim};
     track_launch(static_cast<cudaStream_t>(stream), nullptr, nullptr);
     return cuda_status(kvq::launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+// ---- rolling f16 window + quantised tail ----
+static kvq_status check_window_pair(const kvq_cache *window, const kvq_cache *tail) {
+    if (!window || !tail || window == tail) return KVQ_ERR_INVALID_ARG;
+    if (window->desc.type_k != KVQ_F16 || window->desc.type_v != KVQ_F16) return KVQ_ERR_UNSUPPORTED;
+    if (window->desc.batch != tail->desc.batch || window->desc.n_kv_heads != tail->desc.n_kv_heads ||
+        window->desc.head_dim != tail->desc.head_dim)
+        return KVQ_ERR_INVALID_ARG;
+    return KVQ_OK;
+}
+
+kvq_status kvq_window_append(kvq_cache *window, kvq_cache *tail, const float *k, const float *v, void *stream) {
+    kvq_status st = check_window_pair(window, tail);
+    if (st != KVQ_OK) return st;
+    if (!k || !v) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_ALIGNMENT;
+    const int W = window->desc.capacity;
+    for (int b = 0; b < window->desc.batch; ++b)
+        if (window->h_len[b] >= W && static_cast<long long>(tail->h_len[b]) + 1 > tail->desc.capacity)
+            return KVQ_ERR_CAPACITY;
+    kvq::WindowParams p{};
+    p.w_k = window->k_mem;
+    p.w_v = window->v_mem;
+    p.t_kc = tail->k_mem;
+    p.t_ks = tail->desc.type_k == KVQ_F16 ? nullptr : tail->k_mem + tail->k_code_bytes;
+    p.t_vc = tail->v_mem;
+    p.t_vs = tail->desc.type_v == KVQ_F16 ? nullptr : tail->v_mem + tail->v_code_bytes;
+    p.w_len = window->state;
+    p.ticket = window->state + window->desc.batch;
+    p.w_err = window->state + window->desc.batch + 1;
+    p.t_len = tail->state;
+    p.t_err = tail->state + tail->desc.batch + 1;
+    p.k = k;
+    p.v = v;
+    p.B = window->desc.batch;
+    p.Hkv = window->desc.n_kv_heads;
+    p.D = window->desc.head_dim;
+    p.w_cap = W;
+    p.w_cap_tiles = W / kvq::kTileRows;
+    p.t_cap = tail->desc.capacity;
+    p.t_cap_tiles = tail->desc.capacity / kvq::kTileRows;
+    p.total_warps = p.B * p.Hkv * (p.D / kvq::kSlice);
+    track_launch(static_cast<cudaStream_t>(stream), nullptr, window, tail);
+    if (kvq::launch_window_append(tail->desc.type_k, tail->desc.type_v, p, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return KVQ_ERR_CUDA;
+    for (int b = 0; b < window->desc.batch; ++b) {
+        if (window->h_len[b] < W)
+            window->h_len[b] += 1;
+        else
+            tail->h_len[b] += 1;
+    }
+    return KVQ_OK;
+}
+
+static kvq_status window_splits(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads, int *sw, int *stl) {
+    kvq_status st = check_window_pair(window, tail);
+    if (st != KVQ_OK) return st;
+    st = check_q_heads(window, n_q_heads);
+    if (st != KVQ_OK) return st;
+    if (auto_splits(window, n_q_heads, sw) != 0 || auto_splits(tail, n_q_heads, stl) != 0) return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+kvq_status kvq_window_workspace_size(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads,
+                                     size_t *bytes) {
+    if (!bytes) return KVQ_ERR_INVALID_ARG;
+    int sw = 0, stl = 0;
+    kvq_status st = window_splits(window, tail, n_q_heads, &sw, &stl);
+    if (st != KVQ_OK) return st;
+    const size_t rows = static_cast<size_t>(window->desc.batch) * n_q_heads, S = sw + stl;
+    *bytes = 2 * align256(rows * S * 4) + align256(rows * S * window->desc.head_dim * 4);
+    return KVQ_OK;
+}
+
+kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *tail, const float *q, int32_t n_q_heads,
+                             float scale, void *workspace, float *out, float *lse, void *stream) {
+    if (!q || !workspace || !out) return KVQ_ERR_INVALID_ARG;
+    int sw = 0, stl = 0;
+    kvq_status st = window_splits(window, tail, n_q_heads, &sw, &stl);
+    if (st != KVQ_OK) return st;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || (lse && !aligned16(lse)))
+        return KVQ_ERR_ALIGNMENT;
+    const int S = sw + stl;
+    const size_t rows = static_cast<size_t>(window->desc.batch) * n_q_heads;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *pm = reinterpret_cast<float *>(ws);
+    float *pl = reinterpret_cast<float *>(ws + align256(rows * S * 4));
+    float *po = reinterpret_cast<float *>(ws + 2 * align256(rows * S * 4));
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // each region in its own typed launch, both writing into one set of split triples
+    const kvq_cache *region[2] = {window, tail};
+    const int splits[2] = {sw, stl}, base[2] = {0, sw};
+    for (int r = 0; r < 2; ++r) {
+        kvq::DecodeParams p = base_params(region[r], q, n_q_heads, scale, splits[r]);
+        p.part_o = po;
+        p.part_m = pm;
+        p.part_l = pl;
+        p.part_stride = S;
+        p.part_base = base[r];
+        p.early = track_launch(cs, region[r], nullptr) ? 1 : 0;
+        if (kvq::launch_decode(region[r]->desc.type_k, region[r]->desc.type_v, p, false, cs) != cudaSuccess)
+            return KVQ_ERR_CUDA;
+    }
+    kvq::CombineParams c{po, pm, pl, out, lse, static_cast<int>(rows), S, window->desc.head_dim};
+    track_launch(cs, nullptr, nullptr);
+    return cuda_status(kvq::launch_combine(c, cs));
 }
 
 // ---- decode without a caller workspace: scratch compiled into the library ----

@@ -68,7 +68,96 @@ cudaError_t launch_append_t(const AppendParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Rolling f16 window + quantised tail ("HAL #582 -- per-layer KV compression study",
+// section 5 P2 write path): one new row per sequence.  The window is a ring of w_cap rows
+// (attention does not depend on key order); the row written now goes to slot
+// (tail_len + window_len) mod w_cap.  When the window is full, the row in that slot is the
+// oldest: it is read back from the window, quantised once into the tail at tail_len, and
+// only then overwritten.  One warp per (sequence, KV head, slice); the last CTA advances
+// the lengths (window_len up to w_cap, then tail_len).
+template <int TK, int TV>
+__global__ void __launch_bounds__(256) window_append_kernel(const WindowParams p) {
+    __shared__ int s_last;
+    const int lane = threadIdx.x & 31;
+    const int wg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int NS = p.D / kSlice;
+    if (wg < p.total_warps) {
+        const int sl = wg % NS;
+        const int rest = wg / NS;
+        const int h = rest % p.Hkv, b = rest / p.Hkv;
+        const int Lw = __ldcg(p.w_len + b), Lt = __ldcg(p.t_len + b);
+        const bool full = Lw >= p.w_cap;
+        if (Lw >= 0 && Lw <= p.w_cap && Lt >= 0 && (!full || Lt + 1 <= p.t_cap)) {
+            const int slot = static_cast<int>((static_cast<long long>(Lt) + Lw) % p.w_cap);
+            const size_t wtile = (static_cast<size_t>(b) * p.Hkv + h) * p.w_cap_tiles + (slot >> 4);
+            const int wkt = slot & 15;
+            uint8_t *wk = p.w_k + (wtile * NS + sl) * code_tile_bytes(KVQ_F16);
+            uint8_t *wv = p.w_v + (wtile * NS + sl) * code_tile_bytes(KVQ_F16);
+            if (full) {
+                const float4 xk = load_f16_row<false>(wk, wkt, lane);
+                const float4 xv = load_f16_row<true>(wv, wkt, lane);
+                const size_t ttile = (static_cast<size_t>(b) * p.Hkv + h) * p.t_cap_tiles + (Lt >> 4);
+                const int tkt = Lt & 15;
+                quantize_store_vals<TK, false>(xk, p.t_kc + (ttile * NS + sl) * code_tile_bytes(TK),
+                                               p.t_ks + (ttile * NS + sl) * kScaleTile, tkt, lane);
+                quantize_store_vals<TV, true>(xv, p.t_vc + (ttile * NS + sl) * code_tile_bytes(TV),
+                                              p.t_vs + (ttile * NS + sl) * kScaleTile, tkt, lane);
+            }
+            const size_t src = (static_cast<size_t>(b) * p.Hkv + h) * p.D + sl * kSlice + 4 * lane;
+            quantize_store<KVQ_F16, false>(p.k + src, wk, nullptr, wkt, lane);
+            quantize_store<KVQ_F16, true>(p.v + src, wv, nullptr, wkt, lane);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int t = atomicAdd(p.ticket, 1);
+        s_last = (t == static_cast<int>(gridDim.x) - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+            const int Lw = __ldcg(p.w_len + b), Lt = __ldcg(p.t_len + b);
+            if (Lw < 0 || Lw > p.w_cap || Lt < 0) {
+                atomicOr(p.w_err, KVQ_DEVERR_CAPACITY);
+            } else if (Lw < p.w_cap) {
+                p.w_len[b] = Lw + 1;
+            } else if (Lt + 1 <= p.t_cap) {
+                p.t_len[b] = Lt + 1;
+            } else {
+                atomicOr(p.t_err, KVQ_DEVERR_CAPACITY);
+            }
+        }
+        if (threadIdx.x == 0) *p.ticket = 0;
+    }
+}
+
+template <int TK, int TV>
+cudaError_t launch_window_t(const WindowParams &p, cudaStream_t stream) {
+    const int warps_per_block = 8;
+    const int blocks = (p.total_warps + warps_per_block - 1) / warps_per_block;
+    window_append_kernel<TK, TV><<<blocks, 32 * warps_per_block, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_window_append(int tail_k, int tail_v, const WindowParams &p, cudaStream_t stream) {
+#define KVQ_WINDOW_CASE(KT, VT) \
+    if (tail_k == KT && tail_v == VT) return launch_window_t<KT, VT>(p, stream);
+    KVQ_WINDOW_CASE(KVQ_F16, KVQ_F16)
+    KVQ_WINDOW_CASE(KVQ_F16, KVQ_Q8_0)
+    KVQ_WINDOW_CASE(KVQ_F16, KVQ_Q4_0)
+    KVQ_WINDOW_CASE(KVQ_Q8_0, KVQ_F16)
+    KVQ_WINDOW_CASE(KVQ_Q8_0, KVQ_Q8_0)
+    KVQ_WINDOW_CASE(KVQ_Q8_0, KVQ_Q4_0)
+    KVQ_WINDOW_CASE(KVQ_Q4_0, KVQ_F16)
+    KVQ_WINDOW_CASE(KVQ_Q4_0, KVQ_Q8_0)
+    KVQ_WINDOW_CASE(KVQ_Q4_0, KVQ_Q4_0)
+#undef KVQ_WINDOW_CASE
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_append(int type_k, int type_v, const AppendParams &p, cudaStream_t stream) {
 #define KVQ_APPEND_CASE(KT, VT) \

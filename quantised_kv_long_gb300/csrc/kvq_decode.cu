@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
         if (!fused) {  // partials mode: splits beyond ns are empty triples
             for (int idx = threadIdx.x; idx < rows * (p.D / 4); idx += blockDim.x) {
                 const int g = idx / (p.D / 4), dq = idx % (p.D / 4);
-                const size_t pr = (static_cast<size_t>(bseq) * p.Hq + hq0 + g) * p.n_splits + split;
+                const size_t pr = (static_cast<size_t>(bseq) * p.Hq + hq0 + g) * p.part_stride + p.part_base + split;
                 reinterpret_cast<float4 *>(p.part_o + pr * p.D)[dq] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (dq == 0) {
                     p.part_m[pr] = -CUDART_INF_F;
@@ -858,7 +858,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
             if (dq == 0 && p.lse)
                 p.lse[static_cast<size_t>(bseq) * p.Hq + hq] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -CUDART_INF_F;
         } else {
-            const size_t pr = (static_cast<size_t>(bseq) * p.Hq + hq) * p.n_splits + split;
+            const size_t pr = (static_cast<size_t>(bseq) * p.Hq + hq) * p.part_stride + p.part_base + split;
             reinterpret_cast<float4 *>(p.part_o + pr * D)[dq] = acc;
             if (dq == 0) {
                 p.part_m[pr] = M == -CUDART_INF_F ? -CUDART_INF_F : M * kLn2;

@@ -50,7 +50,8 @@ struct DecodeParams {
     int32_t *err;         // device error word
     const float *q;       // [B][Hq][D]
     float *out, *lse;     // [B][Hq][D], [B][Hq] or nullptr
-    float *part_o, *part_m, *part_l;  // [B][Hq][S][D], [B][Hq][S]
+    float *part_o, *part_m, *part_l;  // [B][Hq][part_stride][D], [B][Hq][part_stride]
+    int part_stride, part_base;       // triples per row; slot of this launch's split 0
     int32_t *counters;    // [B][Hkv][QG] (fused mode) or nullptr (partials mode)
     int32_t *counters1;   // [B][Hkv][QG][n_groups_max]: first-level group arrivals
     float *grp_o, *grp_m, *grp_l;  // [B][Hq][n_groups_max][D], [B][Hq][n_groups_max]
@@ -74,6 +75,16 @@ struct AppendParams {
     int32_t *err;
     const float *k, *v;  // [nb][Hkv][n_new][D]
     int b0, nb, n_new, Hkv, D, cap, cap_tiles;
+    int total_warps;
+};
+
+// rolling f16 window + quantised tail: one new row per sequence (kvq_window_append)
+struct WindowParams {
+    uint8_t *w_k, *w_v;                              // window planes (f16: codes only)
+    uint8_t *t_kc, *t_ks, *t_vc, *t_vs;              // tail planes
+    int32_t *w_len, *t_len, *ticket, *w_err, *t_err;
+    const float *k, *v;                              // [B][Hkv][D]
+    int B, Hkv, D, w_cap, w_cap_tiles, t_cap, t_cap_tiles;
     int total_warps;
 };
 
@@ -169,9 +180,11 @@ __device__ __forceinline__ float round_half_away(float y) {
     return t;
 }
 
+// One row of one 128-value slice, lane l holding values 4l..4l+3 (v4), quantised and
+// stored at row kt of the slice's tile (codes, scales: the slice's tile regions).
 template <int T, bool IS_V>
-__device__ __forceinline__ void quantize_store(const float *x, uint8_t *codes, uint8_t *scales, int kt, int lane) {
-    const float4 v4 = *reinterpret_cast<const float4 *>(x);
+__device__ __forceinline__ void quantize_store_vals(const float4 v4, uint8_t *codes, uint8_t *scales, int kt,
+                                                    int lane) {
     const float xs[4] = {v4.x, v4.y, v4.z, v4.w};
     const int dd0 = 4 * lane;   // first value index of this lane inside the slice
     const int b = lane >> 3;    // quantisation block inside the slice
@@ -293,11 +306,45 @@ __device__ __forceinline__ void quantize_store(const float *x, uint8_t *codes, u
     }
 }
 
+template <int T, bool IS_V>
+__device__ __forceinline__ void quantize_store(const float *x, uint8_t *codes, uint8_t *scales, int kt, int lane) {
+    quantize_store_vals<T, IS_V>(*reinterpret_cast<const float4 *>(x), codes, scales, kt, lane);
+}
+
+// The inverse of quantize_store_vals<KVQ_F16, IS_V>: values 4l..4l+3 of row kt of an f16
+// tile slice, widened to fp32 (exact).
+template <bool IS_V>
+__device__ __forceinline__ float4 load_f16_row(const uint8_t *codes, int kt, int lane) {
+    const int dd0 = 4 * lane, b = lane >> 3, i0 = dd0 & 31;
+    const int n = kt & 7, st = kt >> 3;
+    __half h[4];
+    if constexpr (!IS_V) {
+        const int jd = (dd0 & 15) >> 2, hd = i0 >> 4;
+        const uint2 w = *reinterpret_cast<const uint2 *>(codes + (2 * b + st) * 512 + (4 * n + jd) * 16 + hd * 8);
+        const __half2 p0 = u32_as_h2(w.x), p1 = u32_as_h2(w.y);  // (e0, e2), (e1, e3)
+        h[0] = __low2half(p0);
+        h[2] = __high2half(p0);
+        h[1] = __low2half(p1);
+        h[3] = __high2half(p1);
+    } else {
+        int j, pos;
+        pair_slot(kt, j, pos);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = i0 + e, r = i & 15, hv = i >> 4, n2 = r >> 1;
+            h[e] = *reinterpret_cast<const __half *>(codes + (2 * b + hv) * 512 + (4 * n2 + j) * 16 + (r & 1) * 8 +
+                                                     pos * 2);
+        }
+    }
+    return make_float4(__half2float(h[0]), __half2float(h[1]), __half2float(h[2]), __half2float(h[3]));
+}
+
 }  // namespace kvq
 
 // launchers implemented in the .cu files
 namespace kvq {
 cudaError_t launch_append(int type_k, int type_v, const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_window_append(int tail_k, int tail_v, const WindowParams &p, cudaStream_t stream);
 cudaError_t launch_decode(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 cudaError_t decode_occupancy(int type_k, int type_v, int D, int *ctas_per_sm, int *n_sms);
