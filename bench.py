@@ -406,6 +406,59 @@ def run_window_cell(kvq, torch, wl, window, steps, warmup, peak):
     return res
 
 
+def run_verify_cell(kvq, torch, wl, n_q, steps, warmup, peak):
+    """Draft verify: one step = kvq_decode_verify of n_q queries per sequence on every
+    layer (the draft rows are the last n_q cache rows); the layers form one CUDA graph."""
+    stream = torch.cuda.Stream()
+    cell = Cell(kvq, torch, wl, 0, stream)
+    L, B = wl.layers, wl.batch
+    gen = torch.Generator(device="cuda").manual_seed(n_q)
+    q = torch.randn((L, B, n_q, wl.n_q_heads, wl.head_dim), generator=gen, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((L, B, n_q, wl.n_q_heads), device="cuda")
+    b = __import__("ctypes").c_size_t()
+    kvq._check(kvq.lib.kvq_verify_workspace_size(cell.caches[0].handle, n_q, wl.n_q_heads, 0,
+                                                 __import__("ctypes").byref(b)), "kvq_verify_workspace_size")
+    ws = torch.zeros(b.value, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+
+    def step():
+        for layer, c in enumerate(cell.caches):
+            c.verify(q[layer], scale=wl.scale, out=out[layer], lse=lse[layer], workspace=ws, stream=stream)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    bytes_step = step_kv_bytes(wl, list(wl.lengths))
+    res = {"workload": f"verify-nq{n_q}-{wl.name}", "layers": L, "batch": B, "n_q_heads": wl.n_q_heads,
+           "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "kv": f"{wl.type_k}/{wl.type_v}",
+           "ctx": wl.lengths[0] if B == 1 else list(wl.lengths), "n_q": n_q, "steps_per_s": 1000.0 / ms,
+           "ms_per_step": ms, "kv_gbs": bytes_step / (ms * 1e-3) / 1e9, "kv_bytes_per_step": bytes_step,
+           "pct_hbm_peak": 100.0 * bytes_step / (ms * 1e-3) / 1e9 / peak,
+           "step": f"per layer: verify of {n_q} draft queries per sequence (causal within the draft)"}
+    if any(c.read_error() for c in cell.caches):
+        res["device_error"] = True
+    cell.free()
+    del g
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def chunk_quantise(kvq, torch, wl, reps=20, warmup=3):
     """The 4096-row prefill-chunk quantise of one layer: fp32 K,V [1,Hkv,4096,D] -> cache."""
     n = 4096
@@ -609,6 +662,11 @@ def main():
             r.pop("_wall")
             sweep.append(r)
         sweep.append(run_window_cell(kvq, torch, syn.hybrid(65536, "q8_0", "q8_0"), 4096, args.sweep_steps,
+                                     max(3, min(args.warmup, 5)), peak))
+        for n_q in (4, 16):
+            sweep.append(run_verify_cell(kvq, torch, syn.hybrid(65536, "q8_0", "q8_0"), n_q, args.sweep_steps,
+                                         max(3, min(args.warmup, 5)), peak))
+        sweep.append(run_verify_cell(kvq, torch, syn.dense14b(131072, "q8_0", "q4_0"), 4, args.sweep_steps,
                                      max(3, min(args.warmup, 5)), peak))
         chunk = chunk_quantise(kvq, torch, syn.multi_session())
     else:

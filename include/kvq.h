@@ -245,6 +245,27 @@ KVQ_API kvq_status kvq_combine(const float *part_o, const float *part_m, const f
                        void *stream);
 
 /*
+ * Draft verify: decode attention for n_q (1..KVQ_MAX_VERIFY_QUERIES) queries per sequence,
+ * the last n_q cache rows being the draft tokens (appended before, e.g. with
+ * kvq_quantize_append).  Query i (0-based) of sequence b attends causally to positions
+ * [0, len[b] - n_q + i] -- positions past the length or before 0 are not attended (a query
+ * that sees no position gets out = 0, lse = -inf).  "HAL #582 -- per-layer KV compression
+ * study", section 5 P0: the quantised MMA reader serves decode batches of up to 16 query
+ * rows (draft verify) in the same typed kernels.
+ *   q    : fp32 [B][n_q][n_q_heads][D];   out : fp32 [B][n_q][n_q_heads][D]
+ *   lse  : fp32 [B][n_q][n_q_heads] or NULL
+ *   workspace: kvq_verify_workspace_size bytes, zeroed once before first use (as for
+ *   kvq_decode_attention).  Each group of 8 of the n_q * G query rows of a KV head runs
+ *   in its own CTAs, which read the same tiles at the same time (L2 serves the repeats).
+ */
+#define KVQ_MAX_VERIFY_QUERIES 16
+KVQ_API kvq_status kvq_verify_workspace_size(const kvq_cache *cache, int32_t n_q, int32_t n_q_heads,
+                                             int32_t n_splits, size_t *bytes);
+KVQ_API kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int32_t n_q, int32_t n_q_heads,
+                                     float scale, int32_t n_splits, void *workspace, float *out, float *lse,
+                                     void *stream);
+
+/*
  * Position-axis mixed cache: an f16 window of the most recent tokens in front of a
  * quantised tail, "HAL #582 -- per-layer KV compression study", section 5 P2.  Two caches
  * of one shape (batch, n_kv_heads, head_dim) make the pair: `window` must be f16/f16, its

@@ -66,6 +66,8 @@ def _load():
         "kvq_decode_attention_noalloc": [vp, vp, i32, ctypes.c_float, i32, vp, vp, vp],
         "kvq_append_decode": [vp, vp, vp, vp, i32, ctypes.c_float, i32, vp, vp, vp, vp],
         "kvq_window_append": [vp, vp, vp, vp, vp],
+        "kvq_verify_workspace_size": [vp, i32, i32, i32, ctypes.POINTER(sz)],
+        "kvq_decode_verify": [vp, vp, i32, i32, ctypes.c_float, i32, vp, vp, vp, vp],
         "kvq_window_workspace_size": [vp, vp, i32, ctypes.POINTER(sz)],
         "kvq_window_decode": [vp, vp, vp, i32, ctypes.c_float, vp, vp, vp, vp],
     }
@@ -293,6 +295,25 @@ class KVCache:
         ws = self.workspace(Hq, n_splits) if workspace is None else workspace
         _check(lib.kvq_append_decode(self.handle, _ptr(k_new), _ptr(v_new), _ptr(q), Hq, scale, n_splits, _ptr(ws),
                                      _ptr(out), _ptr(lse), _stream(stream)), "kvq_append_decode")
+        return out, lse
+
+    def verify(self, q, scale=None, n_splits=0, out=None, lse=None, workspace=None, stream=None):
+        """Draft verify: q fp32 [B, n_q, Hq, D], the last n_q cache rows being the draft;
+        query i attends to positions [0, len - n_q + i].  Returns (out [B, n_q, Hq, D],
+        lse [B, n_q, Hq])."""
+        assert q.dtype == torch.float32 and q.is_contiguous() and q.dim() == 4
+        B, n_q, Hq, D = q.shape
+        assert B == self.batch and D == self.head_dim
+        scale = 1.0 / math.sqrt(D) if scale is None else scale
+        out = torch.empty_like(q) if out is None else out
+        lse = torch.empty((B, n_q, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+        if workspace is None:
+            b = ctypes.c_size_t()
+            _check(lib.kvq_verify_workspace_size(self.handle, n_q, Hq, n_splits, ctypes.byref(b)),
+                   "kvq_verify_workspace_size")
+            workspace = torch.zeros(b.value, dtype=torch.uint8, device=self.device)
+        _check(lib.kvq_decode_verify(self.handle, _ptr(q), n_q, Hq, scale, n_splits, _ptr(workspace), _ptr(out),
+                                     _ptr(lse), _stream(stream)), "kvq_decode_verify")
         return out, lse
 
     def decode_noalloc(self, q, scale=None, n_splits=0, out=None, lse=None, stream=None):

@@ -46,13 +46,13 @@ size_t state_bytes_for(int32_t batch) { return ((static_cast<size_t>(batch) + 2)
 
 kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-int auto_splits(const kvq_cache *c, int n_q_heads, int *out) {
+int auto_splits(const kvq_cache *c, int n_q_heads, int *out, int n_q = 1) {
     int ctas = 0, sms = 0;
     if (kvq::decode_occupancy(c->desc.type_k, c->desc.type_v, c->desc.head_dim, &ctas, &sms) != cudaSuccess)
         return -1;
     if (ctas < 1) ctas = 1;
     const int G = n_q_heads / c->desc.n_kv_heads;
-    const int QG = (G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    const int QG = (n_q * G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
     const long long units = static_cast<long long>(c->desc.batch) * c->desc.n_kv_heads * QG;
     // one full wave of CTAs; two waves when sequences may differ in length
     const long long target = static_cast<long long>(sms) * ctas * (c->desc.batch > 1 ? 2 : 1);
@@ -65,16 +65,17 @@ int auto_splits(const kvq_cache *c, int n_q_heads, int *out) {
     return 0;
 }
 
-kvq_status check_q_heads(const kvq_cache *c, int32_t n_q_heads) {
+kvq_status check_q_heads(const kvq_cache *c, int32_t n_q_heads, int32_t n_q = 1) {
     if (n_q_heads < 1 || n_q_heads % c->desc.n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
     const long long G = n_q_heads / c->desc.n_kv_heads;
-    const long long QG = (G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    const long long QG = (n_q * G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
     if (static_cast<long long>(c->desc.batch) * QG > 65535) return KVQ_ERR_UNSUPPORTED;
     if (c->desc.n_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     return KVQ_OK;
 }
 
-kvq::DecodeParams base_params(const kvq_cache *c, const float *q, int32_t n_q_heads, float scale, int32_t splits) {
+kvq::DecodeParams base_params(const kvq_cache *c, const float *q, int32_t n_q_heads, float scale, int32_t splits,
+                              int32_t n_q = 1) {
     kvq::DecodeParams p{};
     p.k_codes = c->k_mem;
     p.k_scales = c->desc.type_k == KVQ_F16 ? nullptr : c->k_mem + c->k_code_bytes;
@@ -87,7 +88,8 @@ kvq::DecodeParams base_params(const kvq_cache *c, const float *q, int32_t n_q_he
     p.Hkv = c->desc.n_kv_heads;
     p.Hq = n_q_heads;
     p.G = n_q_heads / c->desc.n_kv_heads;
-    p.QG = (p.G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    p.QG = (n_q * p.G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    p.n_q = n_q;
     p.D = c->desc.head_dim;
     p.cap_tiles = c->desc.capacity / kvq::kTileRows;
     p.n_splits = splits;
@@ -104,11 +106,11 @@ struct WsLayout {
     int n_groups_max;
 };
 
-WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits) {
+WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits, int32_t n_q = 1) {
     WsLayout w{};
     const size_t G = n_q_heads / c->desc.n_kv_heads;
-    const size_t QG = (G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
-    const size_t rows = static_cast<size_t>(c->desc.batch) * n_q_heads;
+    const size_t QG = (n_q * G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    const size_t rows = static_cast<size_t>(c->desc.batch) * n_q * n_q_heads;
     const size_t units = static_cast<size_t>(c->desc.batch) * c->desc.n_kv_heads * QG;
     const size_t ng = static_cast<size_t>(kvq::max_merge_groups(splits));
     w.n_groups_max = static_cast<int>(ng);
@@ -479,6 +481,47 @@ kvq_status kvq_combine(const float *part_o, const float *part_m, const float *pa
     kvq::CombineParams p{part_o, part_m, part_l, out, lse, rows, n_splits, head_dim};
     track_launch(static_cast<cudaStream_t>(stream), nullptr, nullptr);
     return cuda_status(kvq::launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+// ---- draft verify: several queries per sequence, causal within the draft ----
+kvq_status kvq_verify_workspace_size(const kvq_cache *cache, int32_t n_q, int32_t n_q_heads, int32_t n_splits,
+                                     size_t *bytes) {
+    if (!cache || !bytes || n_q < 1 || n_q > KVQ_MAX_VERIFY_QUERIES) return KVQ_ERR_INVALID_ARG;
+    kvq_status st = check_q_heads(cache, n_q_heads, n_q);
+    if (st != KVQ_OK) return st;
+    if (n_splits < 0 || n_splits > kvq::kMaxSplits) return KVQ_ERR_INVALID_ARG;
+    int s = n_splits;
+    if (s == 0 && auto_splits(cache, n_q_heads, &s, n_q) != 0) return KVQ_ERR_CUDA;
+    *bytes = ws_layout(cache, n_q_heads, s, n_q).total;
+    return KVQ_OK;
+}
+
+kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int32_t n_q, int32_t n_q_heads, float scale,
+                             int32_t n_splits, void *workspace, float *out, float *lse, void *stream) {
+    if (!cache || !q || !workspace || !out || n_q < 1 || n_q > KVQ_MAX_VERIFY_QUERIES) return KVQ_ERR_INVALID_ARG;
+    kvq_status st = check_q_heads(cache, n_q_heads, n_q);
+    if (st != KVQ_OK) return st;
+    if (n_splits < 0 || n_splits > kvq::kMaxSplits) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || (lse && !aligned16(lse)))
+        return KVQ_ERR_ALIGNMENT;
+    int s = n_splits;
+    if (s == 0 && auto_splits(cache, n_q_heads, &s, n_q) != 0) return KVQ_ERR_CUDA;
+    const WsLayout w = ws_layout(cache, n_q_heads, s, n_q);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s, n_q);
+    p.out = out;
+    p.lse = lse;
+    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
+    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
+    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
+    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
+    p.n_groups_max = w.n_groups_max;
+    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
+    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
+    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    p.early = track_launch(static_cast<cudaStream_t>(stream), cache, nullptr) ? 1 : 0;
+    return cuda_status(kvq::launch_verify(cache->desc.type_k, cache->desc.type_v, p, static_cast<cudaStream_t>(stream)));
 }
 
 // ---- rolling f16 window + quantised tail ----

@@ -1,900 +1,10 @@
-// kvq_decode.cu -- split-K flash-decode over the block-quantised cache, and the split merge.
-//
-// Method: single-token grouped-query decode attention with the keys of each (sequence,
-// KV head) split into contiguous ranges; each range is attended with an online softmax
-// in fp32 and the ranges are merged exactly ("HAL #582 -- per-layer KV compression
-// study", section 5 P2 read path: "exact online-softmax combine").  The K/V blocks are
-// dequantised in registers while they are read, which is the cure the same study
-// (section 3b, finding 2) gives for a quantised reader that was kernel-bound: throughput
-// has to follow the bytes moved.
-//
-// GB300 mapping (one CTA per (split, KV head, sequence x row-group)):
-//   * warp 0 (producer): 1-D bulk copies (cp.async.bulk, TMA engine) of a run of whole
-//     16-row tiles per stage into a shared-memory ring; completion on mbarriers; every
-//     wait is bounded and reports KVQ_DEVERR_TIMEOUT instead of hanging.
-//   * consumer warps: each owns one tile (and one 128-value slice) per stage.  Tiles are
-//     stored fragment-native (include/kvq.h), so every lane fetches its mma operands
-//     with 16-byte shared loads, converts codes to exact f16 integers with bit tricks
-//     (no I2F), and runs mma.sync m16n8k16 (f16 in, fp32 accumulate).
-//     S = Q K^T: A = [Q_hi ; Q_lo] (M rows 0-7 / 8-15 = up to 8 query heads split into
-//     f16 hi + lo parts, so Q loses nothing), B = K codes (exact), one accumulator per
-//     32-value block, multiplied by the f16 scale afterwards in fp32.
-//     O += P V: the S accumulator layout is the A layout of the next mma, so P never
-//     leaves registers; the V scale of each (row, block) is folded into P, which is
-//     again split into f16 hi + lo rows.
-//   * the CTA merges its warps in shared memory, writes one split triple, and the last
-//     CTA of each (sequence, KV head, row-group) merges all splits (arrival counter).
-#include <math_constants.h>
-
-#include "kvq_internal.cuh"
+// kvq_decode.cu -- single-token decode launches (kvq_decode_kernel.cuh, one query per
+// sequence), the occupancy query behind the automatic split count, and the public merge
+// of split triples.
+#include "kvq_decode_kernel.cuh"
 
 namespace kvq {
 namespace {
-
-constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units): p <= 2^8 between rescales
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// f32 pair -> (f16 hi pair, f16 lo pair) with hi + lo == x to ~2^-22 relative
-__device__ __forceinline__ void split_hi_lo(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const __half2 h = __floats2half2_rn(x0, x1);
-    const float2 hf = __half22float2(h);
-    hi = h2_as_u32(h);
-    lo = h2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
-}
-
-// ---- codes as f16 subnormals ----
-// Code words become mma operands with a permute and a mask.  A q8_0 code is stored as a
-// sign-magnitude byte (bit 7 sign, bits 0..6 |q|); placing the magnitude in the low bits
-// of an f16 half and the sign in bit 15 gives the subnormal q * 2^-24.  A q4_0 low nibble
-// c in the low bits is c * 2^-24 and a high nibble (bits 4..7) is 16c * 2^-24; the offset
-// 8 times the sum of the other operand is removed afterwards.  mma.sync multiplies f16
-// subnormals exactly, so the accumulators hold exact dot products in units of 2^-24 (or
-// 2^-20), and the unit is folded into one final multiply.
-template <uint32_t SEL>
-__device__ __forceinline__ uint32_t prmt(uint32_t a) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, 0, %2;\n" : "=r"(d) : "r"(a), "n"(SEL));
-    return d;
-}
-// bytes 0, 2 / 1, 3 of a word of q8_0 codes as two f16 halves: byte, then its sign
-// replicated (selector nibble with bit 3 set), masked to sign bit and magnitude
-__device__ __forceinline__ uint32_t q8_02(uint32_t w) { return prmt<0xA280u>(w) & 0x807f807fu; }
-__device__ __forceinline__ uint32_t q8_13(uint32_t w) { return prmt<0xB391u>(w) & 0x807f807fu; }
-constexpr uint32_t kNibLo = 0x000f000fu, kNibHi = 0x00f000f0u;
-constexpr float kTwo24 = 16777216.0f, kTwo20 = 1048576.0f;
-constexpr float kQ4Offset = 8.0f;  // q4_0 value = scale * (c - 8)
-
-// packed fp32 pair arithmetic (one instruction per pair)
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n add.rn.f32x2 rd, ra, rb;\n"
-        " mov.b64 {%0, %1}, rd;\n}\n"
-        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
-        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
-        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-// Split triples of one row group up to this size are merged in one level (one CTA reads
-// them all); larger sets use two levels so that no single CTA reads too much.
-constexpr int kDirectMergeBytes = 96 * 1024;
-constexpr int kMaxMergeWidth = 32;  // ceil(sqrt(kMaxSplits)): widest merge of either level
-
-__device__ __forceinline__ int group_size(int ns) {
-    int g = 1;
-    while (g * g < ns) ++g;
-    return g;
-}
-
-// All threads of the CTA call this after writing their results.  Returns true in the
-// CTA that is the target-th to arrive on *counter (it then sees every earlier write).
-__device__ __forceinline__ bool arrive_last(int32_t *counter, int target, int &s_flag) {
-    __threadfence();  // each thread publishes its own writes
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int t = atomicAdd(counter, 1);
-        s_flag = (t == target - 1);
-    }
-    __syncthreads();
-    const bool last = s_flag != 0;
-    if (last) __threadfence();
-    return last;
-}
-
-// Merge NP split triples (o, m, l) of `rows` consecutive query rows starting at row0:
-//   M = max_s m_s, w_s = exp(m_s - M), O = sum_s w_s o_s, L = sum_s w_s l_s.
-// Triples of row r, split s live at (r * stride + s0 + s).  Writes either the normalised
-// output (out = O / L, lse = M + log L) or one unnormalised triple at (r * q_stride + q_s).
-// The inputs were written by other CTAs and sit in L2.  Each thread owns two output
-// columns and merges up to kMergeChunk splits per L2 round trip, loading m, l and o
-// together and keeping a running maximum (rescaling when it grows), so a merge of up to
-// kMergeChunk splits costs one round trip and needs no shared memory or barrier.
-constexpr int kMergeChunk = 10;
-__device__ void merge_rows(const float *po, const float *pm, const float *pl, int stride, int s0, int NP,
-                           size_t row0, int rows, int D, float *out, float *lse, float *qo, float *qm, float *ql,
-                           int q_stride, int q_s) {
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    const int DQ = D / 4;
-    const int C = rows * DQ;
-    const float4 *po4 = reinterpret_cast<const float4 *>(po);
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = 0; base < C; base += 2 * nthr) {
-        int col[2], g[2], dq[2];
-        bool v[2];
-        float M[2], L[2];
-        float4 A[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            col[k] = base + tid + k * nthr;
-            v[k] = col[k] < C;
-            g[k] = v[k] ? col[k] / DQ : 0;
-            dq[k] = v[k] ? col[k] % DQ : 0;
-            M[k] = -CUDART_INF_F;
-            L[k] = 0.f;
-            A[k] = z4;
-        }
-        for (int sc = 0; sc < NP; sc += kMergeChunk) {
-            float mm[2][kMergeChunk], ll[2][kMergeChunk];
-            float4 oo[2][kMergeChunk];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const size_t pr = (row0 + g[k]) * stride + s0 + sc;
-#pragma unroll
-                for (int u = 0; u < kMergeChunk; ++u) {
-                    const bool in = v[k] && (sc + u < NP);
-                    mm[k][u] = in ? __ldcg(pm + pr + u) : -CUDART_INF_F;
-                    ll[k][u] = in ? __ldcg(pl + pr + u) : 0.f;
-                    oo[k][u] = in ? __ldcg(po4 + (pr + u) * DQ + dq[k]) : z4;
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                float cm = -CUDART_INF_F;
-#pragma unroll
-                for (int u = 0; u < kMergeChunk; ++u) cm = fmaxf(cm, mm[k][u]);
-                const float Mn = fmaxf(M[k], cm);
-                if (Mn == -CUDART_INF_F) continue;  // nothing but empty splits so far
-                const float a = M[k] == -CUDART_INF_F ? 0.f : expf(M[k] - Mn);
-                A[k].x *= a;
-                A[k].y *= a;
-                A[k].z *= a;
-                A[k].w *= a;
-                L[k] *= a;
-#pragma unroll
-                for (int u = 0; u < kMergeChunk; ++u) {
-                    const float w = mm[k][u] == -CUDART_INF_F ? 0.f : expf(mm[k][u] - Mn);
-                    A[k].x = fmaf(w, oo[k][u].x, A[k].x);
-                    A[k].y = fmaf(w, oo[k][u].y, A[k].y);
-                    A[k].z = fmaf(w, oo[k][u].z, A[k].z);
-                    A[k].w = fmaf(w, oo[k][u].w, A[k].w);
-                    L[k] = fmaf(w, ll[k][u], L[k]);
-                }
-                M[k] = Mn;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            if (!v[k]) continue;
-            if (out) {
-                const float inv = L[k] > 0.f ? 1.f / L[k] : 0.f;
-                reinterpret_cast<float4 *>(out + (row0 + g[k]) * D)[dq[k]] =
-                    make_float4(A[k].x * inv, A[k].y * inv, A[k].z * inv, A[k].w * inv);
-                if (dq[k] == 0 && lse) lse[row0 + g[k]] = L[k] > 0.f ? M[k] + logf(L[k]) : -CUDART_INF_F;
-            } else {
-                const size_t dr = (row0 + g[k]) * static_cast<size_t>(q_stride) + q_s;
-                reinterpret_cast<float4 *>(qo + dr * D)[dq[k]] = A[k];
-                if (dq[k] == 0) {
-                    qm[dr] = M[k];
-                    ql[dr] = L[k];
-                }
-            }
-        }
-    }
-}
-
-// Fused append: every CTA of the grid arrives once, after it has read the lengths; the
-// last one advances len[b] by one for each sequence that had room (else it reports
-// KVQ_DEVERR_CAPACITY) and resets the ticket.  Called by one thread per CTA.
-__device__ __noinline__ void grid_ticket(const DecodeParams &p, int cap_rows) {
-    __threadfence();
-    const int total = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
-    if (atomicAdd(p.ticket, 1) != total - 1) return;
-    __threadfence();
-    int32_t *len = const_cast<int32_t *>(p.len);
-    for (int b = 0; b < p.B; ++b) {
-        const int Lb = __ldcg(len + b);
-        if (Lb >= 0 && Lb + 1 <= cap_rows)
-            len[b] = Lb + 1;
-        else
-            atomicOr(p.err, KVQ_DEVERR_CAPACITY);
-    }
-    *p.ticket = 0;
-}
-
-template <int KT, int VT, int NS>
-struct Cfg {
-    static constexpr int TW = NS == 1 ? 8 : 4;  // tile-warps (per 128-value slice)
-    static constexpr int CW = TW * NS;         // consumer warps
-    static constexpr int THREADS = 32 * (CW + 1);
-    static constexpr int KC = code_tile_bytes(KT) * NS;
-    static constexpr int VC = code_tile_bytes(VT) * NS;
-    static constexpr int KS = scale_tile_bytes(KT) * NS;
-    static constexpr int VS = scale_tile_bytes(VT) * NS;
-    static constexpr int TILE = KC + VC + KS + VS;
-    static constexpr int MIN_CTAS = 1;         // one CTA per SM: 8 consumer warps + 1 producer
-    static constexpr int RING_BUDGET = 196608;
-    // tiles each warp takes per stage: two (32 keys share one softmax step) when the ring
-    // still holds at least two stages, else one
-    static constexpr int TPW = (2 * 2 * TW * TILE <= RING_BUDGET) ? 2 : 1;
-    static constexpr int TWT = TW * TPW;       // tiles per stage
-    static constexpr int STAGE = TWT * TILE;
-    static constexpr int STAGES_RAW = RING_BUDGET / STAGE;
-    static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 16 ? 16 : STAGES_RAW);
-    static constexpr int RING = STAGES * STAGE;
-    static constexpr int XCHG = NS == 2 ? TW * 2 * 2 * 32 * 16 * TPW : 0;
-    static constexpr int BAR_OFF = RING + XCHG;
-    // per consumer warp: the K code-offset corrections of its 8 rows x 4 blocks
-    static constexpr int KCOR_OFF = (BAR_OFF + 2 * STAGES * 8 + 15) / 16 * 16;
-    static constexpr int SMEM = KCOR_OFF + CW * 128 + 16;
-    static constexpr int D = NS * kSlice;
-    // merge / combine scratch reuses the ring
-    static_assert(TW * kMaxRowsPerGroup * D * 4 + 2 * TW * kMaxRowsPerGroup * 4 <= RING, "merge buffer");
-};
-
-// Scores of one tile over this warp's 128-value slice for keys A=2j, B=2j+1 (S-tile 0) and
-// C=8+2j, D=9+2j (S-tile 1), row g = lane/4, in log2 units (Q was prescaled).
-template <int KT>
-__device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks, const uint32_t (&qa)[8][4],
-                                            const uint8_t *kcor, int lane, int j, float (&s)[4]) {
-    if constexpr (KT == KVQ_F16) {
-        float acc[2][4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const uint4 w0 = lds128(kc + (2 * b + 0) * 512 + lane * 16);
-            const uint4 w1 = lds128(kc + (2 * b + 1) * 512 + lane * 16);
-            if (b == 0) {
-                mma_16816_z(acc[0], qa[0], w0.x, w0.y);
-                mma_16816_z(acc[1], qa[0], w1.x, w1.y);
-            } else {
-                mma_16816(acc[0], qa[2 * b], w0.x, w0.y);
-                mma_16816(acc[1], qa[2 * b], w1.x, w1.y);
-            }
-            mma_16816(acc[0], qa[2 * b + 1], w0.z, w0.w);
-            mma_16816(acc[1], qa[2 * b + 1], w1.z, w1.w);
-        }
-        s[0] = acc[0][0] + acc[0][2];
-        s[1] = acc[0][1] + acc[0][3];
-        s[2] = acc[1][0] + acc[1][2];
-        s[3] = acc[1][1] + acc[1][3];
-    } else {
-        // accumulators hold sum q * code in units of 2^-24 (q8_0) or, with the low-nibble
-        // chunk of Q prescaled by 16, sum q * c in units of 2^-20 (q4_0), where
-        // kcorr[b] = -8 * sum_b q in the same unit turns c into the code value c - 8
-        float kcorr[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (KT == KVQ_Q4_0) {
-            const float4 kc4 = *reinterpret_cast<const float4 *>(kcor);
-            kcorr[0] = kc4.x;
-            kcorr[1] = kc4.y;
-            kcorr[2] = kc4.z;
-            kcorr[3] = kc4.w;
-        }
-        const uint4 sc0 = lds128(ks + j * 32), sc1 = lds128(ks + j * 32 + 16);
-        const uint32_t kscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
-        float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
-        uint4 wq4 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            float acc[2][4];
-            if constexpr (KT == KVQ_Q8_0) {
-                const uint4 w = lds128(kc + b * 512 + lane * 16);
-                mma_16816_z(acc[0], qa[2 * b], q8_02(w.x), q8_13(w.x));
-                mma_16816(acc[0], qa[2 * b + 1], q8_02(w.y), q8_13(w.y));
-                mma_16816_z(acc[1], qa[2 * b], q8_02(w.z), q8_13(w.z));
-                mma_16816(acc[1], qa[2 * b + 1], q8_02(w.w), q8_13(w.w));
-            } else {
-                if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
-                const uint32_t w0 = (b & 1) ? wq4.z : wq4.x, w0s = w0 >> 8;
-                const uint32_t w1 = (b & 1) ? wq4.w : wq4.y, w1s = w1 >> 8;
-                mma_16816_z(acc[0], qa[2 * b], w0 & kNibLo, w0s & kNibLo);
-                mma_16816(acc[0], qa[2 * b + 1], w0 & kNibHi, w0s & kNibHi);
-                mma_16816_z(acc[1], qa[2 * b], w1 & kNibLo, w1s & kNibLo);
-                mma_16816(acc[1], qa[2 * b + 1], w1 & kNibHi, w1s & kNibHi);
-            }
-            const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
-            const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
-            float2 t01 = add2(make_float2(acc[0][0], acc[0][1]), make_float2(acc[0][2], acc[0][3]));
-            float2 t23 = add2(make_float2(acc[1][0], acc[1][1]), make_float2(acc[1][2], acc[1][3]));
-            if constexpr (KT == KVQ_Q4_0) {
-                const float2 cb = make_float2(kcorr[b], kcorr[b]);
-                t01 = add2(t01, cb);
-                t23 = add2(t23, cb);
-            }
-            s01 = fma2(dab, t01, s01);
-            s23 = fma2(dcd, t23, s23);
-        }
-        constexpr float unit = KT == KVQ_Q8_0 ? kTwo24 : kTwo20;
-        s[0] = s01.x * unit;
-        s[1] = s01.y * unit;
-        s[2] = s23.x * unit;
-        s[3] = s23.y * unit;
-    }
-}
-
-// O += P V for one tile over this warp's slice.  pk: probabilities of keys A,B,C,D of row g;
-// vmask: which of A,B,C,D are inside the sequence (rows past the length may hold any bits).
-template <int VT, bool PARTIAL>
-__device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, const float (&pk)[4],
-                                        const bool (&vmask)[4], int lane, int j, float (&o)[16][4],
-                                        uint32_t magic) {
-    if constexpr (VT == KVQ_F16) {
-        uint32_t a[4];
-        split_hi_lo(pk[0], pk[1], a[0], a[1]);
-        split_hi_lo(pk[2], pk[3], a[2], a[3]);
-        const uint32_t mab = (vmask[0] ? 0x0000ffffu : 0u) | (vmask[1] ? 0xffff0000u : 0u);
-        const uint32_t mcd = (vmask[2] ? 0x0000ffffu : 0u) | (vmask[3] ? 0xffff0000u : 0u);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            uint4 w0 = lds128(vc + (2 * b + 0) * 512 + lane * 16);
-            uint4 w1 = lds128(vc + (2 * b + 1) * 512 + lane * 16);
-            if constexpr (PARTIAL) {
-                w0.x &= mab;
-                w0.y &= mcd;
-                w0.z &= mab;
-                w0.w &= mcd;
-                w1.x &= mab;
-                w1.y &= mcd;
-                w1.z &= mab;
-                w1.w &= mcd;
-            }
-            mma_16816(o[4 * b + 0], a, w0.x, w0.y);
-            mma_16816(o[4 * b + 1], a, w0.z, w0.w);
-            mma_16816(o[4 * b + 2], a, w1.x, w1.y);
-            mma_16816(o[4 * b + 3], a, w1.z, w1.w);
-        }
-    } else {
-        // P' = p x scale per (key, block) as f16 hi + lo: p is split once per tile
-        // (p = ph + pl), then per block  hi = ph*d,  err = fma(ph, d, -hi) (exact: the
-        // rounding error of an f16 product), lo = fma(pl, d, err)  -- three packed f16 ops
-        // per key pair, about 2^-21 relative.  The scale half2 words already pair keys
-        // (A,B) and (C,D), matching the A-fragment pairs.
-        uint32_t ph_ab, pl_ab, ph_cd, pl_cd;
-        split_hi_lo(pk[0], pk[1], ph_ab, pl_ab);
-        split_hi_lo(pk[2], pk[3], ph_cd, pl_cd);
-        const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
-        const uint32_t vscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
-        uint32_t mab = 0xffffffffu, mcd = 0xffffffffu;
-        if constexpr (PARTIAL) {  // scales past the length may hold any bits
-            mab = (vmask[0] ? 0x0000ffffu : 0u) | (vmask[1] ? 0xffff0000u : 0u);
-            mcd = (vmask[2] ? 0x0000ffffu : 0u) | (vmask[3] ? 0xffff0000u : 0u);
-        }
-        uint4 wq4 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const __half2 dab = u32_as_h2(vscale[b][0] & mab);
-            const __half2 dcd = u32_as_h2(vscale[b][1] & mcd);
-            const __half2 hab = __hmul2(u32_as_h2(ph_ab), dab);
-            const __half2 hcd = __hmul2(u32_as_h2(ph_cd), dcd);
-            const __half2 eab = __hfma2(u32_as_h2(ph_ab), dab, __hneg2(hab));
-            const __half2 ecd = __hfma2(u32_as_h2(ph_cd), dcd, __hneg2(hcd));
-            uint32_t a[4];
-            a[0] = h2_as_u32(hab);
-            a[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), dab, eab));
-            a[2] = h2_as_u32(hcd);
-            a[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), dcd, ecd));
-            // o accumulates sum P' * code in units of 2^-24 (q4_0 high nibbles: 16c); for
-            // q4_0, corr column b accumulates sum P' of block b (B = 1.0 in column b), which
-            // removes the code offset 8 at the end
-            if constexpr (VT == KVQ_Q8_0) {
-                const uint4 w = lds128(vc + b * 512 + lane * 16);
-                mma_16816(o[4 * b + 0], a, q8_02(w.x), q8_13(w.x));
-                mma_16816(o[4 * b + 1], a, q8_02(w.y), q8_13(w.y));
-                mma_16816(o[4 * b + 2], a, q8_02(w.z), q8_13(w.z));
-                mma_16816(o[4 * b + 3], a, q8_02(w.w), q8_13(w.w));
-            } else {
-                // q4_0 V: exact f16 values c - 8 by the magic-number route (nibble | 0x6400 is
-                // 1024 + c; the high nibble gives 1024 + 16c, scaled by 1/16 and less 72)
-                if ((b & 1) == 0) wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
-                const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x, wq0s = wq0 >> 8;  // bytes 2n'   of the block
-                const uint32_t wq1 = (b & 1) ? wq4.w : wq4.y, wq1s = wq1 >> 8;  // bytes 2n'+1 of the block
-                const __half2 k1032 = __float2half2_rn(1032.0f), k16th = __float2half2_rn(0.0625f),
-                              km72 = __float2half2_rn(-72.0f);
-                auto lo = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2((x & kNibLo) | magic), k1032)); };
-                auto hi = [&](uint32_t x) { return h2_as_u32(__hfma2(u32_as_h2((x & kNibHi) | magic), k16th, km72)); };
-                mma_16816(o[4 * b + 0], a, lo(wq0), lo(wq0s));
-                mma_16816(o[4 * b + 2], a, hi(wq0), hi(wq0s));
-                mma_16816(o[4 * b + 1], a, lo(wq1), lo(wq1s));
-                mma_16816(o[4 * b + 3], a, hi(wq1), hi(wq1s));
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
-
-// Cache tiles this CTA starts with, pulled into L2 while the previous kernel of the stream
-// drains (called before the programmatic-launch wait).  Only a hint: the length read here
-// may be one append behind and the tiles may still be written; L2 is the coherence point,
-// so later reads see every write either way.  Capped per CTA so that the prefetched set of
-// all CTAs stays well inside L2.
-constexpr int kPrefetchBytes = 384 * 1024;
-template <class C>
-__device__ __noinline__ void prefetch_split(const DecodeParams &p, int bseq, int h, int split, int cap_rows,
-                                            int skip_tiles) {
-    int L = *reinterpret_cast<const volatile int32_t *>(p.len + bseq);
-    if (p.k_new != nullptr) ++L;
-    L = L < 0 ? 0 : (L > cap_rows ? cap_rows : L);
-    const int T = (L + kTileRows - 1) / kTileRows;
-    const int ns = max(1, min(p.n_splits, T));
-    if (split >= ns || T == 0) return;
-    const int tps = (T + ns - 1) / ns;
-    const int t0 = min(T, split * tps + skip_tiles), t1 = min(T, split * tps + tps);
-    const int nt = min(t1 - t0, kPrefetchBytes / C::TILE - skip_tiles);
-    if (nt <= 0) return;
-    const size_t bt = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + t0;
-    constexpr int kChunk = 32768;
-    auto pf = [](const uint8_t *base, size_t bytes) {
-        for (size_t o = 0; o < bytes; o += kChunk)
-            bulk_prefetch_l2(base + o, static_cast<uint32_t>(min(static_cast<size_t>(kChunk), bytes - o)));
-    };
-    pf(p.k_codes + bt * C::KC, static_cast<size_t>(nt) * C::KC);
-    pf(p.v_codes + bt * C::VC, static_cast<size_t>(nt) * C::VC);
-    if constexpr (C::KS > 0) pf(p.k_scales + bt * C::KS, static_cast<size_t>(nt) * C::KS);
-    if constexpr (C::VS > 0) pf(p.v_scales + bt * C::VS, static_cast<size_t>(nt) * C::VS);
-}
-
-template <int KT, int VT, int NS>
-__global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
-    using C = Cfg<KT, VT, NS>;
-    constexpr int TPW = C::TPW;
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int s_flag;
-    __shared__ int s_timeout;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, h = blockIdx.y;
-    const int bseq = blockIdx.z / p.QG, qg = blockIdx.z % p.QG;
-    const int cap_rows = p.cap_tiles * kTileRows;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *empty = full + C::STAGES;
-    if (threadIdx.x == 0) {  // shared memory only: may run before the wait below
-        for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(full + i, 1);
-            mbar_init(empty + i, C::CW);
-        }
-        fence_mbar_init();
-        s_timeout = 0;
-    }
-    __syncthreads();
-    // Programmatic dependent launch.  Global memory that the previous kernel of the stream
-    // may write (queries, new rows, outputs, workspace, and in general the cache) is read
-    // only after griddepcontrol.wait.  With p.early set the host has established that the
-    // previous kernel does not write this cache, so its lengths and tiles are final already:
-    // the lengths are read at once and the producer fills the ring before the wait.  Every
-    // CTA releases its dependents only after its own wait, so while a kernel runs its
-    // pre-wait part at most one earlier kernel of the stream can still be running.
-    const bool early = p.early != 0;
-    if (!early) {
-        if (threadIdx.x == 0) prefetch_split<C>(p, bseq, h, split, cap_rows, 0);
-        grid_dep_wait();
-    }
-    int L_old = __ldcg(p.len + bseq);
-    L_old = L_old < 0 ? 0 : (L_old > cap_rows ? cap_rows : L_old);
-    // fused append: the new row lands at position L_old and is attended to
-    const bool appending = p.k_new != nullptr;
-    const bool do_app = appending && L_old + 1 <= cap_rows;
-    const int L = do_app ? L_old + 1 : L_old;
-    const int T = (L + kTileRows - 1) / kTileRows;
-    const int ns = max(1, min(p.n_splits, T));
-    const int tps = T > 0 ? (T + ns - 1) / ns : 0;
-    const int rows = min(kMaxRowsPerGroup, p.G - qg * kMaxRowsPerGroup);
-    const int hq0 = h * p.G + qg * kMaxRowsPerGroup;  // first query head of this CTA
-
-    if (split >= ns) {
-        if (early) grid_dep_wait();
-        grid_dep_launch();
-        if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
-        if (!fused) {  // partials mode: splits beyond ns are empty triples
-            for (int idx = threadIdx.x; idx < rows * (p.D / 4); idx += blockDim.x) {
-                const int g = idx / (p.D / 4), dq = idx % (p.D / 4);
-                const size_t pr = (static_cast<size_t>(bseq) * p.Hq + hq0 + g) * p.part_stride + p.part_base + split;
-                reinterpret_cast<float4 *>(p.part_o + pr * p.D)[dq] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (dq == 0) {
-                    p.part_m[pr] = -CUDART_INF_F;
-                    p.part_l[pr] = 0.f;
-                }
-            }
-        }
-        return;
-    }
-    const int t_begin = min(T, split * tps), t_end = min(T, t_begin + tps);
-    const int n_stage = (t_end - t_begin + C::TWT - 1) / C::TWT;
-
-    const size_t bh_tile = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles;
-
-    // per-consumer results kept until the merge
-    float m_run = -CUDART_INF_F, l_acc = 0.f;
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    int tw = 0, sl = 0;
-
-    if (warp == 0) {
-        // ---------------- producer ----------------
-        // In fused-append mode the CTA whose split holds the last tile first writes the new
-        // row of its KV head into that tile (all 32 lanes quantise), then copies it in.
-        const bool owner = do_app && t_begin < T && t_end == T;
-        const int app_stage = owner ? (T - 1 - t_begin) / C::TWT : -1;
-        int issued_use[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) issued_use[i] = -1;
-        // one stage: up to TWT tiles of K codes, V codes, K scales, V scales (lane 0 only)
-        auto issue = [&](int k, int slot, int use) {
-            const int t0 = t_begin + k * C::TWT;
-            const int nt = min(C::TWT, t_end - t0);
-            uint8_t *st = smem + slot * C::STAGE;
-            mbar_arrive_expect_tx(full + slot, static_cast<uint32_t>(nt * C::TILE));
-            bulk_g2s(st, p.k_codes + (bh_tile + t0) * C::KC, nt * C::KC, full + slot);
-            bulk_g2s(st + C::TWT * C::KC, p.v_codes + (bh_tile + t0) * C::VC, nt * C::VC, full + slot);
-            if constexpr (C::KS > 0)
-                bulk_g2s(st + C::TWT * (C::KC + C::VC), p.k_scales + (bh_tile + t0) * C::KS, nt * C::KS, full + slot);
-            if constexpr (C::VS > 0)
-                bulk_g2s(st + C::TWT * (C::KC + C::VC + C::KS), p.v_scales + (bh_tile + t0) * C::VS, nt * C::VS,
-                         full + slot);
-            issued_use[slot] = use;
-        };
-        // early mode: fill the ring before the wait, up to (not including) the stage that
-        // holds the row this kernel appends
-        int k0 = 0;
-        if (early) {
-            k0 = min(n_stage, C::STAGES);
-            if (app_stage >= 0) k0 = min(k0, app_stage);
-            if (lane == 0) {
-                for (int k = 0; k < k0; ++k) issue(k, k, 0);
-                prefetch_split<C>(p, bseq, h, split, cap_rows, k0 * C::TWT);
-            }
-            __syncwarp();
-            grid_dep_wait();
-        }
-        grid_dep_launch();
-        bool ok = true;
-        int slot = k0 == C::STAGES ? 0 : k0, use = k0 == C::STAGES ? 1 : 0;
-        for (int k = k0; k < n_stage; ++k) {
-            bool ok_k = true;
-            if (lane == 0 && use > 0) ok_k = mbar_wait(empty + slot, (use - 1) & 1);
-            if (!__shfl_sync(0xffffffffu, ok_k ? 1 : 0, 0)) {
-                ok = false;
-                break;
-            }
-            if (k == app_stage) {
-                const size_t tile = bh_tile + (L_old >> 4);
-                const int kt = L_old & 15;
-                const float *kx = p.k_new + (static_cast<size_t>(bseq) * p.Hkv + h) * p.D;
-                const float *vx = p.v_new + (static_cast<size_t>(bseq) * p.Hkv + h) * p.D;
-#pragma unroll
-                for (int s2 = 0; s2 < NS; ++s2) {
-                    quantize_store<KT, false>(kx + s2 * kSlice + 4 * lane,
-                                              const_cast<uint8_t *>(p.k_codes) + tile * C::KC + s2 * code_tile_bytes(KT),
-                                              const_cast<uint8_t *>(p.k_scales) + tile * C::KS + s2 * kScaleTile, kt, lane);
-                    quantize_store<VT, true>(vx + s2 * kSlice + 4 * lane,
-                                             const_cast<uint8_t *>(p.v_codes) + tile * C::VC + s2 * code_tile_bytes(VT),
-                                             const_cast<uint8_t *>(p.v_scales) + tile * C::VS + s2 * kScaleTile, kt, lane);
-                }
-                // order these generic-proxy stores before the bulk copy (async proxy) that reads them
-                asm volatile("fence.proxy.async.global;\n" ::: "memory");
-                __syncwarp();
-            }
-            if (lane == 0) issue(k, slot, use);
-            __syncwarp();
-            if (++slot == C::STAGES) {
-                slot = 0;
-                ++use;
-            }
-        }
-        // the length advance of a fused append, off the consumers' critical path
-        if (appending && lane == 0) grid_ticket(p, cap_rows);
-        if (!ok && lane == 0) {
-            atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
-            s_timeout = 1;
-            // let the copies already issued land before the CTA can exit
-            for (int i = 0; i < C::STAGES; ++i)
-                if (issued_use[i] >= 0) (void)mbar_wait(full + i, issued_use[i] & 1);
-        }
-    } else {
-        // ---------------- consumers ----------------
-        if (early) grid_dep_wait();
-        grid_dep_launch();
-        const int cw = warp - 1;
-        tw = cw / NS;
-        sl = cw % NS;
-        const int g = lane >> 2, j = lane & 3;
-
-        // Q fragments (scaled to log2 units, split into f16 hi + lo rows).  For q4_0 keys the
-        // low-nibble chunk of each block is prescaled by 16 (exact) to match the high
-        // nibbles, which arrive as 16c, and kcorr[b] = -8 times the block's sum of q in the
-        // accumulator unit is kept for each row.
-        uint32_t qa[8][4];
-        uint8_t *kcor_row = smem + C::KCOR_OFF + cw * 128 + g * 16;
-        {
-            float kcorr[4] = {0.f, 0.f, 0.f, 0.f};
-            const bool rv = g < rows;
-            const float *qrow = p.q + (static_cast<size_t>(bseq) * p.Hq + hq0 + (rv ? g : 0)) * p.D + sl * kSlice;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float4 x = rv ? *reinterpret_cast<const float4 *>(qrow + 16 * c + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                x.x *= p.scale_log2;
-                x.y *= p.scale_log2;
-                x.z *= p.scale_log2;
-                x.w *= p.scale_log2;
-                kcorr[c >> 1] += (x.x + x.y) + (x.z + x.w);
-                const float f = (KT == KVQ_Q4_0 && (c & 1) == 0) ? 16.f : 1.f;
-                split_hi_lo(x.x * f, x.z * f, qa[c][0], qa[c][1]);  // k = 2j, 2j+1  <->  d + 0, d + 2
-                split_hi_lo(x.y * f, x.w * f, qa[c][2], qa[c][3]);  // k = 2j+8, 2j+9 <-> d + 1, d + 3
-            }
-            if constexpr (KT == KVQ_Q4_0) {
-                constexpr float kf = -kQ4Offset / kTwo20;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    kcorr[b] += __shfl_xor_sync(0xffffffffu, kcorr[b], 1);
-                    kcorr[b] += __shfl_xor_sync(0xffffffffu, kcorr[b], 2);
-                    kcorr[b] *= kf;
-                }
-                // kept in shared memory (one row of 4 per lane group) instead of registers
-                if (j == 0)
-                    *reinterpret_cast<float4 *>(kcor_row) = make_float4(kcorr[0], kcorr[1], kcorr[2], kcorr[3]);
-                __syncwarp();
-            }
-        }
-        uint32_t magic;  // 0x64006400 in a register, so each nibble mask-and-or is one instruction
-        asm volatile("mov.b32 %0, 0x64006400;\n" : "=r"(magic));
-        float4 *xchg = reinterpret_cast<float4 *>(smem + C::RING);
-        bool dead = false;
-        // keys of this lane inside a tile: A=2j, B=2j+1, C=8+2j, D=9+2j
-        const int kofs[4] = {2 * j, 2 * j + 1, 8 + 2 * j, 9 + 2 * j};
-
-        int slot = 0, use = 0;
-        for (int k = 0; k < n_stage; ++k) {
-            if (!dead && !mbar_wait(full + slot, use & 1)) {
-                dead = true;
-                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
-                s_timeout = 1;
-            }
-            const int tA = t_begin + (k * C::TW + tw) * TPW;  // first tile of this warp in the stage
-            if (tA < t_end) {
-                const uint8_t *st = smem + slot * C::STAGE;
-                float sc[TPW][4];
-#pragma unroll
-                for (int t = 0; t < TPW; ++t) {
-                    const int ti = tw * TPW + t;  // tile index inside the stage
-                    tile_scores<KT>(st + ti * C::KC + sl * code_tile_bytes(KT),
-                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * kScaleTile, qa, kcor_row, lane,
-                                    j, sc[t]);
-                }
-                if constexpr (NS == 2) {
-                    // the two slice-warps of this tile pair add their partial scores
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t) {
-                        float4 *mine = xchg + (((tw * 2 + (k & 1)) * 2 + sl) * TPW + t) * 32;
-                        mine[lane] = make_float4(sc[t][0], sc[t][1], sc[t][2], sc[t][3]);
-                    }
-                    asm volatile("bar.sync %0, 64;\n" ::"r"(1 + tw) : "memory");
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t) {
-                        const float4 os = xchg[(((tw * 2 + (k & 1)) * 2 + (1 - sl)) * TPW + t) * 32 + lane];
-                        sc[t][0] += os.x;
-                        sc[t][1] += os.y;
-                        sc[t][2] += os.z;
-                        sc[t][3] += os.w;
-                    }
-                }
-                // rows past the length, and a second tile past this split's range (it belongs
-                // to the next split and was not loaded), are masked out
-                bool vmask[TPW][4];
-                const int L_split = min(L, t_end * kTileRows);
-                const bool any_partial = (tA + TPW) * kTileRows > L_split;  // warp-uniform
-                if (any_partial) {
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t) {
-                        const int nvalid = min(kTileRows, max(0, L_split - (tA + t) * kTileRows));
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            vmask[t][i] = kofs[i] < nvalid;
-                            if (!vmask[t][i]) sc[t][i] = -CUDART_INF_F;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) vmask[t][i] = true;
-                }
-
-                // ---- online softmax (log2 units) over TPW x 16 keys, lazy rescale ----
-                // p = exp2(s - m_run) may reach 2^kTau before the running maximum is moved;
-                // the V scales are checked so that p * scale can never overflow f16.
-                float mt = -CUDART_INF_F;
-#pragma unroll
-                for (int t = 0; t < TPW; ++t) mt = fmaxf(mt, fmaxf(fmaxf(sc[t][0], sc[t][1]), fmaxf(sc[t][2], sc[t][3])));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-                bool exact = false;
-                if constexpr (VT != KVQ_F16) {
-                    uint32_t e = 0;
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t) {
-                        const uint8_t *vs = st + C::TWT * (C::KC + C::VC + C::KS) + (tw * TPW + t) * C::VS + sl * kScaleTile;
-                        const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
-                        e |= (sc0.x | sc0.y | sc0.z) | (sc0.w | sc1.x | sc1.y) | (sc1.z | sc1.w);
-                    }
-                    // exponent field of any |scale| >= 256 (or inf/nan); an OR may over-report,
-                    // which only costs an exact rescale.  The four lanes of a row must agree.
-                    exact = __any_sync(0xffffffffu, __vcmpgeu2(e & 0x7c007c00u, 0x5c005c00u) != 0);
-                }
-                const bool need = mt > m_run + (exact ? 0.f : kTau);
-                if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = need ? mt : m_run;
-                    const float alpha = (m_run == -CUDART_INF_F) ? 0.f : ex2(m_run - m_new);
-                    m_run = m_new;
-                    l_acc *= alpha;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        o[i][0] *= alpha;
-                        o[i][1] *= alpha;
-                        o[i][2] *= alpha;
-                        o[i][3] *= alpha;
-                    }
-                }
-                float pk[TPW][4];
-#pragma unroll
-                for (int t = 0; t < TPW; ++t) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) pk[t][i] = ex2(sc[t][i] - m_run);
-                    l_acc += (pk[t][0] + pk[t][1]) + (pk[t][2] + pk[t][3]);
-                }
-
-                // ---- O += P V (masking code only for the rare tile that crosses the end) ----
-                if (!any_partial) {
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t) {
-                        const int ti = tw * TPW + t;
-                        tile_pv<VT, false>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
-                                           st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t],
-                                           vmask[t], lane, j, o, magic);
-                    }
-                } else {
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t) {
-                        const int ti = tw * TPW + t;
-                        tile_pv<VT, true>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
-                                          st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t],
-                                          vmask[t], lane, j, o, magic);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0 && !dead) mbar_arrive(empty + slot);
-            if (++slot == C::STAGES) {
-                slot = 0;
-                ++use;
-            }
-        }
-        // q8_0 V: o to real units
-        if constexpr (VT == KVQ_Q8_0) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                o[i][0] = (o[i][0] + o[i][2]) * kTwo24;
-                o[i][1] = (o[i][1] + o[i][3]) * kTwo24;
-                o[i][2] = 0.f;
-                o[i][3] = 0.f;
-            }
-        }
-        // row sums over the four lanes of a row
-        l_acc += __shfl_xor_sync(0xffffffffu, l_acc, 1);
-        l_acc += __shfl_xor_sync(0xffffffffu, l_acc, 2);
-    }
-
-    // ---------------- merge the tile-warps of this CTA ----------------
-    __syncthreads();  // the ring is free from here on
-    constexpr int D = C::D;
-    float *Ob = reinterpret_cast<float *>(smem);                    // [TW][8][D]
-    float *mb = Ob + C::TW * kMaxRowsPerGroup * D;                 // [TW][8]
-    float *lb = mb + C::TW * kMaxRowsPerGroup;                     // [TW][8]
-    if (warp > 0) {
-        const int g = lane >> 2, j = lane & 3;
-        float *orow = Ob + (tw * kMaxRowsPerGroup + g) * D + sl * kSlice;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            // thread holds d = 32b + 4j + {0..3} (ptiles 0,1 of block b) and +16 (ptiles 2,3)
-            const float4 lo4 = make_float4(o[4 * b + 0][0] + o[4 * b + 0][2], o[4 * b + 1][0] + o[4 * b + 1][2],
-                                           o[4 * b + 0][1] + o[4 * b + 0][3], o[4 * b + 1][1] + o[4 * b + 1][3]);
-            const float4 hi4 = make_float4(o[4 * b + 2][0] + o[4 * b + 2][2], o[4 * b + 3][0] + o[4 * b + 3][2],
-                                           o[4 * b + 2][1] + o[4 * b + 2][3], o[4 * b + 3][1] + o[4 * b + 3][3]);
-            *reinterpret_cast<float4 *>(orow + 32 * b + 4 * j) = lo4;
-            *reinterpret_cast<float4 *>(orow + 32 * b + 16 + 4 * j) = hi4;
-        }
-        if (sl == 0 && j == 0) {
-            mb[tw * kMaxRowsPerGroup + g] = m_run;
-            lb[tw * kMaxRowsPerGroup + g] = l_acc;
-        }
-    }
-    __syncthreads();
-    const bool timed_out = s_timeout != 0;
-    const bool single = (ns == 1) && fused;
-    for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
-        const int g = idx / (D / 4), dq = idx % (D / 4);
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int t = 0; t < C::TW; ++t) M = fmaxf(M, mb[t * kMaxRowsPerGroup + g]);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float lsum = 0.f;
-        if (M != -CUDART_INF_F) {
-#pragma unroll
-            for (int t = 0; t < C::TW; ++t) {
-                const float w = ex2(mb[t * kMaxRowsPerGroup + g] - M);  // exp2(-inf) = 0
-                const float4 v = reinterpret_cast<const float4 *>(Ob + (t * kMaxRowsPerGroup + g) * D)[dq];
-                acc.x = fmaf(w, v.x, acc.x);
-                acc.y = fmaf(w, v.y, acc.y);
-                acc.z = fmaf(w, v.z, acc.z);
-                acc.w = fmaf(w, v.w, acc.w);
-                lsum = fmaf(w, lb[t * kMaxRowsPerGroup + g], lsum);
-            }
-        }
-        const int hq = hq0 + g;
-        if (single) {
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            reinterpret_cast<float4 *>(p.out + (static_cast<size_t>(bseq) * p.Hq + hq) * D)[dq] =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            if (dq == 0 && p.lse)
-                p.lse[static_cast<size_t>(bseq) * p.Hq + hq] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -CUDART_INF_F;
-        } else {
-            const size_t pr = (static_cast<size_t>(bseq) * p.Hq + hq) * p.part_stride + p.part_base + split;
-            reinterpret_cast<float4 *>(p.part_o + pr * D)[dq] = acc;
-            if (dq == 0) {
-                p.part_m[pr] = M == -CUDART_INF_F ? -CUDART_INF_F : M * kLn2;
-                p.part_l[pr] = lsum;
-            }
-        }
-    }
-    if (!fused || single || timed_out) return;
-
-    // ---------------- merge of the splits of this (sequence, KV head, row group) ----------------
-    // Small sets of split triples: the last CTA to arrive merges them all.  Otherwise splits
-    // form groups of ceil(sqrt(ns)); the last arrival of each group merges its group into a
-    // group triple while other CTAs still run, and the last group merges the group triples.
-    const size_t unit = (static_cast<size_t>(bseq) * p.Hkv + h) * p.QG + qg;
-    const size_t row0 = static_cast<size_t>(bseq) * p.Hq + hq0;
-    if (static_cast<long long>(ns) * rows * (D + 2) * 4 <= kDirectMergeBytes) {
-        if (!arrive_last(p.counters + unit, ns, s_flag)) return;
-        merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, 0, ns, row0, rows, D, p.out, p.lse, nullptr, nullptr,
-                   nullptr, 0, 0);
-        if (threadIdx.x == 0) p.counters[unit] = 0;
-        return;
-    }
-    const int gs = group_size(ns);
-    const int n_groups = (ns + gs - 1) / gs;
-    const int grp = split / gs;
-    const int gsize = min(gs, ns - grp * gs);
-    int32_t *cnt1 = p.counters1 + unit * p.n_groups_max + grp;
-    if (!arrive_last(cnt1, gsize, s_flag)) return;
-    merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, grp * gs, gsize, row0, rows, D, nullptr, nullptr, p.grp_o,
-               p.grp_m, p.grp_l, p.n_groups_max, grp);
-    if (threadIdx.x == 0) *cnt1 = 0;
-    if (!arrive_last(p.counters + unit, n_groups, s_flag)) return;
-    merge_rows(p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, 0, n_groups, row0, rows, D, p.out, p.lse, nullptr,
-               nullptr, nullptr, 0, 0);
-    if (threadIdx.x == 0) p.counters[unit] = 0;
-}
 
 // ---------------- public merge of split triples ----------------
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
@@ -940,88 +50,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     if (threadIdx.x == 0 && p.lse) p.lse[r] = s_L > 0.f ? s_M + logf(s_L) : -CUDART_INF_F;
 }
 
-constexpr int kMaxDevices = 64;
-
-template <int KT, int VT, int NS>
-cudaError_t configure_t(int dev) {
-    // the dynamic shared-memory opt-in, once per (instance, device)
-    static bool configured[kMaxDevices] = {};
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<KT, VT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg<KT, VT, NS>::SMEM);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
-    return cudaSuccess;
-}
-
-template <int KT, int VT, int NS>
-cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stream) {
-    using C = Cfg<KT, VT, NS>;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = configure_t<KT, VT, NS>(dev);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B * p.QG);
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<KT, VT, NS>, p, fused ? 1 : 0);
-}
-
-template <int KT, int VT, int NS>
-cudaError_t occupancy_t(int *ctas) {
-    using C = Cfg<KT, VT, NS>;
-    // resident CTAs per SM, queried once per (instance, device)
-    static int cached[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = configure_t<KT, VT, NS>(dev);
-    if (e != cudaSuccess) return e;
-    if (cached[dev] == 0) {
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KT, VT, NS>, C::THREADS, C::SMEM);
-        if (e != cudaSuccess) return e;
-        cached[dev] = n > 0 ? n : 1;
-    }
-    *ctas = cached[dev];
-    return cudaSuccess;
-}
-
 }  // namespace
-
-#define KVQ_DISPATCH(KT_, VT_, NS_, CALL)                                  \
-    if (type_k == KT_ && type_v == VT_ && ns == NS_) return CALL<KT_, VT_, NS_>
-#define KVQ_DISPATCH_ALL(CALL, ARGS)                 \
-    KVQ_DISPATCH(KVQ_F16, KVQ_F16, 1, CALL) ARGS;    \
-    KVQ_DISPATCH(KVQ_F16, KVQ_Q8_0, 1, CALL) ARGS;   \
-    KVQ_DISPATCH(KVQ_F16, KVQ_Q4_0, 1, CALL) ARGS;   \
-    KVQ_DISPATCH(KVQ_Q8_0, KVQ_F16, 1, CALL) ARGS;   \
-    KVQ_DISPATCH(KVQ_Q8_0, KVQ_Q8_0, 1, CALL) ARGS;  \
-    KVQ_DISPATCH(KVQ_Q8_0, KVQ_Q4_0, 1, CALL) ARGS;  \
-    KVQ_DISPATCH(KVQ_Q4_0, KVQ_F16, 1, CALL) ARGS;   \
-    KVQ_DISPATCH(KVQ_Q4_0, KVQ_Q8_0, 1, CALL) ARGS;  \
-    KVQ_DISPATCH(KVQ_Q4_0, KVQ_Q4_0, 1, CALL) ARGS;  \
-    KVQ_DISPATCH(KVQ_F16, KVQ_F16, 2, CALL) ARGS;    \
-    KVQ_DISPATCH(KVQ_F16, KVQ_Q8_0, 2, CALL) ARGS;   \
-    KVQ_DISPATCH(KVQ_F16, KVQ_Q4_0, 2, CALL) ARGS;   \
-    KVQ_DISPATCH(KVQ_Q8_0, KVQ_F16, 2, CALL) ARGS;   \
-    KVQ_DISPATCH(KVQ_Q8_0, KVQ_Q8_0, 2, CALL) ARGS;  \
-    KVQ_DISPATCH(KVQ_Q8_0, KVQ_Q4_0, 2, CALL) ARGS;  \
-    KVQ_DISPATCH(KVQ_Q4_0, KVQ_F16, 2, CALL) ARGS;   \
-    KVQ_DISPATCH(KVQ_Q4_0, KVQ_Q8_0, 2, CALL) ARGS;  \
-    KVQ_DISPATCH(KVQ_Q4_0, KVQ_Q4_0, 2, CALL) ARGS;
 
 cudaError_t launch_decode(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream) {
     const int ns = p.D / kSlice;
-    KVQ_DISPATCH_ALL(launch_decode_t, (p, fused, stream))
+    KVQ_DISPATCH_ALL(launch_decode_t, false, (p, fused, stream))
     return cudaErrorInvalidValue;
 }
 
@@ -1037,7 +70,7 @@ cudaError_t decode_occupancy(int type_k, int type_v, int D, int *ctas_per_sm, in
     }
     *n_sms = sm_cache[dev];
     const int ns = D / kSlice;
-    KVQ_DISPATCH_ALL(occupancy_t, (ctas_per_sm))
+    KVQ_DISPATCH_ALL(occupancy_t, false, (ctas_per_sm))
     return cudaErrorInvalidValue;
 }
 

@@ -57,6 +57,10 @@ struct DecodeParams {
     float *grp_o, *grp_m, *grp_l;  // [B][Hq][n_groups_max][D], [B][Hq][n_groups_max]
     int n_groups_max;
     int B, Hkv, Hq, G, QG, D;
+    // queries per sequence: 1 for decode; up to 16 for a draft verify, query i of sequence b
+    // attending to positions [0, len[b] - n_q + i] (causal within the draft).  The rows of a
+    // (sequence, KV head) are ordered r = i * G + g and grouped 8 per CTA (QG groups).
+    int n_q;
     int cap_tiles;
     int n_splits;
     float scale_log2;     // scale * log2(e)
@@ -345,6 +349,8 @@ __device__ __forceinline__ float4 load_f16_row(const uint8_t *codes, int kt, int
 namespace kvq {
 cudaError_t launch_append(int type_k, int type_v, const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_window_append(int tail_k, int tail_v, const WindowParams &p, cudaStream_t stream);
+cudaError_t launch_verify(int type_k, int type_v, const DecodeParams &p, cudaStream_t stream);
+cudaError_t verify_occupancy(int type_k, int type_v, int D, int *ctas_per_sm);
 cudaError_t launch_decode(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 cudaError_t decode_occupancy(int type_k, int type_v, int D, int *ctas_per_sm, int *n_sms);
