@@ -550,20 +550,27 @@ def cpu_baseline(wl, budget_s=10.0):
 
 
 # ----------------------------------------------------------------------------------------
+def decode_kernel_sha() -> str:
+    """sha256 over the decode kernel's sources (kernel template, decode launches, shared header)."""
+    h = hashlib.sha256()
+    for name in ("kvq_decode_kernel.cuh", "kvq_decode.cu", "kvq_internal.cuh"):
+        with open(os.path.join(ROOT, "quantised_kv_long_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def traffic_from_profiles(wl):
     """ncu DRAM bytes per decode launch recorded in profiles/, if the kernel source is unchanged."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
-    src = os.path.join(ROOT, "quantised_kv_long_gb300", "csrc", "kvq_decode.cu")
     try:
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        sha = decode_kernel_sha()
         kv = {}
         with open(path) as f:
             for line in f:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kvq_decode.cu sha256") != sha or kv.get("workload") != wl.name:
+        if kv.get("decode kernel sha256") != sha or kv.get("workload") != wl.name:
             return None
         return float(kv["dram bytes per launch (read+write)"])
     except Exception:
