@@ -29,7 +29,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvq_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libkvq_oracle.so")
 
-TYPES = {"f16": 0, "q8_0": 1, "q4_0": 2}
+TYPES = {"f16": 0, "q8_0": 1, "q4_0": 2, "q4_1": 3, "q5_0": 4, "q5_1": 5}
 QK = 32
 
 
@@ -76,24 +76,31 @@ def _ptr(a: np.ndarray):
 
 
 def code_dtype(kv_type: str):
-    return {"f16": np.uint16, "q8_0": np.int8, "q4_0": np.uint8}[kv_type]
+    return {"f16": np.uint16, "q8_0": np.int8}.get(kv_type, np.uint8)
 
 
 def code_row_len(kv_type: str, D: int) -> int:
-    """Number of code elements per row (f16: D halves, q8_0: D bytes, q4_0: D/2 bytes)."""
-    return {"f16": D, "q8_0": D, "q4_0": D // 2}[kv_type]
+    """Number of code elements per row (f16: D halves, q8_0: D bytes, q4_0: D/2 packed
+    bytes, q4_1 / q5_0 / q5_1: D codes, one per byte)."""
+    return D // 2 if kv_type == "q4_0" else D
+
+
+def scales_per_block(kv_type: str) -> int:
+    """f16 scale values per 32-value block: 0 (f16), 2 for the types with a minimum (d, lo), else 1."""
+    return 0 if kv_type == "f16" else (2 if kv_type in ("q4_1", "q5_1") else 1)
 
 
 def quantize(kv_type: str, x: np.ndarray, n_threads: int = 1):
     """Quantise fp32 rows ``x[..., D]``.  Returns (codes, scales) in natural layout:
-    codes ``[..., code_row_len]`` (f16 bits / int8 / packed uint8), scales f16 bits
-    ``[..., D/32]`` (an empty trailing axis for f16)."""
+    codes ``[..., code_row_len]`` (f16 bits / int8 / packed uint8 / uint8 codes), scales
+    f16 bits ``[..., D/32 * scales_per_block]`` ((d, lo) pairs for q4_1 / q5_1; an empty
+    trailing axis for f16)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     D = x.shape[-1]
     assert D % QK == 0
     rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
     codes = np.empty(x.shape[:-1] + (code_row_len(kv_type, D),), dtype=code_dtype(kv_type))
-    nsc = 0 if kv_type == "f16" else D // QK
+    nsc = scales_per_block(kv_type) * (D // QK)
     scales = np.empty(x.shape[:-1] + (nsc,), dtype=np.uint16)
     lib().kvqo_quantize_rows(TYPES[kv_type], _ptr(x), rows, D, _ptr(codes), _ptr(scales), n_threads)
     return codes, scales

@@ -29,9 +29,21 @@
  *   - The split-softmax merge ("exact online-softmax combine", HAL #582 section 5,
  *     P2 read path) in fp64.
  *
+ *   - q4_1, q5_0, q5_1 (the further scalar types of the same study, section 5 P0 note
+ *     and the P1 ladder, which prices q5_1 at 24 bytes per 32 values).  The pages name
+ *     these GGML-style formats without defining them; the plain reading is:
+ *       q4_1:  lo = min x, hi = max x, d = (hi - lo)/15, codes min(15, trunc((x - lo) *
+ *              (1/d) + 0.5)) in [0, 15], stored d and lo as f16; x_hat = d*c + lo;
+ *       q5_0:  as q4_0 with 5-bit codes: d = m/-16, codes min(31, trunc(x * (1/d) +
+ *              16.5)) in [0, 31]; x_hat = d*(c - 16);
+ *       q5_1:  as q4_1 with 5-bit codes: d = (hi - lo)/31, codes min(31, ...);
+ *     every step one fp32 rounding (no fused multiply-add), (1/d) = 0 when d = 0.
+ *
  * Natural (row-major) layouts are used throughout:
  *   q8_0 codes  int8   [rows][D]          scales f16 bits [rows][D/32]
  *   q4_0 bytes  uint8  [rows][D/2]        (block b = bytes 16b..16b+15)
+ *   q5_0 codes  uint8  [rows][D]          (one code per value), scales [rows][D/32]
+ *   q4_1, q5_1 codes uint8 [rows][D]      scales [rows][D/32][2] = (d, lo) f16 bits
  *   f16         uint16 [rows][D]
  */
 #include <math.h>
@@ -45,6 +57,9 @@
 #define KVQO_F16 0
 #define KVQO_Q8_0 1
 #define KVQO_Q4_0 2
+#define KVQO_Q4_1 3
+#define KVQO_Q5_0 4
+#define KVQO_Q5_1 5
 #define QK 32
 
 /* ---- f16 helpers: IEEE binary16, round-to-nearest-even via the compiler's _Float16 ---- */
@@ -103,6 +118,50 @@ static void quantize_block_q4_0(const float *x, uint8_t *packed, uint16_t *scale
     *scale = f32_to_f16_bits(d);
 }
 
+/* ---- q5_0: one block -> 32 codes in [0, 31] + f16 scale (q4_0 with 16 levels each side) ---- */
+static void quantize_block_q5_0(const float *x, uint8_t *codes, uint16_t *scale) {
+    float amax = 0.0f, m = 0.0f;
+    for (int j = 0; j < QK; ++j) {
+        float a = fabsf(x[j]);
+        if (a > amax) {
+            amax = a;
+            m = x[j];
+        }
+    }
+    float d = m / -16.0f;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    for (int j = 0; j < QK; ++j) {
+        float y = x[j] * id;
+        float t = y + 16.5f;
+        int v = (int)t;
+        codes[j] = (uint8_t)(v < 31 ? v : 31);
+    }
+    *scale = f32_to_f16_bits(d);
+}
+
+/* ---- q4_1 / q5_1: one block -> codes in [0, levels] + f16 (d, lo): x_hat = d*c + lo ---- */
+static void quantize_block_min(const float *x, int levels, uint8_t *codes, uint16_t *dm) {
+    float lo = x[0], hi = x[0];
+    for (int j = 1; j < QK; ++j) {
+        if (x[j] < lo) lo = x[j];
+        if (x[j] > hi) hi = x[j];
+    }
+    float d = (hi - lo) / (float)levels;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    for (int j = 0; j < QK; ++j) {
+        float t = x[j] - lo;   /* >= 0 */
+        float y = t * id;
+        float z = y + 0.5f;
+        int v = (int)z;
+        codes[j] = (uint8_t)(v < levels ? v : levels);
+    }
+    dm[0] = f32_to_f16_bits(d);
+    dm[1] = f32_to_f16_bits(lo);
+}
+
+/* f16 scale values stored per 32-value block (2 for the types with a minimum). */
+static int scales_per_block(int type) { return (type == KVQO_Q4_1 || type == KVQO_Q5_1) ? 2 : 1; }
+
 /* Quantise n_rows rows of D fp32 values (D a multiple of 32). */
 void kvqo_quantize_rows(int type, const float *x, int64_t n_rows, int D,
                         void *codes, uint16_t *scales, int n_threads) {
@@ -121,10 +180,19 @@ void kvqo_quantize_rows(int type, const float *x, int64_t n_rows, int D,
             int8_t *o = (int8_t *)codes + r * D;
             for (int b = 0; b < nb; ++b)
                 quantize_block_q8_0(xr + b * QK, o + b * QK, scales + r * nb + b);
-        } else {
+        } else if (type == KVQO_Q4_0) {
             uint8_t *o = (uint8_t *)codes + r * (D / 2);
             for (int b = 0; b < nb; ++b)
                 quantize_block_q4_0(xr + b * QK, o + b * (QK / 2), scales + r * nb + b);
+        } else if (type == KVQO_Q5_0) {
+            uint8_t *o = (uint8_t *)codes + r * D;
+            for (int b = 0; b < nb; ++b)
+                quantize_block_q5_0(xr + b * QK, o + b * QK, scales + r * nb + b);
+        } else {
+            uint8_t *o = (uint8_t *)codes + r * D;
+            const int levels = type == KVQO_Q4_1 ? 15 : 31;
+            for (int b = 0; b < nb; ++b)
+                quantize_block_min(xr + b * QK, levels, o + b * QK, scales + (r * nb + b) * 2);
         }
     }
 }
@@ -143,7 +211,7 @@ static void dequant_row(int type, const void *codes, const uint16_t *scales, int
             double d = f16_bits_to_f64(s[b]);
             for (int j = 0; j < QK; ++j) out[b * QK + j] = d * (double)q[b * QK + j];
         }
-    } else {
+    } else if (type == KVQO_Q4_0) {
         const uint8_t *p = (const uint8_t *)codes + row * (D / 2);
         const uint16_t *s = scales + row * nb;
         for (int b = 0; b < nb; ++b) {
@@ -153,6 +221,20 @@ static void dequant_row(int type, const void *codes, const uint16_t *scales, int
                 out[b * QK + i] = d * (double)((int)(byte & 0x0F) - 8);
                 out[b * QK + i + QK / 2] = d * (double)((int)(byte >> 4) - 8);
             }
+        }
+    } else if (type == KVQO_Q5_0) {
+        const uint8_t *c = (const uint8_t *)codes + row * D;
+        const uint16_t *s = scales + row * nb;
+        for (int b = 0; b < nb; ++b) {
+            double d = f16_bits_to_f64(s[b]);
+            for (int j = 0; j < QK; ++j) out[b * QK + j] = d * (double)((int)c[b * QK + j] - 16);
+        }
+    } else {
+        const uint8_t *c = (const uint8_t *)codes + row * D;
+        const uint16_t *s = scales + row * nb * 2;
+        for (int b = 0; b < nb; ++b) {
+            double d = f16_bits_to_f64(s[2 * b]), lo = f16_bits_to_f64(s[2 * b + 1]);
+            for (int j = 0; j < QK; ++j) out[b * QK + j] = d * (double)c[b * QK + j] + lo;
         }
     }
 }
@@ -164,7 +246,7 @@ void kvqo_dequantize_rows(int type, const void *codes, const uint16_t *scales, i
 
 /* Bytes per stored row of one cache plane (codes), and of its scales. */
 static int64_t code_row_bytes(int type, int D) {
-    return type == KVQO_F16 ? 2 * (int64_t)D : (type == KVQO_Q8_0 ? D : D / 2);
+    return type == KVQO_F16 ? 2 * (int64_t)D : (type == KVQO_Q4_0 ? D / 2 : D);
 }
 
 /*
@@ -209,7 +291,7 @@ static void attend_range(int type_k, const void *k_codes, const uint16_t *k_scal
 /*
  * Decode attention for one sequence.
  *   q        fp32 [Hq][D]
- *   k_codes  [Hkv][cap][row bytes], k_scales [Hkv][cap][D/32]  (same for v)
+ *   k_codes  [Hkv][cap][row bytes], k_scales [Hkv][cap][D/32 x scales per block]  (same for v)
  *   n        number of valid rows (n <= cap)
  *   out      fp64 [Hq][D] normalised output, lse fp64 [Hq] (natural log).
  * n == 0 gives out = 0 and lse = -inf.
@@ -288,3 +370,4 @@ void kvqo_combine(const double *part_o, const double *part_m, const double *part
 }
 
 int64_t kvqo_code_row_bytes(int type, int D) { return code_row_bytes(type, D); }
+int kvqo_scales_per_block(int type) { return scales_per_block(type); }

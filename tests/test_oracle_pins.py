@@ -477,3 +477,118 @@ def test_tier_ladder_properties():
         prev = r
     # no cells cost nothing
     assert oracle.select_tier(0, L, H, D, 0) == {"rung": 0, "type_k": "f16", "type_v": "f16", "fits": True, "bytes": 0}
+
+
+# ---------------------------------------------------------------------------------------
+# q4_1 / q5_0 / q5_1 (the further scalar types; GGML-style reading, see kvq_oracle.c)
+# ---------------------------------------------------------------------------------------
+def qx(kv_type, x):
+    c, s = oracle.quantize(kv_type, np.asarray(x, np.float32).reshape(1, 32))
+    return c[0].astype(np.int64), [int(v) for v in s[0]]
+
+
+def f16val(bits):
+    return float(np.uint16(bits).view(np.float16))
+
+
+@pytest.mark.parametrize("kv_type,levels", [("q4_1", 15), ("q5_1", 31)])
+def test_min_types_zero_equal_and_ramp(kv_type, levels):
+    c, s = qx(kv_type, np.zeros(32))
+    assert (c == 0).all() and s == [0, 0]
+    for a in (0.375, -2.5, 1000.0):                      # all equal: d = 0, x_hat = lo = a exactly
+        c, s = qx(kv_type, np.full(32, a))
+        assert (c == 0).all() and s == [0, f16bits(a)]
+        assert (oracle.dequantize(kv_type, c[None].astype(np.uint8), np.array([s], np.uint16), 32) == a).all()
+    lo, step = -1.0, 0.125                               # a ramp over every level: codes are the levels
+    j = np.arange(32) % (levels + 1)
+    x = (lo + step * j).astype(np.float32)
+    c, s = qx(kv_type, x)
+    assert (c == j).all() and s == [f16bits(step), f16bits(lo)]
+    assert np.array_equal(oracle.dequantize(kv_type, c[None].astype(np.uint8), np.array([s], np.uint16), 32)[0], x)
+
+
+@pytest.mark.parametrize("kv_type,levels", [("q4_1", 15), ("q5_1", 31)])
+def test_min_types_brute_force_nearest(kv_type, levels):
+    """c = min(levels, floor((x - lo)/d + 1/2)) in exact arithmetic, near-ties excepted; the
+    code is the nearest level, so |x - (lo + d c)| <= d/2 on the fp32 d."""
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        scale = 10.0 ** rng.uniform(-4, 4)
+        x = (rng.standard_normal(32) * scale + rng.uniform(-3, 3) * scale).astype(np.float32)
+        c, s = qx(kv_type, x)
+        lo, hi = f32(x.min()), f32(x.max())
+        d32 = (hi - lo) / f32(levels)
+        d = Fraction(float(d32))
+        for j in range(32):
+            t = (Fraction(float(x[j])) - Fraction(float(lo))) / d + Fraction(1, 2)
+            fl = math.floor(t)
+            if abs(t - round(t)) < Fraction(1, 2**18) and t != round(t):
+                assert c[j] in {min(levels, fl), min(levels, fl - 1), min(levels, fl + 1)}
+            else:
+                assert c[j] == min(levels, fl)
+            err = abs(Fraction(float(x[j])) - Fraction(float(lo)) - d * c[j])
+            assert err <= d / 2 * (1 + Fraction(1, 2**18)) or c[j] == levels
+        assert s == [f16bits(d32), f16bits(lo)]
+
+
+def test_q5_0_zero_equal_tie_clip_and_brute_force():
+    c, s = qx("q5_0", np.zeros(32))
+    assert (c == 16).all() and s == [0x8000]             # d = 0 / -16 = -0
+    c, s = qx("q5_0", np.full(32, 0.5))                  # all equal: code 0, x_hat = -16 d = a
+    assert (c == 0).all() and f16val(s[0]) == -0.5 / 16
+    x = np.zeros(32, np.float32)
+    x[3], x[7] = 2.0, -2.0                               # tie: the first index sets the sign of d
+    c, s = qx("q5_0", x)
+    assert f16val(s[0]) == -0.125 and c[3] == 0 and c[7] == 31   # -2.0 would be 32: clipped
+    rng = np.random.default_rng(12)
+    for trial in range(300):
+        xb = (rng.standard_normal(32) * 10.0 ** rng.uniform(-4, 4)).astype(np.float32)
+        c, s = qx("q5_0", xb)
+        k = int(np.argmax(np.abs(xb)))
+        d32 = f32(xb[k]) / f32(-16)
+        d = Fraction(float(d32))
+        for j in range(32):
+            t = Fraction(float(xb[j])) / d + Fraction(33, 2)
+            fl = math.floor(t)
+            if abs(t - round(t)) < Fraction(1, 2**18) and t != round(t):
+                assert c[j] in {min(31, fl), min(31, fl - 1), min(31, fl + 1)}
+            else:
+                assert c[j] == min(31, fl)
+        assert s == [f16bits(d32)]
+
+
+@pytest.mark.parametrize("tk,tv", [("q5_0", "q5_0"), ("q4_1", "q4_1"), ("q5_1", "q5_1"), ("q8_0", "q5_0"),
+                                   ("q5_1", "q4_0")])
+def test_new_types_attention_against_independent_decode(tk, tv):
+    """Attention over the new types equals fp64 softmax attention on values decoded here,
+    independently of the oracle's dequantiser, from its codes and scales."""
+    rng = np.random.default_rng(13)
+    H, n, D, G = 2, 37, 64, 3
+    K = rng.standard_normal((H, n, D)).astype(np.float32)
+    V = rng.standard_normal((H, n, D)).astype(np.float32)
+    q = rng.standard_normal((H * G, D)).astype(np.float32)
+
+    def decode(kv_type, c, s):
+        d = np.vectorize(f16val)(s).astype(np.float64)
+        if kv_type == "q8_0":
+            return np.repeat(d, 32, -1) * c
+        if kv_type == "q4_0":
+            codes = np.concatenate([c.reshape(*c.shape[:-1], -1, 16) & 15, c.reshape(*c.shape[:-1], -1, 16) >> 4],
+                                   -1).reshape(*c.shape[:-1], -1)
+            return np.repeat(d, 32, -1) * (codes.astype(np.float64) - 8)
+        if kv_type == "q5_0":
+            return np.repeat(d, 32, -1) * (c.astype(np.float64) - 16)
+        dd, lo = d[..., 0::2], d[..., 1::2]
+        return np.repeat(dd, 32, -1) * c + np.repeat(lo, 32, -1)
+
+    kc, ks = oracle.quantize(tk, K)
+    vc, vs = oracle.quantize(tv, V)
+    Kh, Vh = decode(tk, kc, ks), decode(tv, vc, vs)
+    assert np.array_equal(Kh, oracle.dequantize(tk, kc, ks, D)) and np.array_equal(Vh, oracle.dequantize(tv, vc, vs, D))
+    scale = float(np.float32(1 / math.sqrt(D)))
+    out, lse = oracle.attention(tk, kc, ks, tv, vc, vs, n, q, scale)
+    for hq in range(H * G):
+        s_ = scale * (Kh[hq // G] @ q[hq].astype(np.float64))
+        p = np.exp(s_ - s_.max())
+        assert np.allclose(out[hq], p @ Vh[hq // G] / p.sum(), rtol=1e-12, atol=1e-12)
+        assert abs(lse[hq] - (s_.max() + math.log(p.sum()))) < 1e-12
