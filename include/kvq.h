@@ -27,6 +27,17 @@
  *   f16 : x -> binary16, round to nearest even.
  *   Dequantised values: q8_0 f16(d)*q, q4_0 f16(d)*(c-8), f16 as stored.
  *
+ * Further scalar types (the study's section 5 P0 note lists q8/q5, q5/q5, q5_1/q5_1,
+ * q4_1/q4_1 among the typed readers; section 5 P1 floors its ladder at q5_1 K / q4_0 V).
+ * The pages name these GGML-style formats without defining them; the plain reading is:
+ *   q4_1: lo = min x, hi = max x, d = (hi - lo)/15, c_j = min(15, trunc((x_j - lo)*(1/d)
+ *         + 0.5)); scales f16(d), f16(lo); x_hat = f16(d)*c + f16(lo)
+ *   q5_0: as q4_0 with d = m/-16, c_j = min(31, trunc(x_j*(1/d) + 16.5)); x_hat = f16(d)*(c-16)
+ *   q5_1: as q4_1 with d = (hi - lo)/31 and codes up to 31
+ * Caches accept the pairs of f16/q8_0/q4_0 and the pairs (q8_0, q5_0), (q5_0, q5_0),
+ * (q5_1, q5_1), (q4_1, q4_1), (q5_1, q4_0); draft verify and the window + tail cache
+ * accept f16/q8_0/q4_0 only (KVQ_ERR_UNSUPPORTED otherwise).
+ *
  * ---------------------------------------------------------------------------------
  * Memory ownership.  The library allocates NO device memory.  The caller allocates
  * (with any allocator) the K plane, the V plane, the state block and the decode
@@ -65,7 +76,8 @@
  *     [scales region: B][Hkv][capacity/16][NS][128]             (absent for f16)
  *
  * with code_tile_bytes = 2048 (q8_0), 1024 (q4_0), 4096 (f16) per 16 rows x 128 values,
- * so the plane size equals the GGML block footprint exactly (bits/value 8.5, 4.5, 16).
+ * so the plane size equals the GGML block footprint exactly (bits/value 8.5, 4.5, 16;
+ * 5, 5.5, 6 for q4_1, q5_0, q5_1).
  * Inside a tile, for row kt in [0,16) and value index dd in [0,128) of the slice, with
  *     n = kt % 8, st = kt / 8, and for "pair" order A/B/C/D:
  *         kt < 8 : j = kt/2,      pos = kt%2 ? 1 (B) : 0 (A)
@@ -81,7 +93,13 @@
  *   V, q4_0 : (b/2)*512 + (4n' + j)*16 + (2(b%2) + r%2)*4 + Q(pos),
  *             value in the low nibble if i < 16, else the high nibble
  *   V, f16  : (2b + hv)*512 + (4n' + j)*16 + (r%2)*8 + pos*2
- *   scales (K or V), for block b of the slice: j*32 + b*8 + pos*2   (f16 bits)
+ *   K/V, q4_1, q5_0, q5_1: the low 4 bits of each code at the q4_0 nibble place; for q5_0
+ *             and q5_1 the fifth bits follow the 1024 nibble bytes: for a nibble at byte
+ *             offset o, the 32-bit word at 1024 + (o/512)*128 + ((o%512)/16)*4 holds it at
+ *             bit 8e + 4 + w (low nibble) or 8e + w (high nibble), e = o%4, w = (o%16)/4
+ *             (code_tile_bytes 1024 for q4_1, 1280 for q5_0 and q5_1)
+ *   scales (K or V), for block b of the slice: j*32 + b*8 + pos*2   (f16 bits); q4_1 and
+ *             q5_1 hold lo at 128 + the same offset (scale region 256 bytes per tile slice)
  * The codes and scales are the GGML q8_0/q4_0 values above; only their placement
  * differs from GGML's array-of-blocks order, and a q8_0 code q is stored as a
  * sign-magnitude byte (q < 0 ? 0x80 | -q : q), which a permute and a mask turn into the
@@ -113,8 +131,8 @@ typedef enum {
     KVQ_F16 = 0,
     KVQ_Q8_0 = 1,
     KVQ_Q4_0 = 2,
-    /* storage cost only (kvq_block_bytes, kvq_select_tier); caches of these types are
-       KVQ_ERR_UNSUPPORTED */
+    KVQ_Q4_1 = 3, /* see "Further scalar types" below */
+    KVQ_Q5_0 = 4,
     KVQ_Q5_1 = 5
 } kvq_type;
 
@@ -327,7 +345,7 @@ KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const fl
 
 /*
  * Storage cost of one 32-value block of a type, in bytes: f16 64, q8_0 34, q4_0 18,
- * q5_1 24 (two f16 scales, 32 fifth bits, 16 bytes of nibbles).  0 for an unknown type.
+ * q4_1 20, q5_0 22, q5_1 24.  0 for an unknown type.
  * "HAL #582 -- per-layer KV compression study", section 1 and section 5 P1 (the P1
  * validation prices q5_1 K + q4_0 V at 2016 MiB for 32768 cells of the 14B shape).
  */

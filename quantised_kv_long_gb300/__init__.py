@@ -19,8 +19,10 @@ LIB_PATH = os.path.join(_HERE, "libkvq.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "kvq.h")
 
 F16, Q8_0, Q4_0 = 0, 1, 2
-Q5_1 = 5  # storage cost only (block_bytes, select_tier)
-TYPE_IDS = {"f16": F16, "q8_0": Q8_0, "q4_0": Q4_0, "q5_1": Q5_1}
+Q4_1, Q5_0, Q5_1 = 3, 4, 5
+TYPE_IDS = {"f16": F16, "q8_0": Q8_0, "q4_0": Q4_0, "q4_1": Q4_1, "q5_0": Q5_0, "q5_1": Q5_1}
+# bytes per 16-row x 128-value tile slice: codes, scales
+CODE_TILE = {F16: 4096, Q8_0: 2048, Q4_0: 1024, Q4_1: 1024, Q5_0: 1280, Q5_1: 1280}
 TYPE_NAMES = {v: k for k, v in TYPE_IDS.items()}
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
           4: "KVQ_ERR_ALIGNMENT", 5: "KVQ_ERR_CUDA", 6: "KVQ_ERR_DEVICE", 7: "KVQ_ERR_SCRATCH"}
@@ -215,9 +217,8 @@ class KVCache:
         """(k_codes, k_scales, v_codes, v_scales) uint8 views of the caller-owned planes."""
         ns = self.head_dim // 128
         tiles = self.batch * self.n_kv_heads * (self.capacity // 16)
-        ct = {F16: 4096, Q8_0: 2048, Q4_0: 1024}
-        kc = tiles * ns * ct[_tid(self.type_k)]
-        vc = tiles * ns * ct[_tid(self.type_v)]
+        kc = tiles * ns * CODE_TILE[_tid(self.type_k)]
+        vc = tiles * ns * CODE_TILE[_tid(self.type_v)]
         return self.k_mem[:kc], self.k_mem[kc:], self.v_mem[:vc], self.v_mem[vc:]
 
     def lengths(self):

@@ -19,13 +19,15 @@ struct kvq_cache {
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool valid_type(int32_t t) { return t == KVQ_F16 || t == KVQ_Q8_0 || t == KVQ_Q4_0; }
+bool valid_pair(int32_t tk, int32_t tv) {
+    return (kvq::is_base_type(tk) && kvq::is_base_type(tv)) || kvq::is_ext_pair(tk, tv);
+}
 
 kvq_status check_desc(const kvq_cache_desc *d) {
     if (!d) return KVQ_ERR_INVALID_ARG;
     if (d->batch < 1 || d->n_kv_heads < 1 || d->capacity < 1) return KVQ_ERR_INVALID_ARG;
     if (d->capacity % kvq::kTileRows != 0) return KVQ_ERR_INVALID_ARG;
-    if (!valid_type(d->type_k) || !valid_type(d->type_v)) return KVQ_ERR_UNSUPPORTED;
+    if (!valid_pair(d->type_k, d->type_v)) return KVQ_ERR_UNSUPPORTED;
     if (d->head_dim != 128 && d->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
     return KVQ_OK;
 }
@@ -194,6 +196,8 @@ int32_t kvq_block_bytes(kvq_type type) {
         case KVQ_F16: return 64;
         case KVQ_Q8_0: return 34;
         case KVQ_Q4_0: return 18;
+        case KVQ_Q4_1: return 20;
+        case KVQ_Q5_0: return 22;
         case KVQ_Q5_1: return 24;
     }
     return 0;
@@ -499,6 +503,7 @@ kvq_status kvq_verify_workspace_size(const kvq_cache *cache, int32_t n_q, int32_
 kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int32_t n_q, int32_t n_q_heads, float scale,
                              int32_t n_splits, void *workspace, float *out, float *lse, void *stream) {
     if (!cache || !q || !workspace || !out || n_q < 1 || n_q > KVQ_MAX_VERIFY_QUERIES) return KVQ_ERR_INVALID_ARG;
+    if (!kvq::is_base_type(cache->desc.type_k) || !kvq::is_base_type(cache->desc.type_v)) return KVQ_ERR_UNSUPPORTED;
     kvq_status st = check_q_heads(cache, n_q_heads, n_q);
     if (st != KVQ_OK) return st;
     if (n_splits < 0 || n_splits > kvq::kMaxSplits) return KVQ_ERR_INVALID_ARG;
@@ -528,6 +533,7 @@ kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int32_t n_q
 static kvq_status check_window_pair(const kvq_cache *window, const kvq_cache *tail) {
     if (!window || !tail || window == tail) return KVQ_ERR_INVALID_ARG;
     if (window->desc.type_k != KVQ_F16 || window->desc.type_v != KVQ_F16) return KVQ_ERR_UNSUPPORTED;
+    if (!kvq::is_base_type(tail->desc.type_k) || !kvq::is_base_type(tail->desc.type_v)) return KVQ_ERR_UNSUPPORTED;
     if (window->desc.batch != tail->desc.batch || window->desc.n_kv_heads != tail->desc.n_kv_heads ||
         window->desc.head_dim != tail->desc.head_dim)
         return KVQ_ERR_INVALID_ARG;

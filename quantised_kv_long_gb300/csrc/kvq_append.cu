@@ -33,9 +33,9 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
             const int kt = pos & 15;
             const size_t src = ((static_cast<size_t>(bl) * p.Hkv + h) * p.n_new + row) * p.D + sl * kSlice + 4 * lane;
             quantize_store<KT, false>(p.k + src, p.k_codes + (tile * NS + sl) * code_tile_bytes(KT),
-                                      p.k_scales + (tile * NS + sl) * kScaleTile, kt, lane);
+                                      p.k_scales + (tile * NS + sl) * scale_tile_bytes(KT), kt, lane);
             quantize_store<VT, true>(p.v + src, p.v_codes + (tile * NS + sl) * code_tile_bytes(VT),
-                                     p.v_scales + (tile * NS + sl) * kScaleTile, kt, lane);
+                                     p.v_scales + (tile * NS + sl) * scale_tile_bytes(VT), kt, lane);
         }
     }
     // the last CTA (all others have read len[] by now) advances the lengths
@@ -99,9 +99,9 @@ __global__ void __launch_bounds__(256) window_append_kernel(const WindowParams p
                 const size_t ttile = (static_cast<size_t>(b) * p.Hkv + h) * p.t_cap_tiles + (Lt >> 4);
                 const int tkt = Lt & 15;
                 quantize_store_vals<TK, false>(xk, p.t_kc + (ttile * NS + sl) * code_tile_bytes(TK),
-                                               p.t_ks + (ttile * NS + sl) * kScaleTile, tkt, lane);
+                                               p.t_ks + (ttile * NS + sl) * scale_tile_bytes(TK), tkt, lane);
                 quantize_store_vals<TV, true>(xv, p.t_vc + (ttile * NS + sl) * code_tile_bytes(TV),
-                                              p.t_vs + (ttile * NS + sl) * kScaleTile, tkt, lane);
+                                              p.t_vs + (ttile * NS + sl) * scale_tile_bytes(TV), tkt, lane);
             }
             const size_t src = (static_cast<size_t>(b) * p.Hkv + h) * p.D + sl * kSlice + 4 * lane;
             quantize_store<KVQ_F16, false>(p.k + src, wk, nullptr, wkt, lane);
@@ -171,6 +171,11 @@ cudaError_t launch_append(int type_k, int type_v, const AppendParams &p, cudaStr
     KVQ_APPEND_CASE(KVQ_Q4_0, KVQ_F16)
     KVQ_APPEND_CASE(KVQ_Q4_0, KVQ_Q8_0)
     KVQ_APPEND_CASE(KVQ_Q4_0, KVQ_Q4_0)
+    KVQ_APPEND_CASE(KVQ_Q8_0, KVQ_Q5_0)
+    KVQ_APPEND_CASE(KVQ_Q5_0, KVQ_Q5_0)
+    KVQ_APPEND_CASE(KVQ_Q5_1, KVQ_Q5_1)
+    KVQ_APPEND_CASE(KVQ_Q4_1, KVQ_Q4_1)
+    KVQ_APPEND_CASE(KVQ_Q5_1, KVQ_Q4_0)
 #undef KVQ_APPEND_CASE
     return cudaErrorInvalidValue;
 }

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
 cudaError_t launch_decode(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream) {
     const int ns = p.D / kSlice;
     KVQ_DISPATCH_ALL(launch_decode_t, false, (p, fused, stream))
-    return cudaErrorInvalidValue;
+    return launch_decode_ext(type_k, type_v, p, fused, stream);
 }
 
 cudaError_t decode_occupancy(int type_k, int type_v, int D, int *ctas_per_sm, int *n_sms) {
@@ -71,7 +71,7 @@ cudaError_t decode_occupancy(int type_k, int type_v, int D, int *ctas_per_sm, in
     *n_sms = sm_cache[dev];
     const int ns = D / kSlice;
     KVQ_DISPATCH_ALL(occupancy_t, false, (ctas_per_sm))
-    return cudaErrorInvalidValue;
+    return occupancy_ext(type_k, type_v, D, ctas_per_sm);
 }
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {

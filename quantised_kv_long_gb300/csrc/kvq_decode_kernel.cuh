@@ -69,6 +69,18 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a) {
 __device__ __forceinline__ uint32_t q8_02(uint32_t w) { return prmt<0xA280u>(w) & 0x807f807fu; }
 __device__ __forceinline__ uint32_t q8_13(uint32_t w) { return prmt<0xB391u>(w) & 0x807f807fu; }
 constexpr uint32_t kNibLo = 0x000f000fu, kNibHi = 0x00f000f0u;
+// 5-bit codes of one nibble word w (4 bytes, low and high nibble each) whose fifth bits,
+// shifted down by the word's index, sit at bit 8e + 4 (low nibble of byte e) and 8e (high
+// nibble): out[0], out[1] = low-nibble codes of bytes (0, 2), (1, 3); out[2], out[3] =
+// high-nibble codes of bytes (0, 2), (1, 3); each as two halves holding c in bits 0..4.
+__device__ __forceinline__ void fifth_bit_codes(uint32_t w, uint32_t h, uint32_t (&out)[4]) {
+    const uint32_t tl = (w & 0x0f0f0f0fu) | (h & 0x10101010u);
+    const uint32_t th = ((w >> 4) & 0x0f0f0f0fu) | ((h << 4) & 0x10101010u);
+    out[0] = tl & 0x001f001fu;
+    out[1] = (tl >> 8) & 0x001f001fu;
+    out[2] = th & 0x001f001fu;
+    out[3] = (th >> 8) & 0x001f001fu;
+}
 constexpr float kTwo24 = 16777216.0f, kTwo20 = 1048576.0f;
 constexpr float kQ4Offset = 8.0f;  // q4_0 value = scale * (c - 8)
 
@@ -295,11 +307,12 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
         s[2] = acc[1][0] + acc[1][2];
         s[3] = acc[1][1] + acc[1][3];
     } else {
-        // accumulators hold sum q * code in units of 2^-24 (q8_0) or, with the low-nibble
-        // chunk of Q prescaled by 16, sum q * c in units of 2^-20 (q4_0), where
-        // kcorr[b] = -8 * sum_b q in the same unit turns c into the code value c - 8
+        // accumulators hold sum q * code in units of 2^-24 (q8_0, q5_0, q5_1) or, with the
+        // low-nibble chunk of Q prescaled by 16, sum q * c in units of 2^-20 (q4_0, q4_1).
+        // kcorr[b] (per row, same unit): -K * sum_b q for the offset types (c -> c - K), or
+        // sum_b q for the types with a minimum (times lo of each key)
         float kcorr[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (KT == KVQ_Q4_0) {
+        if constexpr (is_nibble_type(KT)) {
             const float4 kc4 = *reinterpret_cast<const float4 *>(kcor);
             kcorr[0] = kc4.x;
             kcorr[1] = kc4.y;
@@ -310,6 +323,7 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
         const uint32_t kscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
         float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
         uint4 wq4 = make_uint4(0, 0, 0, 0);
+        uint32_t hb = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             float acc[2][4];
@@ -319,7 +333,7 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
                 mma_16816(acc[0], qa[2 * b + 1], q8_02(w.y), q8_13(w.y));
                 mma_16816_z(acc[1], qa[2 * b], q8_02(w.z), q8_13(w.z));
                 mma_16816(acc[1], qa[2 * b + 1], q8_02(w.w), q8_13(w.w));
-            } else {
+            } else if constexpr (!has_fifth_bit(KT)) {
                 if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
                 const uint32_t w0 = (b & 1) ? wq4.z : wq4.x, w0s = w0 >> 8;
                 const uint32_t w1 = (b & 1) ? wq4.w : wq4.y, w1s = w1 >> 8;
@@ -327,20 +341,39 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
                 mma_16816(acc[0], qa[2 * b + 1], w0 & kNibHi, w0s & kNibHi);
                 mma_16816_z(acc[1], qa[2 * b], w1 & kNibLo, w1s & kNibLo);
                 mma_16816(acc[1], qa[2 * b + 1], w1 & kNibHi, w1s & kNibHi);
+            } else {
+                if ((b & 1) == 0) {
+                    wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
+                    hb = *reinterpret_cast<const uint32_t *>(kc + kNibbleBytes + (b >> 1) * 128 + lane * 4);
+                }
+                const int wi0 = 2 * (b & 1), wi1 = wi0 + 1;
+                uint32_t c0[4], c1[4];
+                fifth_bit_codes((b & 1) ? wq4.z : wq4.x, hb >> wi0, c0);
+                fifth_bit_codes((b & 1) ? wq4.w : wq4.y, hb >> wi1, c1);
+                mma_16816_z(acc[0], qa[2 * b], c0[0], c0[1]);
+                mma_16816(acc[0], qa[2 * b + 1], c0[2], c0[3]);
+                mma_16816_z(acc[1], qa[2 * b], c1[0], c1[1]);
+                mma_16816(acc[1], qa[2 * b + 1], c1[2], c1[3]);
             }
             const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
             const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
             float2 t01 = add2(make_float2(acc[0][0], acc[0][1]), make_float2(acc[0][2], acc[0][3]));
             float2 t23 = add2(make_float2(acc[1][0], acc[1][1]), make_float2(acc[1][2], acc[1][3]));
-            if constexpr (KT == KVQ_Q4_0) {
+            if constexpr (KT == KVQ_Q4_0 || KT == KVQ_Q5_0) {
                 const float2 cb = make_float2(kcorr[b], kcorr[b]);
                 t01 = add2(t01, cb);
                 t23 = add2(t23, cb);
             }
             s01 = fma2(dab, t01, s01);
             s23 = fma2(dcd, t23, s23);
+            if constexpr (has_min(KT)) {  // + lo * sum_b q
+                const uint2 lsc = *reinterpret_cast<const uint2 *>(ks + kScaleTile + j * 32 + b * 8);
+                const float2 cb = make_float2(kcorr[b], kcorr[b]);
+                s01 = fma2(__half22float2(u32_as_h2(lsc.x)), cb, s01);
+                s23 = fma2(__half22float2(u32_as_h2(lsc.y)), cb, s23);
+            }
         }
-        constexpr float unit = KT == KVQ_Q8_0 ? kTwo24 : kTwo20;
+        constexpr float unit = (KT == KVQ_Q4_0 || KT == KVQ_Q4_1) ? kTwo20 : kTwo24;
         s[0] = s01.x * unit;
         s[1] = s01.y * unit;
         s[2] = s23.x * unit;
@@ -353,7 +386,7 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
 template <int VT, bool PARTIAL>
 __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, const float (&pk)[4],
                                         const bool (&vmask)[4], int lane, int j, float (&o)[16][4],
-                                        uint32_t magic) {
+                                        uint32_t magic, float (&corr)[4]) {
     if constexpr (VT == KVQ_F16) {
         uint32_t a[4];
         split_hi_lo(pk[0], pk[1], a[0], a[1]);
@@ -396,6 +429,7 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
             mcd = (vmask[2] ? 0x0000ffffu : 0u) | (vmask[3] ? 0xffff0000u : 0u);
         }
         uint4 wq4 = make_uint4(0, 0, 0, 0);
+        uint32_t hb = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             const __half2 dab = u32_as_h2(vscale[b][0] & mab);
@@ -409,29 +443,56 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
             a[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), dab, eab));
             a[2] = h2_as_u32(hcd);
             a[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), dcd, ecd));
-            // o accumulates sum P' * code in units of 2^-24 (q4_0 high nibbles: 16c); for
-            // q4_0, corr column b accumulates sum P' of block b (B = 1.0 in column b), which
-            // removes the code offset 8 at the end
+            // q8_0: o accumulates sum P' * q in units of 2^-24; nibble types: exact f16 code
+            // values by the magic-number route (nibble | 0x6400 is 1024 + c; a high nibble
+            // gives 1024 + 16c, scaled by 1/16), less the offset (8 for q4_0, 16 for q5_0)
             if constexpr (VT == KVQ_Q8_0) {
                 const uint4 w = lds128(vc + b * 512 + lane * 16);
                 mma_16816(o[4 * b + 0], a, q8_02(w.x), q8_13(w.x));
                 mma_16816(o[4 * b + 1], a, q8_02(w.y), q8_13(w.y));
                 mma_16816(o[4 * b + 2], a, q8_02(w.z), q8_13(w.z));
                 mma_16816(o[4 * b + 3], a, q8_02(w.w), q8_13(w.w));
-            } else {
-                // q4_0 V: exact f16 values c - 8 by the magic-number route (nibble | 0x6400 is
-                // 1024 + c; the high nibble gives 1024 + 16c, scaled by 1/16 and less 72)
+            } else if constexpr (!has_fifth_bit(VT)) {
                 if ((b & 1) == 0) wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
                 const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x, wq0s = wq0 >> 8;  // bytes 2n'   of the block
                 const uint32_t wq1 = (b & 1) ? wq4.w : wq4.y, wq1s = wq1 >> 8;  // bytes 2n'+1 of the block
-                const __half2 k1032 = __float2half2_rn(1032.0f), k16th = __float2half2_rn(0.0625f),
-                              km72 = __float2half2_rn(-72.0f);
-                auto lo = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2((x & kNibLo) | magic), k1032)); };
-                auto hi = [&](uint32_t x) { return h2_as_u32(__hfma2(u32_as_h2((x & kNibHi) | magic), k16th, km72)); };
+                constexpr float off = VT == KVQ_Q4_0 ? kQ4Offset : 0.0f;
+                const __half2 klo = __float2half2_rn(1024.0f + off), k16th = __float2half2_rn(0.0625f),
+                              khi = __float2half2_rn(-64.0f - off);
+                auto lo = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2((x & kNibLo) | magic), klo)); };
+                auto hi = [&](uint32_t x) { return h2_as_u32(__hfma2(u32_as_h2((x & kNibHi) | magic), k16th, khi)); };
                 mma_16816(o[4 * b + 0], a, lo(wq0), lo(wq0s));
                 mma_16816(o[4 * b + 2], a, hi(wq0), hi(wq0s));
                 mma_16816(o[4 * b + 1], a, lo(wq1), lo(wq1s));
                 mma_16816(o[4 * b + 3], a, hi(wq1), hi(wq1s));
+            } else {
+                if ((b & 1) == 0) {
+                    wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
+                    hb = *reinterpret_cast<const uint32_t *>(vc + kNibbleBytes + (b >> 1) * 128 + lane * 4);
+                }
+                uint32_t c0[4], c1[4];
+                fifth_bit_codes((b & 1) ? wq4.z : wq4.x, hb >> (2 * (b & 1)), c0);
+                fifth_bit_codes((b & 1) ? wq4.w : wq4.y, hb >> (2 * (b & 1) + 1), c1);
+                const __half2 koff = __float2half2_rn(VT == KVQ_Q5_0 ? 1040.0f : 1024.0f);
+                auto val = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2(x | magic), koff)); };
+                mma_16816(o[4 * b + 0], a, val(c0[0]), val(c0[1]));
+                mma_16816(o[4 * b + 2], a, val(c0[2]), val(c0[3]));
+                mma_16816(o[4 * b + 1], a, val(c1[0]), val(c1[1]));
+                mma_16816(o[4 * b + 3], a, val(c1[2]), val(c1[3]));
+            }
+            if constexpr (has_min(VT)) {
+                // + p * lo for every value of the block: sum over keys of p * lo (f16 hi + lo
+                // like P') lands in column b of corr (B = 1.0 in column b); added at the end
+                const uint2 lsc = *reinterpret_cast<const uint2 *>(vs + kScaleTile + j * 32 + b * 8);
+                const __half2 lab = u32_as_h2(lsc.x & mab), lcd = u32_as_h2(lsc.y & mcd);
+                const __half2 hab2 = __hmul2(u32_as_h2(ph_ab), lab), hcd2 = __hmul2(u32_as_h2(ph_cd), lcd);
+                uint32_t a2[4];
+                a2[0] = h2_as_u32(hab2);
+                a2[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), lab, __hfma2(u32_as_h2(ph_ab), lab, __hneg2(hab2))));
+                a2[2] = h2_as_u32(hcd2);
+                a2[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), lcd, __hfma2(u32_as_h2(ph_cd), lcd, __hneg2(hcd2))));
+                const uint32_t one = (lane >> 2) == b ? 0x3c003c00u : 0u;
+                mma_16816(corr, a2, one, one);
             }
         }
     }
@@ -607,10 +668,10 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 for (int s2 = 0; s2 < NS; ++s2) {
                     quantize_store<KT, false>(kx + s2 * kSlice + 4 * lane,
                                               const_cast<uint8_t *>(p.k_codes) + tile * C::KC + s2 * code_tile_bytes(KT),
-                                              const_cast<uint8_t *>(p.k_scales) + tile * C::KS + s2 * kScaleTile, kt, lane);
+                                              const_cast<uint8_t *>(p.k_scales) + tile * C::KS + s2 * scale_tile_bytes(KT), kt, lane);
                     quantize_store<VT, true>(vx + s2 * kSlice + 4 * lane,
                                              const_cast<uint8_t *>(p.v_codes) + tile * C::VC + s2 * code_tile_bytes(VT),
-                                             const_cast<uint8_t *>(p.v_scales) + tile * C::VS + s2 * kScaleTile, kt, lane);
+                                             const_cast<uint8_t *>(p.v_scales) + tile * C::VS + s2 * scale_tile_bytes(VT), kt, lane);
                 }
                 // order these generic-proxy stores before the bulk copy (async proxy) that reads them
                 asm volatile("fence.proxy.async.global;\n" ::: "memory");
@@ -659,12 +720,15 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 x.z *= p.scale_log2;
                 x.w *= p.scale_log2;
                 kcorr[c >> 1] += (x.x + x.y) + (x.z + x.w);
-                const float f = (KT == KVQ_Q4_0 && (c & 1) == 0) ? 16.f : 1.f;
+                const float f = ((KT == KVQ_Q4_0 || KT == KVQ_Q4_1) && (c & 1) == 0) ? 16.f : 1.f;
                 split_hi_lo(x.x * f, x.z * f, qa[c][0], qa[c][1]);  // k = 2j, 2j+1  <->  d + 0, d + 2
                 split_hi_lo(x.y * f, x.w * f, qa[c][2], qa[c][3]);  // k = 2j+8, 2j+9 <-> d + 1, d + 3
             }
-            if constexpr (KT == KVQ_Q4_0) {
-                constexpr float kf = -kQ4Offset / kTwo20;
+            if constexpr (is_nibble_type(KT)) {
+                // per row and block: -8 (q4_0) or -16 (q5_0) times sum_b q, or sum_b q for the
+                // types with a minimum, in the accumulator unit
+                constexpr float unit = (KT == KVQ_Q4_0 || KT == KVQ_Q4_1) ? kTwo20 : kTwo24;
+                constexpr float kf = (KT == KVQ_Q4_0 ? -kQ4Offset : (KT == KVQ_Q5_0 ? -16.0f : 1.0f)) / unit;
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     kcorr[b] += __shfl_xor_sync(0xffffffffu, kcorr[b], 1);
@@ -677,6 +741,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 __syncwarp();
             }
         }
+        float corr[4] = {0.f, 0.f, 0.f, 0.f};  // V types with a minimum: sum of p * lo per block (column b)
         uint32_t magic;  // 0x64006400 in a register, so each nibble mask-and-or is one instruction
         asm volatile("mov.b32 %0, 0x64006400;\n" : "=r"(magic));
         float4 *xchg = reinterpret_cast<float4 *>(smem + C::RING);
@@ -700,7 +765,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 for (int t = 0; t < TPW; ++t) {
                     const int ti = tw * TPW + t;  // tile index inside the stage
                     tile_scores<KT>(st + ti * C::KC + sl * code_tile_bytes(KT),
-                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * kScaleTile, qa, kcor_row, lane,
+                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * scale_tile_bytes(KT), qa, kcor_row, lane,
                                     j, sc[t]);
                 }
                 if constexpr (NS == 2) {
@@ -766,7 +831,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                     uint32_t e = 0;
 #pragma unroll
                     for (int t = 0; t < TPW; ++t) {
-                        const uint8_t *vs = st + C::TWT * (C::KC + C::VC + C::KS) + (tw * TPW + t) * C::VS + sl * kScaleTile;
+                        const uint8_t *vs = st + C::TWT * (C::KC + C::VC + C::KS) + (tw * TPW + t) * C::VS + sl * scale_tile_bytes(VT);
                         const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
                         e |= (sc0.x | sc0.y | sc0.z) | (sc0.w | sc1.x | sc1.y) | (sc1.z | sc1.w);
                     }
@@ -780,6 +845,10 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                     const float alpha = (m_run == -CUDART_INF_F) ? 0.f : ex2(m_run - m_new);
                     m_run = m_new;
                     l_acc *= alpha;
+                    if constexpr (has_min(VT)) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) corr[i] *= alpha;
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         o[i][0] *= alpha;
@@ -805,16 +874,16 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                     for (int t = 0; t < TPW; ++t) {
                         const int ti = tw * TPW + t;
                         tile_pv<VT, false>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
-                                           st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t],
-                                           vmask[t], lane, j, o, magic);
+                                           st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * scale_tile_bytes(VT), pk[t],
+                                           vmask[t], lane, j, o, magic, corr);
                     }
                 } else {
 #pragma unroll
                     for (int t = 0; t < TPW; ++t) {
                         const int ti = tw * TPW + t;
                         tile_pv<VT, true>(st + C::TWT * C::KC + ti * C::VC + sl * code_tile_bytes(VT),
-                                          st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * kScaleTile, pk[t],
-                                          vmask[t], lane, j, o, magic);
+                                          st + C::TWT * (C::KC + C::VC + C::KS) + ti * C::VS + sl * scale_tile_bytes(VT), pk[t],
+                                          vmask[t], lane, j, o, magic, corr);
                     }
                 }
             }
@@ -823,6 +892,22 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
             if (++slot == C::STAGES) {
                 slot = 0;
                 ++use;
+            }
+        }
+        // V types with a minimum: add sum of p * lo of each block to its values (corr column
+        // b, held by lane 4g + b/2 for the hi and lo rows)
+        if constexpr (has_min(VT)) {
+            const float v0 = corr[0] + corr[2], v1 = corr[1] + corr[3];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float ct = __shfl_sync(0xffffffffu, (b & 1) ? v1 : v0, (lane & ~3) | (b >> 1));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    o[4 * b + i][0] += o[4 * b + i][2] + ct;
+                    o[4 * b + i][1] += o[4 * b + i][3] + ct;
+                    o[4 * b + i][2] = 0.f;
+                    o[4 * b + i][3] = 0.f;
+                }
             }
         }
         // q8_0 V: o to real units

@@ -24,10 +24,21 @@ inline int max_merge_groups(int n_splits) {
 }
 constexpr int kMaxRowsPerGroup = 8;  // query heads of one KV head handled per CTA
 
-__host__ __device__ constexpr int code_tile_bytes(int type) {
-    return type == KVQ_Q8_0 ? 2048 : (type == KVQ_Q4_0 ? 1024 : 4096);
+// per 16-row x 128-value tile slice: nibble types keep the q4_0 nibble layout (1024 B),
+// 5-bit types add a 256-B plane of fifth bits; types with a minimum keep (d, lo) scales
+__host__ __device__ constexpr bool has_fifth_bit(int type) { return type == KVQ_Q5_0 || type == KVQ_Q5_1; }
+__host__ __device__ constexpr bool has_min(int type) { return type == KVQ_Q4_1 || type == KVQ_Q5_1; }
+__host__ __device__ constexpr bool is_nibble_type(int type) {
+    return type == KVQ_Q4_0 || type == KVQ_Q4_1 || type == KVQ_Q5_0 || type == KVQ_Q5_1;
 }
-__host__ __device__ constexpr int scale_tile_bytes(int type) { return type == KVQ_F16 ? 0 : kScaleTile; }
+constexpr int kNibbleBytes = 1024, kFifthBitBytes = 256;
+__host__ __device__ constexpr int code_tile_bytes(int type) {
+    return type == KVQ_Q8_0 ? 2048
+                            : (type == KVQ_F16 ? 4096 : kNibbleBytes + (has_fifth_bit(type) ? kFifthBitBytes : 0));
+}
+__host__ __device__ constexpr int scale_tile_bytes(int type) {
+    return type == KVQ_F16 ? 0 : (has_min(type) ? 2 * kScaleTile : kScaleTile);
+}
 
 // ---- placement inside one (tile, slice); see include/kvq.h for the contract ----
 // pair order of a row inside the 16-row tile: j in [0,4), pos in {A=0,B=1,C=2,D=3}
@@ -250,50 +261,90 @@ __device__ __forceinline__ void quantize_store_vals(const float4 v4, uint8_t *co
         return;
     }
 
-    if constexpr (T == KVQ_Q4_0) {
-        // value of largest magnitude; the lowest index wins a tie
-        float best = xs[0], ba = fabsf(xs[0]);
-        int bi = dd0;
+    if constexpr (is_nibble_type(T)) {
+        int c[4];
+        float d, lo = 0.f;
+        if constexpr (!has_min(T)) {
+            // q4_0 / q5_0: value of largest magnitude (the lowest index wins a tie), d = m / -K,
+            // codes min(2K - 1, trunc(x / d + K + 1/2)) with K = 8 or 16
+            constexpr float K = T == KVQ_Q4_0 ? 8.0f : 16.0f;
+            constexpr int cmax = T == KVQ_Q4_0 ? 15 : 31;
+            float best = xs[0], ba = fabsf(xs[0]);
+            int bi = dd0;
 #pragma unroll
-        for (int e = 1; e < 4; ++e) {
-            const float a = fabsf(xs[e]);
-            if (a > ba) {
-                ba = a;
-                best = xs[e];
-                bi = dd0 + e;
+            for (int e = 1; e < 4; ++e) {
+                const float a = fabsf(xs[e]);
+                if (a > ba) {
+                    ba = a;
+                    best = xs[e];
+                    bi = dd0 + e;
+                }
+            }
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                const float oba = __shfl_xor_sync(0xffffffffu, ba, off);
+                const float obest = __shfl_xor_sync(0xffffffffu, best, off);
+                const int obi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (oba > ba || (oba == ba && obi < bi)) {
+                    ba = oba;
+                    best = obest;
+                    bi = obi;
+                }
+            }
+            d = __fdiv_rn(best, -K);
+            const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = static_cast<int>(__fadd_rn(__fmul_rn(xs[e], id), K + 0.5f));  // truncation
+                c[e] = t < cmax ? t : cmax;
+            }
+        } else {
+            // q4_1 / q5_1: lo = min, hi = max, d = (hi - lo) / L, codes min(L, trunc((x - lo) / d + 1/2))
+            constexpr int L = T == KVQ_Q4_1 ? 15 : 31;
+            lo = fminf(fminf(xs[0], xs[1]), fminf(xs[2], xs[3]));
+            float hi = fmaxf(fmaxf(xs[0], xs[1]), fmaxf(xs[2], xs[3]));
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+                hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+            }
+            d = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(L));
+            const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = static_cast<int>(__fadd_rn(__fmul_rn(__fsub_rn(xs[e], lo), id), 0.5f));
+                c[e] = t < L ? t : L;
             }
         }
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) {
-            const float oba = __shfl_xor_sync(0xffffffffu, ba, off);
-            const float obest = __shfl_xor_sync(0xffffffffu, best, off);
-            const int obi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (oba > ba || (oba == ba && obi < bi)) {
-                ba = oba;
-                best = obest;
-                bi = obi;
-            }
-        }
-        const float d = __fdiv_rn(best, -8.0f);
-        const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-        int c[4], chi[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int t = static_cast<int>(__fadd_rn(__fmul_rn(xs[e], id), 8.5f));  // truncation
-            c[e] = t < 15 ? t : 15;
-        }
+        int chi[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) chi[e] = __shfl_down_sync(0xffffffffu, c[e], 4);
         if ((lane & 7) < 4) {
-            // this lane holds values i0..i0+3 (< 16) and, from lane+4, values i0+16..i0+19
+            // this lane holds values i0..i0+3 (< 16) and, from lane+4, values i0+16..i0+19:
+            // low 4 bits in the nibbles; for 5-bit types the fifth bits go to the plane after
+            // the nibbles: lane L's word of chunk b/2 holds, for nibble word wi of that lane,
+            // byte e's low-nibble code at bit 8e + 4 + wi and its high-nibble code at bit 8e + wi
             uint32_t byte[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) byte[e] = uint32_t(c[e]) | (uint32_t(chi[e]) << 4);
+            for (int e = 0; e < 4; ++e) byte[e] = uint32_t(c[e] & 15) | (uint32_t(chi[e] & 15) << 4);
+            uint32_t *hb_chunk = reinterpret_cast<uint32_t *>(codes + kNibbleBytes + (b >> 1) * 128);
             if constexpr (!IS_V) {
                 const int jb = lane & 7;  // bytes 4jb..4jb+3 of the block
                 const uint32_t w = byte[0] | (byte[1] << 8) | (byte[2] << 16) | (byte[3] << 24);
                 *reinterpret_cast<uint32_t *>(codes + (b >> 1) * 512 + (4 * n + jb) * 16 + (2 * (b & 1) + st) * 4) =
                     w;
+                if constexpr (has_fifth_bit(T)) {
+                    const int wi = 2 * (b & 1) + st;
+                    uint32_t mask = 0, bits = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        mask |= (1u << (8 * e + 4 + wi)) | (1u << (8 * e + wi));
+                        bits |= (uint32_t(c[e] >> 4) << (8 * e + 4 + wi)) | (uint32_t(chi[e] >> 4) << (8 * e + wi));
+                    }
+                    uint32_t *hw = hb_chunk + (4 * n + jb);
+                    atomicAnd(hw, ~mask);  // the bits of other rows of the word are kept
+                    atomicOr(hw, bits);
+                }
             } else {
                 const int vb = vword_byte(pos);
 #pragma unroll
@@ -301,11 +352,23 @@ __device__ __forceinline__ void quantize_store_vals(const float4 v4, uint8_t *co
                     const int r = i0 + e, n2 = r >> 1, qq = r & 1;
                     codes[(b >> 1) * 512 + (4 * n2 + j) * 16 + (2 * (b & 1) + qq) * 4 + vb] =
                         static_cast<uint8_t>(byte[e]);
+                    if constexpr (has_fifth_bit(T)) {
+                        const int wi = 2 * (b & 1) + qq;
+                        const uint32_t mask = (1u << (8 * vb + 4 + wi)) | (1u << (8 * vb + wi));
+                        const uint32_t bits =
+                            (uint32_t(c[e] >> 4) << (8 * vb + 4 + wi)) | (uint32_t(chi[e] >> 4) << (8 * vb + wi));
+                        uint32_t *hw = hb_chunk + (4 * n2 + j);
+                        atomicAnd(hw, ~mask);
+                        atomicOr(hw, bits);
+                    }
                 }
             }
         }
-        if ((lane & 7) == 0)
+        if ((lane & 7) == 0) {
             *reinterpret_cast<__half *>(scales + j * 32 + b * 8 + pos * 2) = __float2half_rn(d);
+            if constexpr (has_min(T))
+                *reinterpret_cast<__half *>(scales + kScaleTile + j * 32 + b * 8 + pos * 2) = __float2half_rn(lo);
+        }
         return;
     }
 }
@@ -350,6 +413,15 @@ namespace kvq {
 cudaError_t launch_append(int type_k, int type_v, const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_window_append(int tail_k, int tail_v, const WindowParams &p, cudaStream_t stream);
 cudaError_t launch_verify(int type_k, int type_v, const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_ext(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream);
+cudaError_t occupancy_ext(int type_k, int type_v, int D, int *ctas_per_sm);
+// the (K, V) type pairs a cache may hold: every pair of f16 / q8_0 / q4_0, plus these
+__host__ __device__ constexpr bool is_base_type(int t) { return t == KVQ_F16 || t == KVQ_Q8_0 || t == KVQ_Q4_0; }
+__host__ __device__ constexpr bool is_ext_pair(int tk, int tv) {
+    return (tk == KVQ_Q8_0 && tv == KVQ_Q5_0) || (tk == KVQ_Q5_0 && tv == KVQ_Q5_0) ||
+           (tk == KVQ_Q5_1 && tv == KVQ_Q5_1) || (tk == KVQ_Q4_1 && tv == KVQ_Q4_1) ||
+           (tk == KVQ_Q5_1 && tv == KVQ_Q4_0);
+}
 cudaError_t verify_occupancy(int type_k, int type_v, int D, int *ctas_per_sm);
 cudaError_t launch_decode(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);

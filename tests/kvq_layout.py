@@ -6,7 +6,9 @@ formulas printed in the header.  Shares nothing with the CUDA path.
 """
 import numpy as np
 
-CODE_TILE = {"f16": 4096, "q8_0": 2048, "q4_0": 1024}
+CODE_TILE = {"f16": 4096, "q8_0": 2048, "q4_0": 1024, "q4_1": 1024, "q5_0": 1280, "q5_1": 1280}
+SCALE_TILE = {"f16": 0, "q8_0": 128, "q4_0": 128, "q4_1": 256, "q5_0": 128, "q5_1": 256}
+NIBBLE = ("q4_0", "q4_1", "q5_0", "q5_1")
 
 
 def _pair(kt):
@@ -31,7 +33,7 @@ def tile_offsets(kv_type: str, is_v: bool):
     if not is_v:
         if kv_type == "q8_0":
             off = b * 512 + (4 * n + (dd % 16) // 4) * 16 + (2 * st + i // 16) * 4 + dd % 4
-        elif kv_type == "q4_0":
+        elif kv_type in NIBBLE:
             off = (b // 2) * 512 + (4 * n + (i % 16) // 4) * 16 + (2 * (b % 2) + st) * 4 + (i % 16) % 4
             nib = (i >= 16).astype(int)
         else:
@@ -42,7 +44,7 @@ def tile_offsets(kv_type: str, is_v: bool):
         n2 = r // 2
         if kv_type == "q8_0":
             off = b * 512 + (4 * n2 + j) * 16 + ((r % 2) + 2 * hv) * 4 + _q_of_pos(pos)
-        elif kv_type == "q4_0":
+        elif kv_type in NIBBLE:
             off = (b // 2) * 512 + (4 * n2 + j) * 16 + (2 * (b % 2) + r % 2) * 4 + _q_of_pos(pos)
             nib = (i >= 16).astype(int)
         else:
@@ -81,19 +83,36 @@ def decode_plane(codes_plane: np.ndarray, scales_plane: np.ndarray, kv_type: str
         codes = q.transpose(0, 1, 2, 4, 3, 5).reshape(B, Hkv, cap, D)
     else:
         c = np.where(nib == 1, byte >> 4, byte & 0x0F).astype(np.uint8)   # [B,Hkv,T,NS,16,128]
+        if kv_type in ("q5_0", "q5_1"):
+            # fifth bits: 32-bit word of lane L = (off % 512) // 16 in the plane after the
+            # nibbles (128 B per 512-B chunk); bit 8e + 4 + wi (low nibble) or 8e + wi (high
+            # nibble), e = byte of the nibble word, wi = word of the lane
+            lane = (off % 512) // 16
+            wi, e = (off % 16) // 4, off % 4
+            woff = 1024 + (off // 512) * 128 + lane * 4
+            words = (raw[..., woff].astype(np.uint32) | (raw[..., woff + 1].astype(np.uint32) << 8) |
+                     (raw[..., woff + 2].astype(np.uint32) << 16) | (raw[..., woff + 3].astype(np.uint32) << 24))
+            bit = np.where(nib == 1, 8 * e + wi, 8 * e + 4 + wi)
+            c = (c | (((words >> bit.astype(np.uint32)) & 1) << 4)).astype(np.uint8)
         c = c.transpose(0, 1, 2, 4, 3, 5).reshape(B, Hkv, cap, D // 32, 32)
-        packed = (c[..., :16] | (c[..., 16:] << 4)).astype(np.uint8)
-        codes = packed.reshape(B, Hkv, cap, D // 2)
-    sraw = np.asarray(scales_plane, dtype=np.uint8).reshape(B, Hkv, T, NS, 128)
+        if kv_type == "q4_0":
+            codes = (c[..., :16] | (c[..., 16:] << 4)).astype(np.uint8).reshape(B, Hkv, cap, D // 2)
+        else:
+            codes = c.reshape(B, Hkv, cap, D)
+    sraw = np.asarray(scales_plane, dtype=np.uint8).reshape(B, Hkv, T, NS, SCALE_TILE[kv_type])
     so = scale_offsets()
     s = sraw[..., so].astype(np.uint16) | (sraw[..., so + 1].astype(np.uint16) << 8)  # [B,Hkv,T,NS,16,4]
     scales = s.transpose(0, 1, 2, 4, 3, 5).reshape(B, Hkv, cap, D // 32)
+    if kv_type in ("q4_1", "q5_1"):  # lo after d, interleaved as (d, lo) per block
+        s2 = sraw[..., so + 128].astype(np.uint16) | (sraw[..., so + 129].astype(np.uint16) << 8)
+        lo = s2.transpose(0, 1, 2, 4, 3, 5).reshape(B, Hkv, cap, D // 32)
+        scales = np.stack([scales, lo], -1).reshape(B, Hkv, cap, D // 16)
     return codes, scales
 
 
 def check_bijective():
     """Every layout maps the 16x128 (row, value) slots onto distinct bytes/nibbles."""
-    for t in ("f16", "q8_0", "q4_0"):
+    for t in ("f16", "q8_0", "q4_0", "q4_1", "q5_0", "q5_1"):
         for is_v in (False, True):
             off, nib = tile_offsets(t, is_v)
             if t == "f16":
@@ -103,6 +122,11 @@ def check_bijective():
                 assert len(set(off.ravel().tolist())) == 16 * 128 and off.max() < CODE_TILE[t]
             else:
                 keys = off.ravel() * 2 + nib.ravel()
-                assert len(set(keys.tolist())) == 16 * 128 and off.max() < CODE_TILE[t]
+                assert len(set(keys.tolist())) == 16 * 128 and off.max() < 1024
+                if t in ("q5_0", "q5_1"):  # fifth-bit (word, bit) places are distinct too
+                    woff = 1024 + (off // 512) * 128 + ((off % 512) // 16) * 4
+                    bit = np.where(nib == 1, 8 * (off % 4) + (off % 16) // 4, 8 * (off % 4) + 4 + (off % 16) // 4)
+                    fb = (woff * 32 + bit).ravel()
+                    assert len(set(fb.tolist())) == 16 * 128 and woff.max() + 4 <= CODE_TILE[t]
     so = scale_offsets()
     assert len(set(so.ravel().tolist())) == 64 and so.max() < 128

@@ -127,3 +127,15 @@ def test_select_tier_rejects_bad_arguments():
                  (1 << 62, 1 << 20, 1 << 10, 1 << 20)]:
         assert kvq.lib.kvq_select_tier(*args, 1 << 30, ctypes.byref(c)) == 1, args
     assert kvq.lib.kvq_select_tier(1, 48, 8, 128, 1 << 30, None) == 1
+
+
+def test_cache_size_of_further_types_is_the_block_footprint():
+    for tk, tv in [("q8_0", "q5_0"), ("q5_0", "q5_0"), ("q5_1", "q5_1"), ("q4_1", "q4_1"), ("q5_1", "q4_0")]:
+        for D in (128, 256):
+            kb, vb, _ = kvq.cache_size(2, 3, D, 64, tk, tv)
+            blocks = 2 * 3 * 64 * D // 32
+            assert kb == blocks * kvq.block_bytes(tk) and vb == blocks * kvq.block_bytes(tv), (tk, tv, D)
+    # pairs outside the supported set are refused
+    d = kvq.Desc(1, 2, 128, 64, kvq.Q5_1, kvq.Q8_0)
+    kb, vb, sb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    assert kvq.lib.kvq_cache_size(ctypes.byref(d), ctypes.byref(kb), ctypes.byref(vb), ctypes.byref(sb)) == 2
