@@ -37,7 +37,7 @@ import numpy as np  # noqa: E402
 import synthetic as syn  # noqa: E402
 
 METRIC = "KV-read GB/s (% of GB300 HBM peak) and decode-attn steps/s vs ctx per KV type"
-BPV = {"f16": 2.0, "q8_0": 34.0 / 32.0, "q4_0": 18.0 / 32.0}
+BPV = {"f16": 2.0, "q8_0": 34 / 32, "q4_0": 18 / 32, "q4_1": 20 / 32, "q5_0": 22 / 32, "q5_1": 24 / 32}
 L2_BYTES = 129 * 10**6
 HBM_FALLBACK = 6800.0
 
@@ -80,6 +80,8 @@ def sweep_workloads(which: str):
     cells.append(syn.dense14b(131072, "q4_0", "q4_0"))
     cells.append(syn.dense14b(262144, "q4_0", "q4_0"))
     cells.append(syn.dense14b(262144, "q8_0", "q8_0"))
+    for tk, tv in (("q8_0", "q5_0"), ("q5_0", "q5_0"), ("q5_1", "q5_1"), ("q4_1", "q4_1"), ("q5_1", "q4_0")):
+        cells.append(syn.dense14b(131072, tk, tv))
     cells.append(syn.multi_session())
     return cells
 

@@ -56,9 +56,11 @@ int auto_splits(const kvq_cache *c, int n_q_heads, int *out, int n_q = 1) {
     const int G = n_q_heads / c->desc.n_kv_heads;
     const int QG = (n_q * G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
     const long long units = static_cast<long long>(c->desc.batch) * c->desc.n_kv_heads * QG;
-    // one full wave of CTAs; two waves when sequences may differ in length
+    // one full wave of CTAs, rounded down so that a unit count that does not divide the
+    // wave does not spill into a partial second one; with several sequences (lengths may
+    // differ) about two waves, rounded up, so that short sequences leave no SM idle
     const long long target = static_cast<long long>(sms) * ctas * (c->desc.batch > 1 ? 2 : 1);
-    long long s = (target + units - 1) / units;
+    long long s = c->desc.batch > 1 ? (target + units - 1) / units : target / units;
     const long long max_tiles = c->desc.capacity / kvq::kTileRows;
     if (s > max_tiles) s = max_tiles;
     if (s > kvq::kMaxSplits) s = kvq::kMaxSplits;
