@@ -302,9 +302,11 @@ KVQ_API kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int
  *
  * kvq_window_decode: decode attention of q [B][Hq][D] over the union of both regions
  * (window_len + tail_len rows per sequence), written like kvq_decode_attention.  Each
- * region runs its own typed decode into one set of split triples in `workspace`
- * (kvq_window_workspace_size bytes; no zeroing needed), and kvq_combine's exact merge
- * forms the result (the read path of section 5 P2).
+ * region runs its own typed decode (the read path of section 5 P2): the window's writes
+ * its normalised result into `workspace`, and the tail's final merge takes that result as
+ * one more split triple, so the output is the exact merge of both regions.  `workspace`:
+ * kvq_window_workspace_size bytes, zeroed once before its first use (as for
+ * kvq_decode_attention).
  */
 KVQ_API kvq_status kvq_window_append(kvq_cache *window, kvq_cache *tail, const float *k, const float *v,
                                      void *stream);

@@ -147,7 +147,7 @@ class WindowedCache:
         return b.value
 
     def workspace(self, n_q_heads):
-        return torch.empty(self.workspace_bytes(n_q_heads), dtype=torch.uint8, device=self.window.device)
+        return torch.zeros(self.workspace_bytes(n_q_heads), dtype=torch.uint8, device=self.window.device)
 
     def decode(self, q, scale=None, out=None, lse=None, workspace=None, stream=None):
         assert q.dtype == torch.float32 and q.is_contiguous() and q.dim() == 3

@@ -595,14 +595,24 @@ static kvq_status window_splits(const kvq_cache *window, const kvq_cache *tail, 
     return KVQ_OK;
 }
 
+// Workspace of a window + tail decode: one decode workspace, used by the window's decode
+// and then by the tail's (each leaves its counters at zero), and the window's result.
+static size_t window_ws(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads, int sw, int stl,
+                        size_t *res_off) {
+    const size_t wsz = ws_layout(window, n_q_heads, sw).total, tsz = ws_layout(tail, n_q_heads, stl).total;
+    const size_t rows = static_cast<size_t>(window->desc.batch) * n_q_heads;
+    *res_off = align256(wsz > tsz ? wsz : tsz);
+    return *res_off + align256(rows * window->desc.head_dim * 4) + align256(rows * 4);
+}
+
 kvq_status kvq_window_workspace_size(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads,
                                      size_t *bytes) {
     if (!bytes) return KVQ_ERR_INVALID_ARG;
     int sw = 0, stl = 0;
     kvq_status st = window_splits(window, tail, n_q_heads, &sw, &stl);
     if (st != KVQ_OK) return st;
-    const size_t rows = static_cast<size_t>(window->desc.batch) * n_q_heads, S = sw + stl;
-    *bytes = 2 * align256(rows * S * 4) + align256(rows * S * window->desc.head_dim * 4);
+    size_t off = 0;
+    *bytes = window_ws(window, tail, n_q_heads, sw, stl, &off);
     return KVQ_OK;
 }
 
@@ -614,30 +624,40 @@ kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *tail, con
     if (st != KVQ_OK) return st;
     if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || (lse && !aligned16(lse)))
         return KVQ_ERR_ALIGNMENT;
-    const int S = sw + stl;
+    size_t res_off = 0;
+    window_ws(window, tail, n_q_heads, sw, stl, &res_off);
     const size_t rows = static_cast<size_t>(window->desc.batch) * n_q_heads;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *pm = reinterpret_cast<float *>(ws);
-    float *pl = reinterpret_cast<float *>(ws + align256(rows * S * 4));
-    float *po = reinterpret_cast<float *>(ws + 2 * align256(rows * S * 4));
+    float *w_out = reinterpret_cast<float *>(ws + res_off);
+    float *w_lse = reinterpret_cast<float *>(ws + res_off + align256(rows * window->desc.head_dim * 4));
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // each region in its own typed launch, both writing into one set of split triples
+    // each region in its own typed decode (the window's first, into the workspace); the
+    // tail's final merge takes the window's result as one more triple
     const kvq_cache *region[2] = {window, tail};
-    const int splits[2] = {sw, stl}, base[2] = {0, sw};
+    const int splits[2] = {sw, stl};
     for (int r = 0; r < 2; ++r) {
+        const WsLayout w = ws_layout(region[r], n_q_heads, splits[r]);
         kvq::DecodeParams p = base_params(region[r], q, n_q_heads, scale, splits[r]);
-        p.part_o = po;
-        p.part_m = pm;
-        p.part_l = pl;
-        p.part_stride = S;
-        p.part_base = base[r];
+        p.out = r == 0 ? w_out : out;
+        p.lse = r == 0 ? w_lse : lse;
+        p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+        p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
+        p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
+        p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
+        p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
+        p.n_groups_max = w.n_groups_max;
+        p.part_m = reinterpret_cast<float *>(ws + w.part_m);
+        p.part_l = reinterpret_cast<float *>(ws + w.part_l);
+        p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+        if (r == 1) {
+            p.ext_out = w_out;
+            p.ext_lse = w_lse;
+        }
         p.early = track_launch(cs, region[r], nullptr) ? 1 : 0;
-        if (kvq::launch_decode(region[r]->desc.type_k, region[r]->desc.type_v, p, false, cs) != cudaSuccess)
+        if (kvq::launch_decode(region[r]->desc.type_k, region[r]->desc.type_v, p, true, cs) != cudaSuccess)
             return KVQ_ERR_CUDA;
     }
-    kvq::CombineParams c{po, pm, pl, out, lse, static_cast<int>(rows), S, window->desc.head_dim};
-    track_launch(cs, nullptr, nullptr);
-    return cuda_status(kvq::launch_combine(c, cs));
+    return KVQ_OK;
 }
 
 // ---- decode without a caller workspace: scratch compiled into the library ----

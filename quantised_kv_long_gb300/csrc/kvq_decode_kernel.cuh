@@ -151,7 +151,8 @@ struct RowMap {
 constexpr int kMergeChunk = 10;
 __device__ void merge_rows(const float *po, const float *pm, const float *pl, int stride, int s0, int NP,
                            size_t row0, int rows, int D, float *out, float *lse, float *qo, float *qm, float *ql,
-                           int q_stride, int q_s, const RowMap map = RowMap{1, 1, 1, 1}) {
+                           int q_stride, int q_s, const RowMap map = RowMap{1, 1, 1, 1},
+                           const float *ext_out = nullptr, const float *ext_lse = nullptr) {
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int DQ = D / 4;
     const int C = rows * DQ;
@@ -215,8 +216,21 @@ __device__ void merge_rows(const float *po, const float *pm, const float *pl, in
         for (int k = 0; k < 2; ++k) {
             if (!v[k]) continue;
             if (out) {
-                const float inv = L[k] > 0.f ? 1.f / L[k] : 0.f;
                 const size_t orow = map.out_row(row0 + g[k]);
+                if (ext_out) {  // one more triple: (ext_out, lse, l = 1)
+                    const float mx = ext_lse[orow];
+                    const float Mn = fmaxf(M[k], mx);
+                    if (Mn != -CUDART_INF_F) {
+                        const float a = M[k] == -CUDART_INF_F ? 0.f : expf(M[k] - Mn);
+                        const float bw = mx == -CUDART_INF_F ? 0.f : expf(mx - Mn);
+                        const float4 x = reinterpret_cast<const float4 *>(ext_out + orow * D)[dq[k]];
+                        A[k] = make_float4(fmaf(bw, x.x, a * A[k].x), fmaf(bw, x.y, a * A[k].y),
+                                           fmaf(bw, x.z, a * A[k].z), fmaf(bw, x.w, a * A[k].w));
+                        L[k] = fmaf(a, L[k], bw);
+                        M[k] = Mn;
+                    }
+                }
+                const float inv = L[k] > 0.f ? 1.f / L[k] : 0.f;
                 reinterpret_cast<float4 *>(out + orow * D)[dq[k]] =
                     make_float4(A[k].x * inv, A[k].y * inv, A[k].z * inv, A[k].w * inv);
                 if (dq[k] == 0 && lse) lse[orow] = L[k] > 0.f ? M[k] + logf(L[k]) : -CUDART_INF_F;
@@ -972,8 +986,21 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
             }
         }
         if (single) {
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             const size_t orow = rmap.out_row(prow0 + g);
+            if (p.ext_out) {  // one more triple (ext_out, lse, l = 1), in log2 units here
+                const float mx = p.ext_lse[orow] * 1.44269504088896340736f;
+                const float Mn = fmaxf(M, mx);
+                if (Mn != -CUDART_INF_F) {
+                    const float a = M == -CUDART_INF_F ? 0.f : ex2(M - Mn);
+                    const float bw = mx == -CUDART_INF_F ? 0.f : ex2(mx - Mn);
+                    const float4 x = reinterpret_cast<const float4 *>(p.ext_out + orow * D)[dq];
+                    acc = make_float4(fmaf(bw, x.x, a * acc.x), fmaf(bw, x.y, a * acc.y), fmaf(bw, x.z, a * acc.z),
+                                      fmaf(bw, x.w, a * acc.w));
+                    lsum = fmaf(a, lsum, bw);
+                    M = Mn;
+                }
+            }
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             reinterpret_cast<float4 *>(p.out + orow * D)[dq] =
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             if (dq == 0 && p.lse) p.lse[orow] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -CUDART_INF_F;
@@ -997,7 +1024,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     if (static_cast<long long>(ns) * rows * (D + 2) * 4 <= kDirectMergeBytes) {
         if (!arrive_last(p.counters + unit, ns, s_flag)) return;
         merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, 0, ns, row0, rows, D, p.out, p.lse, nullptr, nullptr,
-                   nullptr, 0, 0, rmap);
+                   nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
         if (threadIdx.x == 0) p.counters[unit] = 0;
         return;
     }
@@ -1012,7 +1039,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     if (threadIdx.x == 0) *cnt1 = 0;
     if (!arrive_last(p.counters + unit, n_groups, s_flag)) return;
     merge_rows(p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, 0, n_groups, row0, rows, D, p.out, p.lse, nullptr,
-               nullptr, nullptr, 0, 0, rmap);
+               nullptr, nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
     if (threadIdx.x == 0) p.counters[unit] = 0;
 }
 

@@ -72,6 +72,9 @@ struct DecodeParams {
     // attending to positions [0, len[b] - n_q + i] (causal within the draft).  The rows of a
     // (sequence, KV head) are ordered r = i * G + g and grouped 8 per CTA (QG groups).
     int n_q;
+    // optional: a normalised result (out, natural-log lse per query row) over other keys,
+    // merged exactly into this decode's output (the window of a window + tail cache)
+    const float *ext_out, *ext_lse;
     int cap_tiles;
     int n_splits;
     float scale_log2;     // scale * log2(e)
