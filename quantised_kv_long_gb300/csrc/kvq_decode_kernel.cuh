@@ -285,7 +285,10 @@ struct Cfg {
     static constexpr int STAGES_RAW = RING_BUDGET / STAGE;
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 16 ? 16 : STAGES_RAW);
     static constexpr int RING = STAGES * STAGE;
-    static constexpr int XCHG = NS == 2 ? TW * 2 * 2 * 32 * 16 * TPW : 0;
+    // score exchange of the two slice-warps of each tile pair (double-buffered), then one
+    // guard flag per warp and buffer
+    static constexpr int XCHG_SC = NS == 2 ? TW * 2 * 2 * 32 * 16 * TPW : 0;
+    static constexpr int XCHG = NS == 2 ? XCHG_SC + (TW * 2 * 2 * 4 + 15) / 16 * 16 : 0;
     static constexpr int BAR_OFF = RING + XCHG;
     // per consumer warp: the K code-offset corrections of its 8 rows x 4 blocks
     static constexpr int KCOR_OFF = (BAR_OFF + 2 * STAGES * 8 + 15) / 16 * 16;
@@ -759,6 +762,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
         uint32_t magic;  // 0x64006400 in a register, so each nibble mask-and-or is one instruction
         asm volatile("mov.b32 %0, 0x64006400;\n" : "=r"(magic));
         float4 *xchg = reinterpret_cast<float4 *>(smem + C::RING);
+        int *xflag = reinterpret_cast<int *>(smem + C::RING + C::XCHG_SC);
         bool dead = false;
         // keys of this lane inside a tile: A=2j, B=2j+1, C=8+2j, D=9+2j
         const int kofs[4] = {2 * j, 2 * j + 1, 8 + 2 * j, 9 + 2 * j};
@@ -782,17 +786,42 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                                     st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * scale_tile_bytes(KT), qa, kcor_row, lane,
                                     j, sc[t]);
                 }
+                // f16 overflow guard: p = exp2(s - m_run) may reach 2^kTau before the running
+                // maximum is moved, so a tile pair holding a V scale with |scale| >= 256 (or
+                // inf/nan bits) takes an exact rescale instead.  The exponent test on an OR of
+                // the scale words may over-report, which only costs that exact rescale.
+                auto guard = [&]() {
+                    bool x = false;
+                    if constexpr (VT != KVQ_F16) {
+                        uint32_t e = 0;
+#pragma unroll
+                        for (int t = 0; t < TPW; ++t) {
+                            const uint8_t *vs = st + C::TWT * (C::KC + C::VC + C::KS) + (tw * TPW + t) * C::VS + sl * scale_tile_bytes(VT);
+                            const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
+                            e |= (sc0.x | sc0.y | sc0.z) | (sc0.w | sc1.x | sc1.y) | (sc1.z | sc1.w);
+                        }
+                        x = __any_sync(0xffffffffu, __vcmpgeu2(e & 0x7c007c00u, 0x5c005c00u) != 0);
+                    }
+                    return x;
+                };
+                bool exact = false;
+                if constexpr (NS == 2) exact = guard();
                 if constexpr (NS == 2) {
-                    // the two slice-warps of this tile pair add their partial scores
+                    // the two slice-warps of this tile pair add their partial scores, and agree
+                    // on the guard (each saw the V scales of its own slice only): their running
+                    // maxima must move together, as the merge keeps one per tile pair
+                    const int xi = (tw * 2 + (k & 1)) * 2;
 #pragma unroll
                     for (int t = 0; t < TPW; ++t) {
-                        float4 *mine = xchg + (((tw * 2 + (k & 1)) * 2 + sl) * TPW + t) * 32;
+                        float4 *mine = xchg + ((xi + sl) * TPW + t) * 32;
                         mine[lane] = make_float4(sc[t][0], sc[t][1], sc[t][2], sc[t][3]);
                     }
+                    if (lane == 0) xflag[xi + sl] = exact ? 1 : 0;
                     asm volatile("bar.sync %0, 64;\n" ::"r"(1 + tw) : "memory");
+                    exact = exact || xflag[xi + 1 - sl] != 0;
 #pragma unroll
                     for (int t = 0; t < TPW; ++t) {
-                        const float4 os = xchg[(((tw * 2 + (k & 1)) * 2 + (1 - sl)) * TPW + t) * 32 + lane];
+                        const float4 os = xchg[((xi + 1 - sl) * TPW + t) * 32 + lane];
                         sc[t][0] += os.x;
                         sc[t][1] += os.y;
                         sc[t][2] += os.z;
@@ -833,26 +862,12 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 }
 
                 // ---- online softmax (log2 units) over TPW x 16 keys, lazy rescale ----
-                // p = exp2(s - m_run) may reach 2^kTau before the running maximum is moved;
-                // the V scales are checked so that p * scale can never overflow f16.
                 float mt = -CUDART_INF_F;
 #pragma unroll
                 for (int t = 0; t < TPW; ++t) mt = fmaxf(mt, fmaxf(fmaxf(sc[t][0], sc[t][1]), fmaxf(sc[t][2], sc[t][3])));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-                bool exact = false;
-                if constexpr (VT != KVQ_F16) {
-                    uint32_t e = 0;
-#pragma unroll
-                    for (int t = 0; t < TPW; ++t) {
-                        const uint8_t *vs = st + C::TWT * (C::KC + C::VC + C::KS) + (tw * TPW + t) * C::VS + sl * scale_tile_bytes(VT);
-                        const uint4 sc0 = lds128(vs + j * 32), sc1 = lds128(vs + j * 32 + 16);
-                        e |= (sc0.x | sc0.y | sc0.z) | (sc0.w | sc1.x | sc1.y) | (sc1.z | sc1.w);
-                    }
-                    // exponent field of any |scale| >= 256 (or inf/nan); an OR may over-report,
-                    // which only costs an exact rescale.  The four lanes of a row must agree.
-                    exact = __any_sync(0xffffffffu, __vcmpgeu2(e & 0x7c007c00u, 0x5c005c00u) != 0);
-                }
+                if constexpr (NS == 1) exact = guard();
                 const bool need = mt > m_run + (exact ? 0.f : kTau);
                 if (__any_sync(0xffffffffu, need)) {
                     const float m_new = need ? mt : m_run;

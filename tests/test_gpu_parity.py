@@ -178,6 +178,53 @@ def test_decode_lengths_and_splits(kvq, lens, n_splits):
     run_case(kvq, "q8_0", "q4_0", 128, Hkv=2, G=4, lens=lens, cap=2064, n_splits=n_splits, seed=len(lens))
 
 
+@pytest.mark.parametrize("tk,tv", [("q8_0", "q8_0"), ("q4_0", "q4_0"), ("q8_0", "q4_0")])
+@pytest.mark.parametrize("n_splits", [4, 7, 13])
+def test_decode_d256_split_tile_counts(kvq, tk, tv, n_splits):
+    """Head dim 256 (two slice-warps per tile pair) with 33, 19 and 10 tiles per split: the
+    last stage of a split is partial, sometimes with an odd tile count, so the second tile
+    of a pair lies in a ring slot that holds stale or never-written bytes."""
+    run_case(kvq, tk, tv, 256, Hkv=2, G=8, lens=[2049], cap=2064, n_splits=n_splits, seed=n_splits)
+
+
+@pytest.mark.parametrize("tk,tv", [("q8_0", "q8_0"), ("q4_0", "q4_0"), ("q8_0", "q4_0"), ("q5_1", "q5_1")])
+@pytest.mark.parametrize("big_slice", [0, 1])
+def test_decode_large_v_scales_in_one_slice(kvq, tk, tv, big_slice):
+    """V blocks with |scale| >= 256 in one 128-value half of a 256-wide head only (every
+    other tile).  The f16 overflow guard then fires for one slice-warp of each tile pair and
+    not the other; both must still move their running maximum together, or the merge
+    combines accumulators taken against different maxima."""
+    B, H, G, D, L = 1, 2, 8, 256, 700
+    wl = syn.Workload("bigv", 1, B, H * G, H, D, tk, tv, (L,), seed=31 + big_slice)
+    cache = kvq.KVCache(B, H, D, 704, tk, tv)
+    K = torch.stack([syn.kv_rows(wl, syn.KIND_K, 0, 0, h, 0, L) for h in range(H)])
+    V = torch.stack([syn.kv_rows(wl, syn.KIND_V, 0, 0, h, 0, L) for h in range(H)])
+    # scale d = amax / 127 (q8_0) or amax / 8 (4- and 5-bit types) reaches 256 and more
+    factor = 1.0e4 if tv == "q8_0" else 2.0e3
+    big = torch.zeros(L, dtype=torch.bool, device=V.device)
+    big[(torch.arange(L, device=V.device) // 16) % 2 == 1] = True
+    lo, hi = big_slice * 128, big_slice * 128 + 128
+    V[:, big, lo:hi] *= factor
+    cache.append(K[None].contiguous(), V[None].contiguous())
+    q = syn.queries(wl, 0)
+    out, lse = cache.decode(q, scale=wl.scale, n_splits=2)
+    torch.cuda.synchronize()
+    assert cache.read_error() == 0
+    kc, ks = oracle.quantize(tk, K.cpu().numpy())
+    vc, vs = oracle.quantize(tv, V.cpu().numpy())
+    spb = oracle.scales_per_block(tv)
+    d = vs.view(np.float16).astype(np.float64)[..., ::spb]  # the block scales d (not the minima)
+    assert np.abs(d[:, :, lo // 32:hi // 32]).max() >= 256  # the guard's threshold is reached
+    assert np.abs(d[:, :, (128 - lo) // 32:(256 - lo) // 32]).max() < 256
+    ref, ref_lse = oracle.attention(tk, kc, ks, tv, vc, vs, L, q[0].cpu().numpy(), wl.scale)
+    o = out[0].cpu().numpy()
+    other = slice(128 - lo, 256 - lo) if big_slice == 0 else slice(0, 128)
+    assert np.abs(o[:, other] - ref[:, other]).max() <= TOL
+    # the large half: f32 accumulation of values up to about 4 x factor
+    assert np.abs(o[:, lo:hi] - ref[:, lo:hi]).max() <= TOL + 1e-5 * factor
+    assert np.abs(lse[0].cpu().numpy() - ref_lse).max() <= TOL
+
+
 @pytest.mark.parametrize("G", [9, 16, 12])
 def test_decode_wide_groups(kvq, G):
     """More than 8 query heads per KV head: several row groups per KV head."""
