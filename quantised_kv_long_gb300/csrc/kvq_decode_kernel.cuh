@@ -18,8 +18,9 @@
 //     with 16-byte shared loads, converts codes to exact f16 integers with bit tricks
 //     (no I2F), and runs mma.sync m16n8k16 (f16 in, fp32 accumulate).
 //     S = Q K^T: A = [Q_hi ; Q_lo] (M rows 0-7 / 8-15 = up to 8 query heads split into
-//     f16 hi + lo parts, so Q loses nothing), B = K codes (exact), one accumulator per
-//     32-value block, multiplied by the f16 scale afterwards in fp32.
+//     f16 hi + lo parts, so Q loses nothing; built once per slice in shared memory and
+//     read by every tile-warp), B = K codes (exact), one accumulator per 32-value block,
+//     multiplied by the f16 scale afterwards in fp32.
 //     O += P V: the S accumulator layout is the A layout of the next mma, so P never
 //     leaves registers; the V scale of each (row, block) is folded into P, which is
 //     again split into f16 hi + lo rows.
@@ -267,7 +268,9 @@ __device__ __noinline__ void grid_ticket(const DecodeParams &p, int cap_rows) {
 
 template <int KT, int VT, int NS>
 struct Cfg {
-    static constexpr int TW = NS == 1 ? 8 : 4;  // tile-warps (per 128-value slice)
+    // tile-warps per 128-value slice: 11 for 128-wide heads with quantised keys (the
+    // conversion work wants the warps), 8 for f16 keys, 4 pairs for 256-wide heads
+    static constexpr int TW = NS == 2 ? 4 : (KT == KVQ_F16 ? 8 : 11);
     static constexpr int CW = TW * NS;         // consumer warps
     static constexpr int THREADS = 32 * (CW + 1);
     static constexpr int KC = code_tile_bytes(KT) * NS;
@@ -275,7 +278,7 @@ struct Cfg {
     static constexpr int KS = scale_tile_bytes(KT) * NS;
     static constexpr int VS = scale_tile_bytes(VT) * NS;
     static constexpr int TILE = KC + VC + KS + VS;
-    static constexpr int MIN_CTAS = 1;         // one CTA per SM: 8 consumer warps + 1 producer
+    static constexpr int MIN_CTAS = 1;         // one CTA per SM: up to 11 consumer warps + 1 producer
     static constexpr int RING_BUDGET = 196608;
     // tiles each warp takes per stage: two (32 keys share one softmax step) when the ring
     // still holds at least two stages, else one
@@ -290,19 +293,30 @@ struct Cfg {
     static constexpr int XCHG_SC = NS == 2 ? TW * 2 * 2 * 32 * 16 * TPW : 0;
     static constexpr int XCHG = NS == 2 ? XCHG_SC + (TW * 2 * 2 * 4 + 15) / 16 * 16 : 0;
     static constexpr int BAR_OFF = RING + XCHG;
-    // per consumer warp: the K code-offset corrections of its 8 rows x 4 blocks
+    // per slice: the K code-offset corrections of its 8 rows x 4 blocks, and the Q
+    // fragments (8 chunks x 32 lanes x 16 B) that every tile-warp of the slice reads
     static constexpr int KCOR_OFF = (BAR_OFF + 2 * STAGES * 8 + 15) / 16 * 16;
-    static constexpr int SMEM = KCOR_OFF + CW * 128 + 16;
+    static constexpr int QSM_OFF = KCOR_OFF + NS * 128;
+    static constexpr int SMEM = QSM_OFF + NS * 8 * 32 * 16 + 16;
     static constexpr int D = NS * kSlice;
     // merge / combine scratch reuses the ring
     static_assert(TW * kMaxRowsPerGroup * D * 4 + 2 * TW * kMaxRowsPerGroup * 4 <= RING, "merge buffer");
 };
 
+struct QFrag {
+    uint32_t a[4];
+};
+
 // Scores of one tile over this warp's 128-value slice for keys A=2j, B=2j+1 (S-tile 0) and
 // C=8+2j, D=9+2j (S-tile 1), row g = lane/4, in log2 units (Q was prescaled).
 template <int KT>
-__device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks, const uint32_t (&qa)[8][4],
+__device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks, const uint8_t *qsm,
                                             const uint8_t *kcor, int lane, int j, float (&s)[4]) {
+    // Q fragment of chunk c (16 values), read from shared memory where it is used
+    auto qa = [&](int c) {
+        const uint4 v = lds128(qsm + (c * 32 + lane) * 16);
+        return QFrag{{v.x, v.y, v.z, v.w}};
+    };
     if constexpr (KT == KVQ_F16) {
         float acc[2][4];
 #pragma unroll
@@ -310,14 +324,14 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
             const uint4 w0 = lds128(kc + (2 * b + 0) * 512 + lane * 16);
             const uint4 w1 = lds128(kc + (2 * b + 1) * 512 + lane * 16);
             if (b == 0) {
-                mma_16816_z(acc[0], qa[0], w0.x, w0.y);
-                mma_16816_z(acc[1], qa[0], w1.x, w1.y);
+                mma_16816_z(acc[0], qa(0).a, w0.x, w0.y);
+                mma_16816_z(acc[1], qa(0).a, w1.x, w1.y);
             } else {
-                mma_16816(acc[0], qa[2 * b], w0.x, w0.y);
-                mma_16816(acc[1], qa[2 * b], w1.x, w1.y);
+                mma_16816(acc[0], qa(2 * b).a, w0.x, w0.y);
+                mma_16816(acc[1], qa(2 * b).a, w1.x, w1.y);
             }
-            mma_16816(acc[0], qa[2 * b + 1], w0.z, w0.w);
-            mma_16816(acc[1], qa[2 * b + 1], w1.z, w1.w);
+            mma_16816(acc[0], qa(2 * b + 1).a, w0.z, w0.w);
+            mma_16816(acc[1], qa(2 * b + 1).a, w1.z, w1.w);
         }
         s[0] = acc[0][0] + acc[0][2];
         s[1] = acc[0][1] + acc[0][3];
@@ -346,18 +360,18 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
             float acc[2][4];
             if constexpr (KT == KVQ_Q8_0) {
                 const uint4 w = lds128(kc + b * 512 + lane * 16);
-                mma_16816_z(acc[0], qa[2 * b], q8_02(w.x), q8_13(w.x));
-                mma_16816(acc[0], qa[2 * b + 1], q8_02(w.y), q8_13(w.y));
-                mma_16816_z(acc[1], qa[2 * b], q8_02(w.z), q8_13(w.z));
-                mma_16816(acc[1], qa[2 * b + 1], q8_02(w.w), q8_13(w.w));
+                mma_16816_z(acc[0], qa(2 * b).a, q8_02(w.x), q8_13(w.x));
+                mma_16816(acc[0], qa(2 * b + 1).a, q8_02(w.y), q8_13(w.y));
+                mma_16816_z(acc[1], qa(2 * b).a, q8_02(w.z), q8_13(w.z));
+                mma_16816(acc[1], qa(2 * b + 1).a, q8_02(w.w), q8_13(w.w));
             } else if constexpr (!has_fifth_bit(KT)) {
                 if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
                 const uint32_t w0 = (b & 1) ? wq4.z : wq4.x, w0s = w0 >> 8;
                 const uint32_t w1 = (b & 1) ? wq4.w : wq4.y, w1s = w1 >> 8;
-                mma_16816_z(acc[0], qa[2 * b], w0 & kNibLo, w0s & kNibLo);
-                mma_16816(acc[0], qa[2 * b + 1], w0 & kNibHi, w0s & kNibHi);
-                mma_16816_z(acc[1], qa[2 * b], w1 & kNibLo, w1s & kNibLo);
-                mma_16816(acc[1], qa[2 * b + 1], w1 & kNibHi, w1s & kNibHi);
+                mma_16816_z(acc[0], qa(2 * b).a, w0 & kNibLo, w0s & kNibLo);
+                mma_16816(acc[0], qa(2 * b + 1).a, w0 & kNibHi, w0s & kNibHi);
+                mma_16816_z(acc[1], qa(2 * b).a, w1 & kNibLo, w1s & kNibLo);
+                mma_16816(acc[1], qa(2 * b + 1).a, w1 & kNibHi, w1s & kNibHi);
             } else {
                 if ((b & 1) == 0) {
                     wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
@@ -367,10 +381,10 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
                 uint32_t c0[4], c1[4];
                 fifth_bit_codes((b & 1) ? wq4.z : wq4.x, hb >> wi0, c0);
                 fifth_bit_codes((b & 1) ? wq4.w : wq4.y, hb >> wi1, c1);
-                mma_16816_z(acc[0], qa[2 * b], c0[0], c0[1]);
-                mma_16816(acc[0], qa[2 * b + 1], c0[2], c0[3]);
-                mma_16816_z(acc[1], qa[2 * b], c1[0], c1[1]);
-                mma_16816(acc[1], qa[2 * b + 1], c1[2], c1[3]);
+                mma_16816_z(acc[0], qa(2 * b).a, c0[0], c0[1]);
+                mma_16816(acc[0], qa(2 * b + 1).a, c0[2], c0[3]);
+                mma_16816_z(acc[1], qa(2 * b).a, c1[0], c1[1]);
+                mma_16816(acc[1], qa(2 * b + 1).a, c1[2], c1[3]);
             }
             const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
             const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
@@ -723,9 +737,10 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
         // low-nibble chunk of each block is prescaled by 16 (exact) to match the high
         // nibbles, which arrive as 16c, and kcorr[b] = -8 times the block's sum of q in the
         // accumulator unit is kept for each row.
-        uint32_t qa[8][4];
-        uint8_t *kcor_row = smem + C::KCOR_OFF + cw * 128 + g * 16;
-        {
+        uint8_t *kcor_row = smem + C::KCOR_OFF + sl * 128 + g * 16;
+        uint8_t *qsm = smem + C::QSM_OFF + sl * (8 * 32 * 16);
+        if (tw == 0) {  // one warp per slice builds what all tile-warps of the slice read
+            uint32_t qa[8][4];
             float kcorr[4] = {0.f, 0.f, 0.f, 0.f};
             const bool rv = g < rows;
             const float *qrow = p.q + rmap.out_row(prow0 + (rv ? g : 0)) * p.D + sl * kSlice;
@@ -740,6 +755,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 const float f = ((KT == KVQ_Q4_0 || KT == KVQ_Q4_1) && (c & 1) == 0) ? 16.f : 1.f;
                 split_hi_lo(x.x * f, x.z * f, qa[c][0], qa[c][1]);  // k = 2j, 2j+1  <->  d + 0, d + 2
                 split_hi_lo(x.y * f, x.w * f, qa[c][2], qa[c][3]);  // k = 2j+8, 2j+9 <-> d + 1, d + 3
+                *reinterpret_cast<uint4 *>(qsm + (c * 32 + lane) * 16) = make_uint4(qa[c][0], qa[c][1], qa[c][2], qa[c][3]);
             }
             if constexpr (is_nibble_type(KT)) {
                 // per row and block: -8 (q4_0) or -16 (q5_0) times sum_b q, or sum_b q for the
@@ -755,9 +771,9 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 // kept in shared memory (one row of 4 per lane group) instead of registers
                 if (j == 0)
                     *reinterpret_cast<float4 *>(kcor_row) = make_float4(kcorr[0], kcorr[1], kcorr[2], kcorr[3]);
-                __syncwarp();
             }
         }
+        asm volatile("bar.sync 15, %0;\n" ::"r"(C::CW * 32) : "memory");  // consumer warps only
         float corr[4] = {0.f, 0.f, 0.f, 0.f};  // V types with a minimum: sum of p * lo per block (column b)
         uint32_t magic;  // 0x64006400 in a register, so each nibble mask-and-or is one instruction
         asm volatile("mov.b32 %0, 0x64006400;\n" : "=r"(magic));
@@ -783,7 +799,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                 for (int t = 0; t < TPW; ++t) {
                     const int ti = tw * TPW + t;  // tile index inside the stage
                     tile_scores<KT>(st + ti * C::KC + sl * code_tile_bytes(KT),
-                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * scale_tile_bytes(KT), qa, kcor_row, lane,
+                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * scale_tile_bytes(KT), qsm, kcor_row, lane,
                                     j, sc[t]);
                 }
                 // f16 overflow guard: p = exp2(s - m_run) may reach 2^kTau before the running
