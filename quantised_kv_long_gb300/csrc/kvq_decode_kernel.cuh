@@ -247,6 +247,116 @@ __device__ void merge_rows(const float *po, const float *pm, const float *pl, in
     }
 }
 
+// Wide merge: when the grid is resident at once, the last P CTAs to arrive for a row group
+// share its merge, each taking a range of output columns (float4 columns c of the rows x
+// D/4 grid, row c / (D/4)).  Each column is served by sg threads, thread k taking splits
+// k, k + sg, ... with the same running-maximum rule as merge_rows (a handful of splits per
+// thread, one L2 round trip); the sg partial triples of a column are then combined in
+// shared memory.  Memory for the reduction: 24 bytes per thread at `red`.
+constexpr int kWideMinBytes = kDirectMergeBytes;  // smaller row groups merge in one CTA
+constexpr int kWideBytes = 32 * 1024;     // triple bytes per merging CTA
+constexpr int kWideChunk = 8;
+__device__ void merge_cols(const float *po, const float *pm, const float *pl, int stride, int NP, size_t row0,
+                           int D, int c0, int c1, float *out, float *lse, const RowMap map, const float *ext_out,
+                           const float *ext_lse, uint8_t *red) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int DQ = D / 4;
+    const int ncol = c1 - c0;
+    const int sg = max(1, min(nthr / max(ncol, 1), (NP + 3) / 4));  // threads per column
+    float4 *rA = reinterpret_cast<float4 *>(red);
+    float *rM = reinterpret_cast<float *>(red + static_cast<size_t>(nthr) * 16);
+    float *rL = rM + nthr;
+    const float4 *po4 = reinterpret_cast<const float4 *>(po);
+    for (int base = 0; base < ncol * sg; base += nthr) {
+        const int item = base + tid;
+        const bool v = item < ncol * sg;
+        const int ci = v ? item % ncol : 0, k = v ? item / ncol : 0;
+        const int col = c0 + ci;
+        const size_t pr = (row0 + col / DQ) * stride;
+        const int dq = col % DQ;
+        float M = -CUDART_INF_F, L = 0.f;
+        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = k; v && s < NP; s += kWideChunk * sg) {
+            float mm[kWideChunk], ll[kWideChunk];
+            float4 oo[kWideChunk];
+#pragma unroll
+            for (int u = 0; u < kWideChunk; ++u) {
+                const int su = s + u * sg;
+                const bool in = su < NP;
+                mm[u] = in ? __ldcg(pm + pr + su) : -CUDART_INF_F;
+                ll[u] = in ? __ldcg(pl + pr + su) : 0.f;
+                oo[u] = in ? __ldcg(po4 + (pr + su) * DQ + dq) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float cm = -CUDART_INF_F;
+#pragma unroll
+            for (int u = 0; u < kWideChunk; ++u) cm = fmaxf(cm, mm[u]);
+            const float Mn = fmaxf(M, cm);
+            if (Mn == -CUDART_INF_F) continue;
+            const float a = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
+            A = make_float4(A.x * a, A.y * a, A.z * a, A.w * a);
+            L *= a;
+#pragma unroll
+            for (int u = 0; u < kWideChunk; ++u) {
+                const float w = mm[u] == -CUDART_INF_F ? 0.f : expf(mm[u] - Mn);
+                A = make_float4(fmaf(w, oo[u].x, A.x), fmaf(w, oo[u].y, A.y), fmaf(w, oo[u].z, A.z), fmaf(w, oo[u].w, A.w));
+                L = fmaf(w, ll[u], L);
+            }
+            M = Mn;
+        }
+        if (sg > 1) {
+            if (v) {
+                rA[k * ncol + ci] = A;
+                rM[k * ncol + ci] = M;
+                rL[k * ncol + ci] = L;
+            }
+            __syncthreads();
+            if (v && k == 0) {
+                for (int k2 = 1; k2 < sg; ++k2) {
+                    const float m2 = rM[k2 * ncol + ci];
+                    const float Mn = fmaxf(M, m2);
+                    if (Mn == -CUDART_INF_F) continue;
+                    const float a = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
+                    const float b = m2 == -CUDART_INF_F ? 0.f : expf(m2 - Mn);
+                    const float4 x = rA[k2 * ncol + ci];
+                    A = make_float4(fmaf(b, x.x, a * A.x), fmaf(b, x.y, a * A.y), fmaf(b, x.z, a * A.z), fmaf(b, x.w, a * A.w));
+                    L = fmaf(b, rL[k2 * ncol + ci], a * L);
+                    M = Mn;
+                }
+            }
+            __syncthreads();
+        }
+        if (!v || k != 0) continue;
+        const size_t orow = map.out_row(row0 + col / DQ);
+        if (ext_out) {  // one more triple: (ext_out, lse, l = 1)
+            const float mx = ext_lse[orow];
+            const float Mn = fmaxf(M, mx);
+            if (Mn != -CUDART_INF_F) {
+                const float a = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
+                const float bw = mx == -CUDART_INF_F ? 0.f : expf(mx - Mn);
+                const float4 x = reinterpret_cast<const float4 *>(ext_out + orow * D)[dq];
+                A = make_float4(fmaf(bw, x.x, a * A.x), fmaf(bw, x.y, a * A.y), fmaf(bw, x.z, a * A.z), fmaf(bw, x.w, a * A.w));
+                L = fmaf(a, L, bw);
+                M = Mn;
+            }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        reinterpret_cast<float4 *>(out + orow * D)[dq] = make_float4(A.x * inv, A.y * inv, A.z * inv, A.w * inv);
+        if (dq == 0 && lse) lse[orow] = L > 0.f ? M + logf(L) : -CUDART_INF_F;
+    }
+}
+
+// Bounded wait (thread 0) until *counter >= target; false after about two seconds.
+__device__ __forceinline__ bool wait_count(const int32_t *counter, int target) {
+    const long long t0 = clock64();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(counter) : "memory");
+        if (v >= target) return true;
+        if (clock64() - t0 > kWaitCycles) return false;
+        __nanosleep(64);
+    }
+}
+
 // Fused append: every CTA of the grid arrives once, after it has read the lengths; the
 // last one advances len[b] by one for each sequence that had room (else it reports
 // KVQ_DEVERR_CAPACITY) and resets the ticket.  Called by one thread per CTA.
@@ -1052,7 +1162,37 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     // group triple while other CTAs still run, and the last group merges the group triples.
     const size_t unit = (static_cast<size_t>(bseq) * p.Hkv + h) * p.QG + qg;
     const size_t row0 = prow0;
-    if (static_cast<long long>(ns) * rows * (D + 2) * 4 <= kDirectMergeBytes) {
+    const long long tbytes = static_cast<long long>(ns) * rows * (D + 2) * 4;
+    if (p.wide && tbytes > kWideMinBytes) {
+        // the last P arrivals each merge a range of columns once every split has arrived;
+        // their second arrivals count P more, and the last of those clears the counter
+        const int C = rows * (D / 4);
+        const int P = max(1, min(min(ns, C), static_cast<int>((tbytes + kWideBytes - 1) / kWideBytes)));
+        int32_t *cnt = p.counters + unit;
+        __threadfence();  // each thread publishes its own writes
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int t = atomicAdd(cnt, 1);
+            int role = t >= ns - P ? t - (ns - P) : -1;  // merger index, or -1
+            if (role >= 0 && t != ns - 1 && !wait_count(cnt, ns)) {
+                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
+                role = -2;  // a merger that gave up: no merge, but its second arrival counts
+            }
+            s_flag = role;
+        }
+        __syncthreads();
+        const int role = s_flag;
+        if (role == -1) return;
+        if (role >= 0) {
+            __threadfence();
+            merge_cols(p.part_o, p.part_m, p.part_l, p.n_splits, ns, row0, D, role * C / P, (role + 1) * C / P,
+                       p.out, p.lse, rmap, p.ext_out, p.ext_lse, smem);
+            __syncthreads();
+        }
+        if (threadIdx.x == 0 && atomicAdd(cnt, 1) == ns + P - 1) atomicExch(cnt, 0);
+        return;
+    }
+    if (tbytes <= kDirectMergeBytes) {
         if (!arrive_last(p.counters + unit, ns, s_flag)) return;
         merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, 0, ns, row0, rows, D, p.out, p.lse, nullptr, nullptr,
                    nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
@@ -1091,26 +1231,6 @@ cudaError_t configure_t(int dev) {
 }
 
 template <int KT, int VT, int NS, bool MQ>
-cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stream) {
-    using C = Cfg<KT, VT, NS>;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = configure_t<KT, VT, NS, MQ>(dev);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B * p.QG);
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<KT, VT, NS, MQ>, p, fused ? 1 : 0);
-}
-
-template <int KT, int VT, int NS, bool MQ>
 cudaError_t occupancy_t(int *ctas) {
     using C = Cfg<KT, VT, NS>;
     // resident CTAs per SM, queried once per (instance, device)
@@ -1128,6 +1248,48 @@ cudaError_t occupancy_t(int *ctas) {
     *ctas = cached[dev];
     return cudaSuccess;
 }
+
+// SM count of a device, queried once
+inline cudaError_t sm_count(int dev, int *n) {
+    static int cached[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (cached[dev] == 0) {
+        int v = 0;
+        const cudaError_t e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cached[dev] = v > 0 ? v : 1;
+    }
+    *n = cached[dev];
+    return cudaSuccess;
+}
+
+template <int KT, int VT, int NS, bool MQ>
+cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stream) {
+    using C = Cfg<KT, VT, NS>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = configure_t<KT, VT, NS, MQ>(dev);
+    int occ = 1, sms = 0;
+    if (e == cudaSuccess) e = occupancy_t<KT, VT, NS, MQ>(&occ);
+    if (e == cudaSuccess) e = sm_count(dev, &sms);
+    if (e != cudaSuccess) return e;
+    // a grid that is resident at once lets the last CTAs of a row group wait for the rest
+    DecodeParams q = p;
+    const long long ctas = static_cast<long long>(p.n_splits) * p.Hkv * p.B * p.QG;
+    q.wide = (fused && ctas <= static_cast<long long>(occ) * sms) ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B * p.QG);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<KT, VT, NS, MQ>, q, fused ? 1 : 0);
+}
+
 
 }  // namespace
 

@@ -84,6 +84,9 @@ struct DecodeParams {
     // 1: the previous kernel of the stream does not write this cache, so lengths and tiles
     // may be read before the programmatic-launch wait (set by the host, see kvq_api.cu)
     int early;
+    // 1: the whole grid is resident at once (one wave), so the last CTAs of a row group may
+    // wait for the others and share the merge of its splits (set at launch)
+    int wide;
 };
 
 struct AppendParams {
