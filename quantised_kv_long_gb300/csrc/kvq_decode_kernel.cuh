@@ -389,7 +389,9 @@ struct Cfg {
     static constexpr int VS = scale_tile_bytes(VT) * NS;
     static constexpr int TILE = KC + VC + KS + VS;
     static constexpr int MIN_CTAS = 1;         // one CTA per SM: up to 11 consumer warps + 1 producer
-    static constexpr int RING_BUDGET = 196608;
+    // 256-wide heads: 204 KB, so that three stages of eight q8_0 tiles fit beside the score
+    // exchange (more bytes in flight per SM)
+    static constexpr int RING_BUDGET = NS == 2 ? 208896 : 196608;
     // tiles each warp takes per stage: two (32 keys share one softmax step) when the ring
     // still holds at least two stages, else one
     static constexpr int TPW = (2 * 2 * TW * TILE <= RING_BUDGET) ? 2 : 1;
@@ -398,10 +400,9 @@ struct Cfg {
     static constexpr int STAGES_RAW = RING_BUDGET / STAGE;
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 16 ? 16 : STAGES_RAW);
     static constexpr int RING = STAGES * STAGE;
-    // score exchange of the two slice-warps of each tile pair (double-buffered), then one
-    // guard flag per warp and buffer
-    static constexpr int XCHG_SC = NS == 2 ? TW * 2 * 2 * 32 * 16 * TPW : 0;
-    static constexpr int XCHG = NS == 2 ? XCHG_SC + (TW * 2 * 2 * 4 + 15) / 16 * 16 : 0;
+    // score exchange of the two slice-warps of each tile pair, then one guard flag per warp
+    static constexpr int XCHG_SC = NS == 2 ? TW * 2 * 32 * 16 * TPW : 0;
+    static constexpr int XCHG = NS == 2 ? XCHG_SC + (TW * 2 * 4 + 15) / 16 * 16 : 0;
     static constexpr int BAR_OFF = RING + XCHG;
     // per slice: the K code-offset corrections of its 8 rows x 4 blocks, and the Q
     // fragments (8 chunks x 32 lanes x 16 B) that every tile-warp of the slice reads
@@ -936,7 +937,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                     // the two slice-warps of this tile pair add their partial scores, and agree
                     // on the guard (each saw the V scales of its own slice only): their running
                     // maxima must move together, as the merge keeps one per tile pair
-                    const int xi = (tw * 2 + (k & 1)) * 2;
+                    const int xi = tw * 2;
 #pragma unroll
                     for (int t = 0; t < TPW; ++t) {
                         float4 *mine = xchg + ((xi + sl) * TPW + t) * 32;
@@ -953,6 +954,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
                         sc[t][2] += os.z;
                         sc[t][3] += os.w;
                     }
+                    asm volatile("bar.sync %0, 64;\n" ::"r"(1 + tw) : "memory");  // the buffer is free again
                 }
                 // rows past the length, and a second tile past this split's range (it belongs
                 // to the next split and was not loaded), are masked out
