@@ -389,16 +389,19 @@ struct Cfg {
     static constexpr int VS = scale_tile_bytes(VT) * NS;
     static constexpr int TILE = KC + VC + KS + VS;
     static constexpr int MIN_CTAS = 1;         // one CTA per SM: up to 11 consumer warps + 1 producer
-    // 256-wide heads: 204 KB, so that three stages of eight q8_0 tiles fit beside the score
-    // exchange (more bytes in flight per SM)
-    static constexpr int RING_BUDGET = NS == 2 ? 208896 : 196608;
+    // ring budget: 204 KB for 256-wide heads, so that three stages of eight q8_0 tiles fit
+    // beside the score exchange; 220 KB for 128-wide heads, so that q8_0/q4_0 gets a third
+    // stage (more bytes in flight per SM)
+    static constexpr int RING_BUDGET = NS == 2 ? 208896 : 225280;
     // tiles each warp takes per stage: two (32 keys share one softmax step) when the ring
     // still holds at least two stages, else one
     static constexpr int TPW = (2 * 2 * TW * TILE <= RING_BUDGET) ? 2 : 1;
     static constexpr int TWT = TW * TPW;       // tiles per stage
     static constexpr int STAGE = TWT * TILE;
     static constexpr int STAGES_RAW = RING_BUDGET / STAGE;
-    static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 16 ? 16 : STAGES_RAW);
+    // 128-wide heads: at most three stages (a fourth, for 4-bit pairs, measured slower)
+    static constexpr int STAGES_MAX = NS == 1 ? 3 : 16;
+    static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > STAGES_MAX ? STAGES_MAX : STAGES_RAW);
     static constexpr int RING = STAGES * STAGE;
     // score exchange of the two slice-warps of each tile pair, then one guard flag per warp
     static constexpr int XCHG_SC = NS == 2 ? TW * 2 * 32 * 16 * TPW : 0;
