@@ -78,6 +78,11 @@ cudaError_t launch_append_t(const AppendParams &p, cudaStream_t stream) {
 template <int TK, int TV>
 __global__ void __launch_bounds__(256) window_append_kernel(const WindowParams p) {
     __shared__ int s_last;
+    // Programmatic dependent launch: everything below reads what the previous kernel of the
+    // stream may write, so wait for it first; the next kernel (the window's decode) may then
+    // start its own pre-wait part, which reads nothing this kernel writes.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int wg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int NS = p.D / kSlice;
@@ -137,8 +142,16 @@ template <int TK, int TV>
 cudaError_t launch_window_t(const WindowParams &p, cudaStream_t stream) {
     const int warps_per_block = 8;
     const int blocks = (p.total_warps + warps_per_block - 1) / warps_per_block;
-    window_append_kernel<TK, TV><<<blocks, 32 * warps_per_block, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(32 * warps_per_block);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, window_append_kernel<TK, TV>, p);
 }
 
 }  // namespace
