@@ -150,13 +150,14 @@ bool g_track_lost = false;
 // (nullptr: none) and writes caches `w0`, `w1` (nullptr: none).  Returns whether the
 // reads may start before the previous kernel of the stream completes.
 bool track_launch(cudaStream_t stream, const kvq_cache *reads, const kvq_cache *w0,
-                  const kvq_cache *w1 = nullptr) {
+                  const kvq_cache *w1 = nullptr, const kvq_cache *reads2 = nullptr) {
     std::lock_guard<std::mutex> lock(g_track_mu);
     int i = 0;
     while (i < g_track_n && g_track[i].stream != stream) ++i;
     bool early;
     if (i < g_track_n) {
-        early = g_track[i].wrote[0] != reads && g_track[i].wrote[1] != reads;
+        early = g_track[i].wrote[0] != reads && g_track[i].wrote[1] != reads &&
+                (!reads2 || (g_track[i].wrote[0] != reads2 && g_track[i].wrote[1] != reads2));
     } else {
         early = !g_track_lost;
         if (g_track_n < kTrackSlots) {
@@ -595,14 +596,42 @@ static kvq_status window_splits(const kvq_cache *window, const kvq_cache *tail, 
     return KVQ_OK;
 }
 
+// One launch over both regions (256-wide heads): the tail's automatic split count S is
+// shared between the regions in proportion to their capacity bytes, at least one each.
+static bool dual_splits(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads, int *nw, int *S) {
+    if (window->desc.head_dim != 2 * kvq::kSlice) return false;
+    int s = 0;
+    if (auto_splits(tail, n_q_heads, &s) != 0 || s < 2) return false;
+    auto row_bytes = [](const kvq_cache *c) {
+        const int NS = c->desc.head_dim / kvq::kSlice;
+        return static_cast<double>(NS) *
+               (kvq::code_tile_bytes(c->desc.type_k) + kvq::code_tile_bytes(c->desc.type_v) +
+                kvq::scale_tile_bytes(c->desc.type_k) + kvq::scale_tile_bytes(c->desc.type_v)) /
+               kvq::kTileRows;
+    };
+    const double bw = row_bytes(window) * window->desc.capacity, bt = row_bytes(tail) * tail->desc.capacity;
+    int w = static_cast<int>(s * bw / (bw + bt) + 0.5);
+    w = w < 1 ? 1 : (w > s - 1 ? s - 1 : w);
+    *nw = w;
+    *S = s;
+    return true;
+}
+
 // Workspace of a window + tail decode: one decode workspace, used by the window's decode
-// and then by the tail's (each leaves its counters at zero), and the window's result.
+// and then by the tail's (each leaves its counters at zero), and the window's result; or,
+// for the one-launch form, one decode workspace over the splits of both regions.
 static size_t window_ws(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads, int sw, int stl,
                         size_t *res_off) {
     const size_t wsz = ws_layout(window, n_q_heads, sw).total, tsz = ws_layout(tail, n_q_heads, stl).total;
     const size_t rows = static_cast<size_t>(window->desc.batch) * n_q_heads;
     *res_off = align256(wsz > tsz ? wsz : tsz);
-    return *res_off + align256(rows * window->desc.head_dim * 4) + align256(rows * 4);
+    size_t total = *res_off + align256(rows * window->desc.head_dim * 4) + align256(rows * 4);
+    int nw = 0, S = 0;
+    if (dual_splits(window, tail, n_q_heads, &nw, &S)) {
+        const size_t d = ws_layout(tail, n_q_heads, S).total;
+        if (d > total) total = d;
+    }
+    return total;
 }
 
 kvq_status kvq_window_workspace_size(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads,
@@ -631,6 +660,33 @@ kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *tail, con
     float *w_out = reinterpret_cast<float *>(ws + res_off);
     float *w_lse = reinterpret_cast<float *>(ws + res_off + align256(rows * window->desc.head_dim * 4));
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int nw = 0, S = 0;
+    if (dual_splits(window, tail, n_q_heads, &nw, &S)) {
+        // one launch: splits [0, nw) over the window, [nw, S) over the tail, one merge
+        const WsLayout w = ws_layout(tail, n_q_heads, S);
+        kvq::DecodeParams pr[2] = {base_params(window, q, n_q_heads, scale, nw),
+                                   base_params(tail, q, n_q_heads, scale, S - nw)};
+        for (int r = 0; r < 2; ++r) {
+            kvq::DecodeParams &p = pr[r];
+            p.out = out;
+            p.lse = lse;
+            p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+            p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
+            p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
+            p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
+            p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
+            p.n_groups_max = w.n_groups_max;
+            p.part_m = reinterpret_cast<float *>(ws + w.part_m);
+            p.part_l = reinterpret_cast<float *>(ws + w.part_l);
+            p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+            p.part_stride = S;
+            p.part_base = r == 0 ? 0 : nw;
+            p.merge_slots = S;
+        }
+        pr[0].early = pr[1].early = track_launch(cs, window, nullptr, nullptr, tail) ? 1 : 0;
+        return cuda_status(kvq::launch_window_dual(tail->desc.type_k, tail->desc.type_v, window->desc.head_dim, pr[0],
+                                                   pr[1], nw, cs));
+    }
     // each region in its own typed decode (the window's first, into the workspace); the
     // tail's final merge takes the window's result as one more triple
     const kvq_cache *region[2] = {window, tail};

@@ -677,8 +677,71 @@ __device__ __noinline__ void prefetch_split(const DecodeParams &p, int bseq, int
     if constexpr (C::VS > 0) pf(p.v_scales + bt * C::VS, static_cast<size_t>(nt) * C::VS);
 }
 
+// ---------------- merge of the split triples of one (sequence, KV head, row group) ----------------
+// Called by every CTA of the row group once it has written its triple at slot `slot` of
+// the NP slots (row r, slot s at r * part_stride + s).  Small sets: the last CTA to arrive
+// merges them all.  Larger sets in a grid that is resident at once: the last P arrivals
+// share the merge by columns.  Otherwise slots form groups of ceil(sqrt(NP)); the last
+// arrival of each group merges its group into a group triple while other CTAs still run,
+// and the last group merges the group triples.
+__device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int slot, int rows, int D, size_t row0,
+                                            size_t unit, const RowMap &rmap, int &s_flag, uint8_t *smem) {
+    const long long tbytes = static_cast<long long>(NP) * rows * (D + 2) * 4;
+    if (p.wide && tbytes > kWideMinBytes) {
+        // the last P arrivals each merge a range of columns once every split has arrived;
+        // their second arrivals count P more, and the last of those clears the counter
+        const int C = rows * (D / 4);
+        const int P = max(1, min(min(NP, C), static_cast<int>((tbytes + kWideBytes - 1) / kWideBytes)));
+        int32_t *cnt = p.counters + unit;
+        __threadfence();  // each thread publishes its own writes
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int t = atomicAdd(cnt, 1);
+            int role = t >= NP - P ? t - (NP - P) : -1;  // merger index, or -1
+            if (role >= 0 && t != NP - 1 && !wait_count(cnt, NP)) {
+                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
+                role = -2;  // a merger that gave up: no merge, but its second arrival counts
+            }
+            s_flag = role;
+        }
+        __syncthreads();
+        const int role = s_flag;
+        if (role == -1) return;
+        if (role >= 0) {
+            __threadfence();
+            merge_cols(p.part_o, p.part_m, p.part_l, p.part_stride, NP, row0, D, role * C / P, (role + 1) * C / P,
+                       p.out, p.lse, rmap, p.ext_out, p.ext_lse, smem);
+            __syncthreads();
+        }
+        if (threadIdx.x == 0 && atomicAdd(cnt, 1) == NP + P - 1) atomicExch(cnt, 0);
+        return;
+    }
+    if (tbytes <= kDirectMergeBytes) {
+        if (!arrive_last(p.counters + unit, NP, s_flag)) return;
+        merge_rows(p.part_o, p.part_m, p.part_l, p.part_stride, 0, NP, row0, rows, D, p.out, p.lse, nullptr, nullptr,
+                   nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
+        if (threadIdx.x == 0) p.counters[unit] = 0;
+        return;
+    }
+    const int gs = group_size(NP);
+    const int n_groups = (NP + gs - 1) / gs;
+    const int grp = slot / gs;
+    const int gsize = min(gs, NP - grp * gs);
+    int32_t *cnt1 = p.counters1 + unit * p.n_groups_max + grp;
+    if (!arrive_last(cnt1, gsize, s_flag)) return;
+    merge_rows(p.part_o, p.part_m, p.part_l, p.part_stride, grp * gs, gsize, row0, rows, D, nullptr, nullptr, p.grp_o,
+               p.grp_m, p.grp_l, p.n_groups_max, grp);
+    if (threadIdx.x == 0) *cnt1 = 0;
+    if (!arrive_last(p.counters + unit, n_groups, s_flag)) return;
+    merge_rows(p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, 0, n_groups, row0, rows, D, p.out, p.lse, nullptr,
+               nullptr, nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
+    if (threadIdx.x == 0) p.counters[unit] = 0;
+}
+
+// The decode of one CTA: split `split` of this launch's cache (blockIdx.y = KV head,
+// blockIdx.z = sequence x row group).
 template <int KT, int VT, int NS, bool MQ>
-__global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
+__device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split) {
     using C = Cfg<KT, VT, NS>;
     constexpr int TPW = C::TPW;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -686,7 +749,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     __shared__ int s_timeout;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, h = blockIdx.y;
+    const int h = blockIdx.y;
     const int bseq = blockIdx.z / p.QG, qg = blockIdx.z % p.QG;
     const int cap_rows = p.cap_tiles * kTileRows;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
@@ -728,7 +791,9 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     const size_t prow0 = (static_cast<size_t>(bseq) * p.Hkv + h) * unit_rows + r0;  // its triple row
     const RowMap rmap{n_q, p.G, p.Hq, p.Hkv};
 
-    if (split >= ns) {
+    // A split beyond ns has no tiles.  Alone it publishes nothing; as a region of a larger
+    // merge it runs on with an empty range (t_begin = t_end = T) and publishes an empty triple.
+    if (split >= ns && p.merge_slots == 0) {
         if (early) grid_dep_wait();
         grid_dep_launch();
         if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
@@ -1111,7 +1176,7 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     }
     __syncthreads();
     const bool timed_out = s_timeout != 0;
-    const bool single = (ns == 1) && fused;
+    const bool single = (ns == 1) && fused && p.merge_slots == 0;
     for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
         const int g = idx / (D / 4), dq = idx % (D / 4);
         float M = -CUDART_INF_F;
@@ -1161,62 +1226,26 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     }
     if (!fused || single || timed_out) return;
 
-    // ---------------- merge of the splits of this (sequence, KV head, row group) ----------------
-    // Small sets of split triples: the last CTA to arrive merges them all.  Otherwise splits
-    // form groups of ceil(sqrt(ns)); the last arrival of each group merges its group into a
-    // group triple while other CTAs still run, and the last group merges the group triples.
     const size_t unit = (static_cast<size_t>(bseq) * p.Hkv + h) * p.QG + qg;
-    const size_t row0 = prow0;
-    const long long tbytes = static_cast<long long>(ns) * rows * (D + 2) * 4;
-    if (p.wide && tbytes > kWideMinBytes) {
-        // the last P arrivals each merge a range of columns once every split has arrived;
-        // their second arrivals count P more, and the last of those clears the counter
-        const int C = rows * (D / 4);
-        const int P = max(1, min(min(ns, C), static_cast<int>((tbytes + kWideBytes - 1) / kWideBytes)));
-        int32_t *cnt = p.counters + unit;
-        __threadfence();  // each thread publishes its own writes
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const int t = atomicAdd(cnt, 1);
-            int role = t >= ns - P ? t - (ns - P) : -1;  // merger index, or -1
-            if (role >= 0 && t != ns - 1 && !wait_count(cnt, ns)) {
-                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
-                role = -2;  // a merger that gave up: no merge, but its second arrival counts
-            }
-            s_flag = role;
-        }
-        __syncthreads();
-        const int role = s_flag;
-        if (role == -1) return;
-        if (role >= 0) {
-            __threadfence();
-            merge_cols(p.part_o, p.part_m, p.part_l, p.n_splits, ns, row0, D, role * C / P, (role + 1) * C / P,
-                       p.out, p.lse, rmap, p.ext_out, p.ext_lse, smem);
-            __syncthreads();
-        }
-        if (threadIdx.x == 0 && atomicAdd(cnt, 1) == ns + P - 1) atomicExch(cnt, 0);
-        return;
-    }
-    if (tbytes <= kDirectMergeBytes) {
-        if (!arrive_last(p.counters + unit, ns, s_flag)) return;
-        merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, 0, ns, row0, rows, D, p.out, p.lse, nullptr, nullptr,
-                   nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
-        if (threadIdx.x == 0) p.counters[unit] = 0;
-        return;
-    }
-    const int gs = group_size(ns);
-    const int n_groups = (ns + gs - 1) / gs;
-    const int grp = split / gs;
-    const int gsize = min(gs, ns - grp * gs);
-    int32_t *cnt1 = p.counters1 + unit * p.n_groups_max + grp;
-    if (!arrive_last(cnt1, gsize, s_flag)) return;
-    merge_rows(p.part_o, p.part_m, p.part_l, p.n_splits, grp * gs, gsize, row0, rows, D, nullptr, nullptr, p.grp_o,
-               p.grp_m, p.grp_l, p.n_groups_max, grp);
-    if (threadIdx.x == 0) *cnt1 = 0;
-    if (!arrive_last(p.counters + unit, n_groups, s_flag)) return;
-    merge_rows(p.grp_o, p.grp_m, p.grp_l, p.n_groups_max, 0, n_groups, row0, rows, D, p.out, p.lse, nullptr,
-               nullptr, nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
-    if (threadIdx.x == 0) p.counters[unit] = 0;
+    split_merge(p, p.merge_slots ? p.merge_slots : ns, p.part_base + split, rows, D, prow0, unit, rmap, s_flag, smem);
+}
+
+template <int KT, int VT, int NS, bool MQ>
+__global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
+    decode_body<KT, VT, NS, MQ>(p, fused, blockIdx.x);
+}
+
+// One launch over an f16 window and a quantised tail of the same sequences: splits
+// [0, nw) decode the window, the rest the tail; both regions publish their triples into
+// one set of merge slots (merge_slots = all splits of the grid), merged exactly as one.
+template <int KT, int VT, int NS>
+__global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS)
+    dual_kernel(const DecodeParams pw, const DecodeParams pt, const int nw) {
+    static_assert(Cfg<KVQ_F16, KVQ_F16, NS>::THREADS == Cfg<KT, VT, NS>::THREADS, "one block size for both regions");
+    if (static_cast<int>(blockIdx.x) < nw)
+        decode_body<KVQ_F16, KVQ_F16, NS, false>(pw, 1, blockIdx.x);
+    else
+        decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw);
 }
 
 constexpr int kMaxDevices = 64;
@@ -1295,6 +1324,44 @@ cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stre
     return cudaLaunchKernelEx(&cfg, decode_kernel<KT, VT, NS, MQ>, q, fused ? 1 : 0);
 }
 
+
+template <int KT, int VT, int NS>
+cudaError_t launch_dual_t(const DecodeParams &pw, const DecodeParams &pt, int nw, cudaStream_t stream) {
+    using C = Cfg<KT, VT, NS>;
+    constexpr int kSmem = Cfg<KVQ_F16, KVQ_F16, NS>::SMEM > C::SMEM ? Cfg<KVQ_F16, KVQ_F16, NS>::SMEM : C::SMEM;
+    static bool configured[kMaxDevices] = {};
+    static int occ_cached[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(dual_kernel<KT, VT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dual_kernel<KT, VT, NS>, C::THREADS, kSmem);
+        if (e != cudaSuccess) return e;
+        occ_cached[dev] = n > 0 ? n : 1;
+        configured[dev] = true;
+    }
+    int sms = 0;
+    e = sm_count(dev, &sms);
+    if (e != cudaSuccess) return e;
+    DecodeParams a = pw, b = pt;
+    const long long ctas = static_cast<long long>(pt.merge_slots) * pt.Hkv * pt.B * pt.QG;
+    a.wide = b.wide = ctas <= static_cast<long long>(occ_cached[dev]) * sms ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pt.merge_slots, pt.Hkv, pt.B * pt.QG);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dual_kernel<KT, VT, NS>, a, b, nw);
+}
 
 }  // namespace
 

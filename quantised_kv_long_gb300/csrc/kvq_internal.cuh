@@ -87,6 +87,10 @@ struct DecodeParams {
     // 1: the whole grid is resident at once (one wave), so the last CTAs of a row group may
     // wait for the others and share the merge of its splits (set at launch)
     int wide;
+    // 0: the merge covers this launch's splits.  > 0: this launch is one region of a grid
+    // whose merge_slots splits all publish a triple (empty ones too) at part_base + split of
+    // part_stride slots per row, merged as one set.
+    int merge_slots;
 };
 
 struct AppendParams {
@@ -420,6 +424,10 @@ cudaError_t launch_append(int type_k, int type_v, const AppendParams &p, cudaStr
 cudaError_t launch_window_append(int tail_k, int tail_v, const WindowParams &p, cudaStream_t stream);
 cudaError_t launch_verify(int type_k, int type_v, const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_ext(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream);
+// one launch over an f16 window (params pw, splits [0, nw)) and a quantised tail (pt, the
+// remaining pt.merge_slots - nw splits); cudaErrorNotSupported where it is not built
+cudaError_t launch_window_dual(int tail_k, int tail_v, int D, const DecodeParams &pw, const DecodeParams &pt, int nw,
+                               cudaStream_t stream);
 cudaError_t occupancy_ext(int type_k, int type_v, int D, int *ctas_per_sm);
 // the (K, V) type pairs a cache may hold: every pair of f16 / q8_0 / q4_0, plus these
 __host__ __device__ constexpr bool is_base_type(int t) { return t == KVQ_F16 || t == KVQ_Q8_0 || t == KVQ_Q4_0; }

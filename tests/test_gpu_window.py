@@ -5,7 +5,9 @@ front of a quantised tail ("HAL #582 -- per-layer KV compression study", section
   oracle quantising the same token's f16 value; the window holds the f16 values of the
   last W tokens, each in ring slot t mod W.
 * Read path: decode over both regions matches the oracle's two-region result (split
-  triples of each region, merged by the oracle's exact combine) within 1e-3.
+  triples of each region, merged by the oracle's exact combine) within 1e-3; 256-wide heads
+  take the one-launch form (both regions' splits in one grid and one merge), 128-wide heads
+  two launches.
 """
 import numpy as np
 import pytest
@@ -50,7 +52,8 @@ def reference(tk, tv, Xk, Xv, n, W, q, scale):
     return oracle.combine(np.concatenate([ow, ot], 1), np.concatenate([mw, mt], 1), np.concatenate([lw, lt], 1))
 
 
-@pytest.mark.parametrize("tk,tv,D,G", [("q8_0", "q4_0", 128, 5), ("q8_0", "q8_0", 256, 8), ("q4_0", "q4_0", 128, 4)])
+@pytest.mark.parametrize("tk,tv,D,G", [("q8_0", "q4_0", 128, 5), ("q8_0", "q8_0", 256, 8), ("q4_0", "q4_0", 128, 4),
+                                    ("q4_0", "q8_0", 256, 2), ("f16", "q4_0", 256, 5)])
 def test_window_evicts_bit_exact_and_decodes(kvq, tk, tv, D, G):
     B, H, W, N = 2, 2, 32, 90
     wl = syn.Workload("window", 1, B, H * G, H, D, tk, tv, (N, N), seed=40 + D + G)
