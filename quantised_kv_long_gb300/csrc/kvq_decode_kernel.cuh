@@ -311,16 +311,22 @@ __device__ void merge_cols(const float *po, const float *pm, const float *pl, in
             }
             __syncthreads();
             if (v && k == 0) {
-                for (int k2 = 1; k2 < sg; ++k2) {
-                    const float m2 = rM[k2 * ncol + ci];
-                    const float Mn = fmaxf(M, m2);
-                    if (Mn == -CUDART_INF_F) continue;
-                    const float a = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
-                    const float b = m2 == -CUDART_INF_F ? 0.f : expf(m2 - Mn);
-                    const float4 x = rA[k2 * ncol + ci];
-                    A = make_float4(fmaf(b, x.x, a * A.x), fmaf(b, x.y, a * A.y), fmaf(b, x.z, a * A.z), fmaf(b, x.w, a * A.w));
-                    L = fmaf(b, rL[k2 * ncol + ci], a * L);
-                    M = Mn;
+                // the maximum over the sg partial triples first, then independent weights
+                float Mx = M;
+                for (int k2 = 1; k2 < sg; ++k2) Mx = fmaxf(Mx, rM[k2 * ncol + ci]);
+                if (Mx != -CUDART_INF_F) {
+                    const float a = M == -CUDART_INF_F ? 0.f : expf(M - Mx);
+                    A = make_float4(a * A.x, a * A.y, a * A.z, a * A.w);
+                    L *= a;
+#pragma unroll 4
+                    for (int k2 = 1; k2 < sg; ++k2) {
+                        const float m2 = rM[k2 * ncol + ci];
+                        const float b = m2 == -CUDART_INF_F ? 0.f : expf(m2 - Mx);
+                        const float4 x = rA[k2 * ncol + ci];
+                        A = make_float4(fmaf(b, x.x, A.x), fmaf(b, x.y, A.y), fmaf(b, x.z, A.z), fmaf(b, x.w, A.w));
+                        L = fmaf(b, rL[k2 * ncol + ci], L);
+                    }
+                    M = Mx;
                 }
             }
             __syncthreads();
