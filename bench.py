@@ -169,12 +169,24 @@ class Cell:
                     del K, V
                 self.caches.append(c)
             L, B = wl.layers, wl.batch
-            self.q = torch.stack([syn.queries(wl, layer) for layer in range(L)]).contiguous()
+            q = torch.stack([syn.queries(wl, layer) for layer in range(L)])
             news = [syn.new_rows(wl, layer, 0) for layer in range(L)]
-            self.knew = torch.stack([k for k, _ in news]).contiguous()
-            self.vnew = torch.stack([v for _, v in news]).contiguous()
-            self.out = torch.empty_like(self.q)
-            self.lse = torch.empty((L, B, wl.n_q_heads), device=dev, dtype=torch.float32)
+            knew = torch.stack([k for k, _ in news])
+            vnew = torch.stack([v for _, v in news])
+            # a step's inputs (q, new K, new V) and results (out, lse) each in one flat buffer,
+            # so that a host round trip is one copy in and one copy out
+            nq, nk, nv = q.numel(), knew.numel(), vnew.numel()
+            self.inputs = torch.empty(nq + nk + nv, device=dev, dtype=torch.float32)
+            self.q = self.inputs[:nq].view(q.shape)
+            self.knew = self.inputs[nq:nq + nk].view(knew.shape)
+            self.vnew = self.inputs[nq + nk:].view(vnew.shape)
+            self.q.copy_(q)
+            self.knew.copy_(knew)
+            self.vnew.copy_(vnew)
+            del q, knew, vnew, news
+            self.results = torch.empty(nq + L * B * wl.n_q_heads, device=dev, dtype=torch.float32)
+            self.out = self.results[:nq].view(self.q.shape)
+            self.lse = self.results[nq:].view(L, B, wl.n_q_heads)
             self.splits = self.caches[0].auto_splits(wl.n_q_heads)
             self.ws = self.caches[0].workspace(wl.n_q_heads, self.splits)  # layers run in order: one workspace
         torch.cuda.synchronize()
@@ -286,23 +298,15 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
                                   "steps (event nodes serialise launches; the step time comes from the event-free pass)")
     if e2e:
         pin = dict(pin_memory=True)
-        q_h = torch.empty(cell.q.shape, dtype=torch.float32, **pin)
-        kn_h = torch.empty(cell.knew.shape, dtype=torch.float32, **pin)
-        vn_h = torch.empty(cell.vnew.shape, dtype=torch.float32, **pin)
-        out_h = torch.empty(cell.out.shape, dtype=torch.float32, **pin)
-        lse_h = torch.empty(cell.lse.shape, dtype=torch.float32, **pin)
-        q_h.copy_(cell.q)
-        kn_h.copy_(cell.knew)
-        vn_h.copy_(cell.vnew)
+        in_h = torch.empty(cell.inputs.shape, dtype=torch.float32, **pin)  # q, new K, new V
+        res_h = torch.empty(cell.results.shape, dtype=torch.float32, **pin)  # out, lse
+        in_h.copy_(cell.inputs)
         torch.cuda.synchronize()
 
         def e2e_step():
-            cell.q.copy_(q_h, non_blocking=True)
-            cell.knew.copy_(kn_h, non_blocking=True)
-            cell.vnew.copy_(vn_h, non_blocking=True)
+            cell.inputs.copy_(in_h, non_blocking=True)
             g_plain.replay()
-            out_h.copy_(cell.out, non_blocking=True)
-            lse_h.copy_(cell.lse, non_blocking=True)
+            res_h.copy_(cell.results, non_blocking=True)
 
         with torch.cuda.stream(stream):
             for _ in range(warmup):
@@ -319,11 +323,11 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
         cell.executed(steps)
         ms_e = f0.elapsed_time(f1) / steps
         b_e = step_kv_bytes(wl, [x + (steps + 1) / 2.0 for x in lens_e])
-        h2d = (q_h.numel() + kn_h.numel() + vn_h.numel()) * 4
-        d2h = (out_h.numel() + lse_h.numel()) * 4
+        h2d = in_h.numel() * 4
+        d2h = res_h.numel() * 4
         res["e2e"] = {"value": b_e / (ms_e * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "ms_per_step": ms_e,
-                      "how": "pinned-host inputs copied in, graph step, outputs copied out, every step"}
+                      "how": "pinned-host inputs (q, new K, new V) copied in, graph step, outputs (out, lse) copied out, every step: one copy each way"}
     for c in cell.caches:
         if c.read_error() != 0:
             res["device_error"] = True
