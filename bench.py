@@ -583,6 +583,21 @@ def traffic_from_profiles(wl):
         return None
 
 
+def max_over_ranks(dist, value, device):
+    """The largest per-rank value (a step time): the whole job is as slow as its slowest rank.
+    Every rank gets the result."""
+    import torch
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, bytes_per_rank_step, ms_per_step):
+    """Whole-job KV-read GB/s: each of the `world` replicas reads its own bytes every step,
+    and a step lasts the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -661,9 +676,7 @@ def main():
     torch.cuda.synchronize()
     ms = head["ms_per_step"]
     if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(dist, ms, "cuda")
         dist.barrier()
     wall0, wall1 = head.pop("_wall")
     clocks = sampler.summary(wall0, wall1)
@@ -692,7 +705,7 @@ def main():
 
     if rank != 0:
         return 0
-    value = world * step_kv_bytes(wl, [wl.lengths[0]]) / (ms * 1e-3) / 1e9 if world > 1 else head["kv_gbs"]
+    value = job_value(world, step_kv_bytes(wl, [wl.lengths[0]]), ms) if world > 1 else head["kv_gbs"]
     achieved = head.get("decode_gbs")
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": (achieved / peak) if achieved else None, "traffic": traffic_from_profiles(wl),
