@@ -9,11 +9,13 @@
 // (section 3b, finding 2) gives for a quantised reader that was kernel-bound: throughput
 // has to follow the bytes moved.
 //
-// GB300 mapping (one CTA per (split, KV head, sequence x row-group)):
+// GB300 mapping (one CTA per (split, KV head, sequence x row-group), one CTA per SM):
 //   * warp 0 (producer): 1-D bulk copies (cp.async.bulk, TMA engine) of a run of whole
-//     16-row tiles per stage into a shared-memory ring; completion on mbarriers; every
-//     wait is bounded and reports KVQ_DEVERR_TIMEOUT instead of hanging.
-//   * consumer warps: each owns one tile (and one 128-value slice) per stage.  Tiles are
+//     16-row tiles per stage into a shared-memory ring of two or three stages; completion
+//     on mbarriers; every wait is bounded and reports KVQ_DEVERR_TIMEOUT instead of hanging.
+//   * consumer warps (11 tile-warps for 128-wide heads with quantised keys, 8 for f16
+//     keys, 4 slice-warp pairs for 256-wide heads): each owns two tiles (and one 128-value
+//     slice) per stage.  Tiles are
 //     stored fragment-native (include/kvq.h), so every lane fetches its mma operands
 //     with 16-byte shared loads, converts codes to exact f16 integers with bit tricks
 //     (no I2F), and runs mma.sync m16n8k16 (f16 in, fp32 accumulate).
@@ -24,8 +26,11 @@
 //     O += P V: the S accumulator layout is the A layout of the next mma, so P never
 //     leaves registers; the V scale of each (row, block) is folded into P, which is
 //     again split into f16 hi + lo rows.
-//   * the CTA merges its warps in shared memory, writes one split triple, and the last
-//     CTA of each (sequence, KV head, row-group) merges all splits (arrival counter).
+//   * the CTA merges its warps in shared memory and writes one split triple; the splits
+//     of each (sequence, KV head, row-group) are merged after an arrival counter: by the
+//     last CTA, by the last few CTAs column by column when the grid is resident at once,
+//     or in two levels (split_merge).  dual_kernel runs an f16 window and a quantised
+//     tail of the same sequences in one grid and one merge.
 #pragma once
 #include <math_constants.h>
 
