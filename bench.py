@@ -341,7 +341,7 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
 def run_window_cell(kvq, torch, wl, window, steps, warmup, peak):
     """Position-axis mixed cache (f16 window of the last `window` tokens + quantised tail):
     one step = for every layer, kvq_window_append (1 row, evicting the oldest window row
-    into the tail) + kvq_window_decode (window and tail decodes + exact merge); the layers
+    into the tail) + kvq_window_decode (both regions in one launch, exact merge); the layers
     of a step form one CUDA graph."""
     stream = torch.cuda.Stream()
     L, B = wl.layers, wl.batch
@@ -397,12 +397,14 @@ def run_window_cell(kvq, torch, wl, window, steps, warmup, peak):
     n_tail = ctx - window + 1 + warmup + steps / 2.0  # mean tail length over the timed steps
     bytes_step = L * B * H * D * (window * 4.0 + n_tail * (bpv[wl.type_k] + bpv[wl.type_v]))
     err = any(c.window.read_error() or c.tail.read_error() for c in caches)
-    res = {"workload": f"hybrid-{L}L-window{window}-f16+{wl.type_k}-{wl.type_v}-ctx{ctx}", "layers": L, "batch": B,
+    family = wl.name.split("-")[0]
+    res = {"workload": f"{family}-{L}L-window{window}-f16+{wl.type_k}-{wl.type_v}-ctx{ctx}", "layers": L, "batch": B,
            "n_q_heads": wl.n_q_heads, "n_kv_heads": H, "head_dim": D, "kv": f"f16 window + {wl.type_k}/{wl.type_v} tail",
            "ctx": ctx, "window": window, "steps_per_s": 1000.0 / ms, "ms_per_step": ms,
            "kv_gbs": bytes_step / (ms * 1e-3) / 1e9, "kv_bytes_per_step": bytes_step,
            "pct_hbm_peak": 100.0 * bytes_step / (ms * 1e-3) / 1e9 / peak,
-           "step": "per layer: window append (evict oldest into tail) + window decode + tail decode + merge"}
+           "step": "per layer: window append (evict oldest into tail) + one decode over both regions "
+                   "(window and tail splits in one grid, one exact merge)"}
     if err:
         res["device_error"] = True
     del g
@@ -688,6 +690,8 @@ def main():
             r.pop("_wall")
             sweep.append(r)
         sweep.append(run_window_cell(kvq, torch, syn.hybrid(65536, "q8_0", "q8_0"), 4096, args.sweep_steps,
+                                     max(3, min(args.warmup, 5)), peak))
+        sweep.append(run_window_cell(kvq, torch, syn.dense14b(131072, "q8_0", "q4_0"), 4096, args.sweep_steps,
                                      max(3, min(args.warmup, 5)), peak))
         for n_q in (4, 16):
             sweep.append(run_verify_cell(kvq, torch, syn.hybrid(65536, "q8_0", "q8_0"), n_q, args.sweep_steps,

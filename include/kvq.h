@@ -303,11 +303,11 @@ KVQ_API kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int
  * kvq_window_decode: decode attention of q [B][Hq][D] over the union of both regions
  * (window_len + tail_len rows per sequence), written like kvq_decode_attention.  Each
  * region is read by its own typed decode (the read path of section 5 P2) and the output is
- * the exact merge of both regions.  For head_dim 256 this is one launch: its first splits
- * read the window, the rest the tail (the split count shared in proportion to the regions'
- * capacity bytes), and all split triples are merged as one set.  Otherwise two launches:
- * the window's decode writes its normalised result into `workspace`, and the tail's final
- * merge takes that result as one more split triple.  `workspace`:
+ * the exact merge of both regions.  Normally one launch: its first splits read the window,
+ * the rest the tail (the split count shared in proportion to the regions' capacity bytes),
+ * and all split triples are merged as one set.  Where the tail's split count is below two,
+ * two launches: the window's decode writes its normalised result into `workspace`, and the
+ * tail's final merge takes that result as one more split triple.  `workspace`:
  * kvq_window_workspace_size bytes, zeroed once before its first use (as for
  * kvq_decode_attention).
  */

@@ -596,10 +596,10 @@ static kvq_status window_splits(const kvq_cache *window, const kvq_cache *tail, 
     return KVQ_OK;
 }
 
-// One launch over both regions (256-wide heads): the tail's automatic split count S is
-// shared between the regions in proportion to their capacity bytes, at least one each.
+// One launch over both regions: the tail's automatic split count S is shared between the
+// regions in proportion to their capacity bytes, at least one each.
 static bool dual_splits(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads, int *nw, int *S) {
-    if (window->desc.head_dim != 2 * kvq::kSlice) return false;
+    if (window->desc.head_dim != kvq::kSlice && window->desc.head_dim != 2 * kvq::kSlice) return false;
     int s = 0;
     if (auto_splits(tail, n_q_heads, &s) != 0 || s < 2) return false;
     auto row_bytes = [](const kvq_cache *c) {

@@ -387,11 +387,12 @@ __device__ __noinline__ void grid_ticket(const DecodeParams &p, int cap_rows) {
     *p.ticket = 0;
 }
 
-template <int KT, int VT, int NS>
+template <int KT, int VT, int NS, int TW_ = 0>
 struct Cfg {
     // tile-warps per 128-value slice: 11 for 128-wide heads with quantised keys (the
-    // conversion work wants the warps), 8 for f16 keys, 4 pairs for 256-wide heads
-    static constexpr int TW = NS == 2 ? 4 : (KT == KVQ_F16 ? 8 : 11);
+    // conversion work wants the warps), 8 for f16 keys, 4 pairs for 256-wide heads; TW_
+    // overrides (the f16 window body of a two-region launch takes the tail's count)
+    static constexpr int TW = TW_ ? TW_ : (NS == 2 ? 4 : (KT == KVQ_F16 ? 8 : 11));
     static constexpr int CW = TW * NS;         // consumer warps
     static constexpr int THREADS = 32 * (CW + 1);
     static constexpr int KC = code_tile_bytes(KT) * NS;
@@ -751,9 +752,9 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
 
 // The decode of one CTA: split `split` of this launch's cache (blockIdx.y = KV head,
 // blockIdx.z = sequence x row group).
-template <int KT, int VT, int NS, bool MQ>
+template <int KT, int VT, int NS, bool MQ, int TW_ = 0>
 __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split) {
-    using C = Cfg<KT, VT, NS>;
+    using C = Cfg<KT, VT, NS, TW_>;
     constexpr int TPW = C::TPW;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_flag;
@@ -1252,9 +1253,10 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
 template <int KT, int VT, int NS>
 __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS)
     dual_kernel(const DecodeParams pw, const DecodeParams pt, const int nw) {
-    static_assert(Cfg<KVQ_F16, KVQ_F16, NS>::THREADS == Cfg<KT, VT, NS>::THREADS, "one block size for both regions");
+    constexpr int TWW = Cfg<KT, VT, NS>::TW;  // the window body runs with the tail's warp count
+    static_assert(Cfg<KVQ_F16, KVQ_F16, NS, TWW>::THREADS == Cfg<KT, VT, NS>::THREADS, "one block size");
     if (static_cast<int>(blockIdx.x) < nw)
-        decode_body<KVQ_F16, KVQ_F16, NS, false>(pw, 1, blockIdx.x);
+        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x);
     else
         decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw);
 }
@@ -1339,7 +1341,8 @@ cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stre
 template <int KT, int VT, int NS>
 cudaError_t launch_dual_t(const DecodeParams &pw, const DecodeParams &pt, int nw, cudaStream_t stream) {
     using C = Cfg<KT, VT, NS>;
-    constexpr int kSmem = Cfg<KVQ_F16, KVQ_F16, NS>::SMEM > C::SMEM ? Cfg<KVQ_F16, KVQ_F16, NS>::SMEM : C::SMEM;
+    using CW_ = Cfg<KVQ_F16, KVQ_F16, NS, C::TW>;  // the window body's configuration
+    constexpr int kSmem = CW_::SMEM > C::SMEM ? CW_::SMEM : C::SMEM;
     static bool configured[kMaxDevices] = {};
     static int occ_cached[kMaxDevices] = {};
     int dev = 0;

@@ -428,6 +428,8 @@ cudaError_t launch_decode_ext(int type_k, int type_v, const DecodeParams &p, boo
 // remaining pt.merge_slots - nw splits); cudaErrorNotSupported where it is not built
 cudaError_t launch_window_dual(int tail_k, int tail_v, int D, const DecodeParams &pw, const DecodeParams &pt, int nw,
                                cudaStream_t stream);
+cudaError_t launch_window_dual_ns1(int tail_k, int tail_v, const DecodeParams &pw, const DecodeParams &pt, int nw,
+                                   cudaStream_t stream);
 cudaError_t occupancy_ext(int type_k, int type_v, int D, int *ctas_per_sm);
 // the (K, V) type pairs a cache may hold: every pair of f16 / q8_0 / q4_0, plus these
 __host__ __device__ constexpr bool is_base_type(int t) { return t == KVQ_F16 || t == KVQ_Q8_0 || t == KVQ_Q4_0; }

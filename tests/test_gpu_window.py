@@ -5,9 +5,8 @@ front of a quantised tail ("HAL #582 -- per-layer KV compression study", section
   oracle quantising the same token's f16 value; the window holds the f16 values of the
   last W tokens, each in ring slot t mod W.
 * Read path: decode over both regions matches the oracle's two-region result (split
-  triples of each region, merged by the oracle's exact combine) within 1e-3; 256-wide heads
-  take the one-launch form (both regions' splits in one grid and one merge), 128-wide heads
-  two launches.
+  triples of each region, merged by the oracle's exact combine) within 1e-3, through the
+  one-launch form (both regions' splits in one grid and one merge) at D = 128 and 256.
 """
 import numpy as np
 import pytest
