@@ -500,8 +500,11 @@ def oracle_cell(wl, layer=0):
     import torch
     n = wl.lengths[0]
     extra = 64
-    K = torch.stack([syn.kv_rows(wl, syn.KIND_K, layer, 0, h, 0, n, device="cuda") for h in range(wl.n_kv_heads)])
-    V = torch.stack([syn.kv_rows(wl, syn.KIND_V, layer, 0, h, 0, n, device="cuda") for h in range(wl.n_kv_heads)])
+    # the GPU arm's generator where a GPU is present (the same values as that arm); else the
+    # host's (other values of the same distribution: the oracle's time depends on sizes only)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    K = torch.stack([syn.kv_rows(wl, syn.KIND_K, layer, 0, h, 0, n, device=dev) for h in range(wl.n_kv_heads)])
+    V = torch.stack([syn.kv_rows(wl, syn.KIND_V, layer, 0, h, 0, n, device=dev) for h in range(wl.n_kv_heads)])
     kc, ks = oracle.quantize(wl.type_k, K.cpu().numpy(), n_threads=0)
     vc, vs = oracle.quantize(wl.type_v, V.cpu().numpy(), n_threads=0)
 
@@ -509,8 +512,8 @@ def oracle_cell(wl, layer=0):
         pad = np.zeros((a.shape[0], extra) + a.shape[2:], a.dtype)
         return np.concatenate([a, pad], axis=1)
     kc, ks, vc, vs = grow(kc), grow(ks), grow(vc), grow(vs)
-    q = syn.queries(wl, layer).cpu().numpy()[0]
-    kn, vn = syn.new_rows(wl, layer, 0)
+    q = syn.queries(wl, layer, device=dev).cpu().numpy()[0]
+    kn, vn = syn.new_rows(wl, layer, 0, device=dev)
     return {"kc": kc, "ks": ks, "vc": vc, "vs": vs, "n": n, "q": q,
             "kn": kn.cpu().numpy()[0, :, 0], "vn": vn.cpu().numpy()[0, :, 0]}
 
