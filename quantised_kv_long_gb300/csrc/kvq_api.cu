@@ -130,6 +130,19 @@ WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits, int32_
     return w;
 }
 
+// Decode parameters: the arrival counters, split triples and group triples in `ws`.
+void set_workspace(kvq::DecodeParams &p, uint8_t *ws, const WsLayout &w) {
+    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
+    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
+    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
+    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
+    p.n_groups_max = w.n_groups_max;
+    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
+    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
+    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+}
+
 // ---- per-stream record of which cache each library launch writes ----
 // A decode launch reads its cache's lengths and tiles before the previous kernel of the
 // stream has finished (DecodeParams::early) unless the library's previous launch on that
@@ -403,15 +416,7 @@ kvq_status kvq_decode_attention(const kvq_cache *cache, const float *q, int32_t 
     kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s);
     p.out = out;
     p.lse = lse;
-    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
-    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
-    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
-    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
-    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
-    p.n_groups_max = w.n_groups_max;
-    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
-    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
-    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    set_workspace(p, ws, w);
     p.early = track_launch(static_cast<cudaStream_t>(stream), cache, nullptr) ? 1 : 0;
     return cuda_status(
         kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, static_cast<cudaStream_t>(stream)));
@@ -443,15 +448,7 @@ kvq_status kvq_append_decode(kvq_cache *cache, const float *k_new, const float *
     kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s);
     p.out = out;
     p.lse = lse;
-    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
-    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
-    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
-    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
-    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
-    p.n_groups_max = w.n_groups_max;
-    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
-    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
-    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    set_workspace(p, ws, w);
     p.k_new = k_new;
     p.v_new = v_new;
     p.ticket = cache->state + cache->desc.batch;
@@ -519,15 +516,7 @@ kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int32_t n_q
     kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s, n_q);
     p.out = out;
     p.lse = lse;
-    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
-    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
-    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
-    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
-    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
-    p.n_groups_max = w.n_groups_max;
-    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
-    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
-    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    set_workspace(p, ws, w);
     p.early = track_launch(static_cast<cudaStream_t>(stream), cache, nullptr) ? 1 : 0;
     return cuda_status(kvq::launch_verify(cache->desc.type_k, cache->desc.type_v, p, static_cast<cudaStream_t>(stream)));
 }
@@ -670,15 +659,7 @@ kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *tail, con
             kvq::DecodeParams &p = pr[r];
             p.out = out;
             p.lse = lse;
-            p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
-            p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
-            p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
-            p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
-            p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
-            p.n_groups_max = w.n_groups_max;
-            p.part_m = reinterpret_cast<float *>(ws + w.part_m);
-            p.part_l = reinterpret_cast<float *>(ws + w.part_l);
-            p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+            set_workspace(p, ws, w);
             p.part_stride = S;
             p.part_base = r == 0 ? 0 : nw;
             p.merge_slots = S;
@@ -696,15 +677,7 @@ kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *tail, con
         kvq::DecodeParams p = base_params(region[r], q, n_q_heads, scale, splits[r]);
         p.out = r == 0 ? w_out : out;
         p.lse = r == 0 ? w_lse : lse;
-        p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
-        p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
-        p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
-        p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
-        p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
-        p.n_groups_max = w.n_groups_max;
-        p.part_m = reinterpret_cast<float *>(ws + w.part_m);
-        p.part_l = reinterpret_cast<float *>(ws + w.part_l);
-        p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+        set_workspace(p, ws, w);
         if (r == 1) {
             p.ext_out = w_out;
             p.ext_lse = w_lse;
@@ -761,15 +734,7 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const float *q, 
     kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s);
     p.out = out;
     p.lse = lse;
-    p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
-    p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
-    p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
-    p.grp_l = reinterpret_cast<float *>(ws + w.grp_l);
-    p.grp_o = reinterpret_cast<float *>(ws + w.grp_o);
-    p.n_groups_max = w.n_groups_max;
-    p.part_m = reinterpret_cast<float *>(ws + w.part_m);
-    p.part_l = reinterpret_cast<float *>(ws + w.part_l);
-    p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    set_workspace(p, ws, w);
     p.early = track_launch(cs, cache, nullptr) ? 1 : 0;
     return cuda_status(kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, true, cs));
 }
