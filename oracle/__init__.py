@@ -166,11 +166,23 @@ def combine(part_o: np.ndarray, part_m: np.ndarray, part_l: np.ndarray):
     return out, lse
 
 
-# Bytes of one 32-value block.  f16, q8_0, q4_0 from the size model table of "HAL #582 --
-# per-layer KV compression study", section 1 (192 / 102 / 54 KiB per token of the 14B
-# shape); q5_1 from the section 5 P1 validation (q5_1 K + q4_0 V = 2016 MiB at 32768
-# cells, i.e. 63 KiB per token, of which q4_0 V is 27).
-BLOCK_BYTES = {"f16": 64, "q8_0": 34, "q4_0": 18, "q5_1": 24}
+# Bits of one stored code of each type (f16: the value itself).
+CODE_BITS = {"f16": 16, "q8_0": 8, "q4_0": 4, "q4_1": 4, "q5_0": 5, "q5_1": 5}
+
+
+def block_storage_bytes(kv_type: str) -> int:
+    """Packed storage of one 32-value block: 32 codes of CODE_BITS bits plus its f16 scale
+    values (d, and lo for the types with a minimum).  The natural layouts returned by
+    ``quantize`` keep 5-bit and q4_1 codes one per byte, so their arrays are larger."""
+    return QK * CODE_BITS[kv_type] // 8 + 2 * scales_per_block(kv_type)
+
+
+# Bytes of one 32-value block, pinned by the pages: f16, q8_0, q5_0, q4_0 by the size model
+# table of "HAL #582 -- per-layer KV compression study", section 1 (192 / 102 / 66 / 54
+# KiB per token of the 14B shape); q5_1 by the section 5 P1 validation (q5_1 K + q4_0 V =
+# 2016 MiB at 32768 cells, i.e. 63 KiB per token, of which q4_0 V is 27).  q4_1 is not
+# printed on the pages (its 20 bytes follow from block_storage_bytes alone).
+BLOCK_BYTES = {t: block_storage_bytes(t) for t in ("f16", "q8_0", "q4_0", "q5_0", "q5_1")}
 TIER_LADDER = [("f16", "f16"), ("q8_0", "q8_0"), ("q8_0", "q4_0"), ("q5_1", "q4_0")]
 
 

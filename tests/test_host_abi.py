@@ -21,7 +21,7 @@ def test_library_exports_every_header_symbol():
     for n in names:
         assert n in exported, n
         assert hasattr(kvq.lib, n)
-    assert kvq.lib.kvq_abi_version() == 2
+    assert kvq.lib.kvq_abi_version() == 3
 
 
 def test_status_strings():
@@ -130,11 +130,16 @@ def test_select_tier_rejects_bad_arguments():
 
 
 def test_cache_size_of_further_types_is_the_block_footprint():
+    """Plane sizes of the further types against the oracle's packed block sizes (q5_0 and
+    q5_1 pinned there by the pages' 66 KiB/token and 2016 MiB rows), not the library's own."""
+    import oracle
     for tk, tv in [("q8_0", "q5_0"), ("q5_0", "q5_0"), ("q5_1", "q5_1"), ("q4_1", "q4_1"), ("q5_1", "q4_0")]:
         for D in (128, 256):
             kb, vb, _ = kvq.cache_size(2, 3, D, 64, tk, tv)
             blocks = 2 * 3 * 64 * D // 32
-            assert kb == blocks * kvq.block_bytes(tk) and vb == blocks * kvq.block_bytes(tv), (tk, tv, D)
+            assert kb == blocks * oracle.block_storage_bytes(tk), (tk, tv, D)
+            assert vb == blocks * oracle.block_storage_bytes(tv), (tk, tv, D)
+            assert kvq.block_bytes(tk) == oracle.block_storage_bytes(tk)
     # pairs outside the supported set are refused
     d = kvq.Desc(1, 2, 128, 64, kvq.Q5_1, kvq.Q8_0)
     kb, vb, sb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()

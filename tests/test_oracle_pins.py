@@ -53,7 +53,7 @@ def _golden_rows():
 @pytest.mark.parametrize("row", _golden_rows(), ids=lambda r: f"{r[0]}-{r[4]}-{r[5]}-{r[6]}")
 def test_oracle_storage_matches_pages(row):
     src, L, H, D, tk, tv, ctx, val, unit = row
-    per_tok = L * H * (_oracle_bytes_per_row(tk, D) + _oracle_bytes_per_row(tv, D))
+    per_tok = L * H * (D // 32) * (oracle.BLOCK_BYTES[tk] + oracle.BLOCK_BYTES[tv])
     if unit == "KiB_per_token":
         assert per_tok / 1024 == val
     elif unit == "MiB":
@@ -67,6 +67,19 @@ def test_oracle_storage_matches_pages(row):
 def test_bytes_per_block():
     for t, nb in BYTES_PER_BLOCK.items():
         assert _oracle_bytes_per_row(t, 32) == nb
+        # where the natural layout is already packed, the packed-storage formula agrees with it
+        assert oracle.block_storage_bytes(t) == nb
+
+
+def test_packed_storage_of_five_bit_codes():
+    """q5_0 blocks: 32 five-bit codes (16 bytes of nibbles + 4 bytes of fifth bits) and one
+    f16 scale = 22 bytes, which the q5_0/q5_0 row of the size model table (66 KiB per
+    token) confirms; q5_1 adds the f16 minimum (24 bytes, the P1 ladder's floor)."""
+    assert oracle.block_storage_bytes("q5_0") == 16 + 4 + 2
+    assert oracle.block_storage_bytes("q5_1") == 16 + 4 + 2 + 2
+    assert oracle.block_storage_bytes("q4_1") == 16 + 2 + 2
+    # the oracle's natural q5_0 layout keeps one code per byte: the packed figure is smaller
+    assert _oracle_bytes_per_row("q5_0", 32) == 32 + 2
 
 
 # ---------------------------------------------------------------------------------
