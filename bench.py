@@ -216,9 +216,30 @@ def make_event(torch, external):
     return torch.cuda.Event(enable_timing=True)
 
 
-def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_event_graphs=16):
+def launch_ctas(cell):
+    """CTAs of one decode launch of a cell: splits x KV heads x sequences x row groups."""
+    wl = cell.wl
+    return cell.splits * wl.n_kv_heads * wl.batch * ((wl.G + 7) // 8)
+
+
+def stamp_spans(stamps, n_launch, layers, ctas):
+    """Per-launch timing from the CTA timer stamps of the last replay of each stamp graph:
+    span = last CTA exit - first CTA start (includes the overlap with the neighbouring
+    layers under programmatic dependent launch); gap = this launch's last exit - the
+    previous launch's last exit (the time a layer adds to the step)."""
+    st = stamps.view(n_launch, ctas, 2).double()
+    starts, ends = st[:, :, 0].min(dim=1).values, st[:, :, 1].max(dim=1).values
+    spans = ((ends - starts) * 1e-3).tolist()  # us
+    gaps = []
+    for g in range(n_launch // layers):
+        e = ends[g * layers:(g + 1) * layers]
+        gaps += ((e[1:] - e[:-1]) * 1e-3).tolist()
+    return spans, gaps
+
+
+def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_event_graphs=16, n_stamp_graphs=4):
     stream = torch.cuda.Stream()
-    extra = 1 + warmup + 2 * steps + (warmup + steps if e2e else 0) + 8
+    extra = 1 + warmup + 3 * steps + (warmup + steps if e2e else 0) + 8
     cell = Cell(kvq, torch, wl, extra, stream)
     L = wl.layers
     # eager warm-up step (also configures the kernels outside any capture)
@@ -241,6 +262,20 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
         with torch.cuda.graph(g, stream=stream):
             cell.launch_step(ev_sets[k])
         g_ev.append(g)
+    # graphs whose launches write per-CTA timer stamps (no events: the same schedule as g_plain)
+    ctas = launch_ctas(cell)
+    n_sg = min(steps, n_stamp_graphs)
+    stamps = torch.zeros(n_sg * L * ctas * 2, dtype=torch.int64, device=stream.device)
+    kvq.set_launch_stamps(stamps, n_sg * L, ctas)
+    g_st = []
+    try:
+        for k in range(n_sg):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                cell.launch_step()
+            g_st.append(g)
+    finally:
+        kvq.set_launch_stamps(None)
     torch.cuda.synchronize()
     for _ in range(warmup):
         g_plain.replay()
@@ -270,6 +305,18 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
                 g_ev[k % n_eg].replay()
         torch.cuda.synchronize()
         cell.executed(steps)
+    # timed region 3: the same steps through the stamp graphs (timer stamps per CTA)
+    ms_stamp = None
+    if n_sg:
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s0.record(stream)
+            for k in range(steps):
+                g_st[k % n_sg].replay()
+            s1.record(stream)
+        s1.synchronize()
+        ms_stamp = s0.elapsed_time(s1) / steps
+        cell.executed(steps)
     # mean lengths over the timed steps (each step appends one row before its decode)
     mean_lens = [x + (steps + 1) / 2.0 for x in lens0]
     bytes_step = step_kv_bytes(wl, mean_lens)
@@ -283,6 +330,17 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
     }
     res["pct_hbm_peak"] = 100.0 * res["kv_gbs"] / peak
     res["_wall"] = (wall0, wall1)
+    # the step holds nothing but decode launches (one per layer): its CUDA-event time over
+    # the timed region / layers is the kernel's average in-step launch duration
+    res["decode_instep_us"] = ms_step * 1e3 / L
+    if n_sg:
+        spans, gaps = stamp_spans(stamps, n_sg * L, L, ctas)
+        res["stamps"] = {"span_us_mean": statistics.fmean(spans), "span_us_median": statistics.median(spans),
+                         "gap_us_mean": statistics.fmean(gaps) if gaps else None,
+                         "launches": len(spans), "ms_per_step_stamp_pass": ms_stamp,
+                         "how": "%globaltimer at CTA start and exit in event-free graph replays; span = first "
+                                "start to last exit of a launch (overlaps its neighbours under programmatic "
+                                "dependent launch), gap = last exit of a launch - last exit of the previous one"}
     if n_eg:
         durs = []
         for k in range(n_eg):
@@ -332,10 +390,53 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
         if c.read_error() != 0:
             res["device_error"] = True
     cell.free()
-    del g_plain, g_ev
+    del g_plain, g_ev, g_st
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
+
+
+def run_rotating(kvq, torch, wl, steps, warmup, peak):
+    """A cell whose step set is within 4x L2, timed over R copies of its caches used in turn
+    (R x set > 4x L2), so that each step reads its KV from HBM rather than from L2."""
+    one = step_kv_bytes(wl, list(wl.lengths))
+    R = int(math.ceil(4 * L2_BYTES / one)) + 1
+    stream = torch.cuda.Stream()
+    extra = 1 + warmup + steps + 8
+    cells = [Cell(kvq, torch, wl, extra, stream) for _ in range(R)]
+    for c in cells:
+        c.launch_step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in cells:
+            c.launch_step()
+    torch.cuda.synchronize()
+    reps = max(1, steps // R)
+    for _ in range(max(1, warmup // R)):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * R)
+    bytes_step = step_kv_bytes(wl, [x + 2 + max(1, warmup // R) + reps / 2.0 for x in wl.lengths])
+    err = any(c2.read_error() for c in cells for c2 in c.caches)
+    for c in cells:
+        c.free()
+    del g, cells
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    r = {"copies": R, "set_bytes": R * one, "ms_per_step": ms, "steps_per_s": 1000.0 / ms,
+         "kv_gbs": bytes_step / (ms * 1e-3) / 1e9, "pct_hbm_peak": 100.0 * bytes_step / (ms * 1e-3) / 1e9 / peak,
+         "steps": reps * R}
+    if err:
+        r["device_error"] = True
+    return r
 
 
 def run_window_cell(kvq, torch, wl, window, steps, warmup, peak):
@@ -542,6 +643,44 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def oracle_attend_rate(wl, st, n_threads, budget_s):
+    """GB/s of the oracle's fp64 attention over the cell's cache (one layer per call)."""
+    import oracle
+    n = st["n"]
+    oracle.attention(wl.type_k, st["kc"], st["ks"], wl.type_v, st["vc"], st["vs"], n, st["q"], wl.scale,
+                     n_threads=n_threads)
+    t0 = time.perf_counter()
+    k = 0
+    while True:
+        oracle.attention(wl.type_k, st["kc"], st["ks"], wl.type_v, st["vc"], st["vs"], n, st["q"], wl.scale,
+                         n_threads=n_threads)
+        k += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"gbs": k * n * row_bytes(wl) / dt / 1e9, "s_per_layer": dt / k, "calls": k}
+
+
+def oracle_quantise_rate(n_threads, budget_s, rows=1024):
+    """Rows/s of the oracle's quantiser on the 14B shape's K (q8_0) and V (q4_0) rows
+    (8 KV heads x 128 values per row and plane)."""
+    import oracle
+    rng = np.random.default_rng(7)
+    K = rng.standard_normal((8, rows, 128)).astype(np.float32)
+    V = rng.standard_normal((8, rows, 128)).astype(np.float32)
+    oracle.quantize("q8_0", K, n_threads=n_threads)
+    t0 = time.perf_counter()
+    k = 0
+    while True:
+        oracle.quantize("q8_0", K, n_threads=n_threads)
+        oracle.quantize("q4_0", V, n_threads=n_threads)
+        k += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"rows_per_s": k * rows / dt, "gbs": k * rows * 8 * 128 * 4 * 2 / dt / 1e9}
+
+
 def cpu_baseline(wl, budget_s=10.0):
     st = oracle_cell(wl)
     oracle_step(wl, st)  # warm
@@ -553,11 +692,19 @@ def cpu_baseline(wl, budget_s=10.0):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+    cores = cpu_cores()
+    # the same oracle single-threaded and on all cores (thread count set explicitly each call)
+    detail = {"attention_1_thread": oracle_attend_rate(wl, st, 1, budget_s / 2),
+              "attention_all_cores": oracle_attend_rate(wl, st, cores, budget_s / 4),
+              "quantise_1_thread": oracle_quantise_rate(1, budget_s / 8),
+              "quantise_all_cores": oracle_quantise_rate(cores, budget_s / 8),
+              "scaled": f"the oracle runs one layer of {wl.name}; a {wl.layers}-layer step takes "
+                        f"{wl.layers} x that (GB/s is the same)"}
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{nsteps} single-layer decode steps (1-row quantise + fp64 attention of all "
                       f"{wl.n_q_heads} query heads over {wl.lengths[0]}+ rows) of {wl.name}; GB/s of the "
                       f"same algorithmic KV bytes, OpenMP over query heads",
-            "seconds": dt}
+            "seconds": dt, "detail": detail}
 
 
 # ----------------------------------------------------------------------------------------
@@ -570,9 +717,9 @@ def decode_kernel_sha() -> str:
     return h.hexdigest()
 
 
-def traffic_from_profiles(wl):
+def traffic_from_profiles(wl, path=None):
     """ncu DRAM bytes per decode launch recorded in profiles/, if the kernel source is unchanged."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    path = path or os.path.join(ROOT, "profiles", "decode_traffic.txt")
     try:
         sha = decode_kernel_sha()
         kv = {}
@@ -586,6 +733,30 @@ def traffic_from_profiles(wl):
         return float(kv["dram bytes per launch (read+write)"])
     except Exception:
         return None
+
+
+def short_name(r):
+    """A short cell label: shape, KV types, context."""
+    w = r["workload"]
+    fam = "hyb" if w.startswith("hybrid") else ("ms16" if w.startswith("multi") else "d48")
+    if w.startswith("verify"):
+        fam = "vfy" + str(r.get("n_q", "")) + "-" + ("hyb" if "hybrid" in w else "d48")
+    kv = r["kv"].replace("_0", "").replace("_1", "1").replace("f16 window + ", "w+").replace(" tail", "")
+    ctx = r["ctx"] if isinstance(r["ctx"], int) else "mix"
+    return f"{fam} {kv} {ctx // 1024}K" if isinstance(ctx, int) else f"{fam} {kv} {ctx}"
+
+
+def compact_cells(sweep, chunk):
+    """[label, steps/s, KV GB/s, % of HBM peak] per cell (+ rotating-buffer % where taken)."""
+    out = []
+    for r in sweep:
+        row = [short_name(r), round(r["steps_per_s"], 1), round(r["kv_gbs"]), round(r["pct_hbm_peak"], 1)]
+        if "rotating" in r:
+            row.append(round(r["rotating"]["pct_hbm_peak"], 1))
+        out.append(row)
+    if chunk:
+        out.append(["chunk4096 q8/q4", round(chunk["us_per_chunk"], 1), round(chunk["gbs"]), None])
+    return out
 
 
 def max_over_ranks(dist, value, device):
@@ -691,6 +862,8 @@ def main():
         for w in sweep_workloads("default")[1:]:
             r = run_cell(kvq, torch, w, args.sweep_steps, max(3, min(args.warmup, 5)), peak)
             r.pop("_wall")
+            if r["kv_bytes_per_step"] <= 4 * L2_BYTES:
+                r["rotating"] = run_rotating(kvq, torch, w, max(args.sweep_steps, 24), 6, peak)
             sweep.append(r)
         sweep.append(run_window_cell(kvq, torch, syn.hybrid(65536, "q8_0", "q8_0"), 4096, args.sweep_steps,
                                      max(3, min(args.warmup, 5)), peak))
@@ -713,13 +886,27 @@ def main():
     if rank != 0:
         return 0
     value = job_value(world, step_kv_bytes(wl, [wl.lengths[0]]), ms) if world > 1 else head["kv_gbs"]
-    achieved = head.get("decode_gbs")
+    bpl = head["kv_bytes_per_step"] / wl.layers  # algorithmic bytes per launch (mean length)
+    achieved = bpl / (head["decode_instep_us"] * 1e-6) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": (achieved / peak) if achieved else None, "traffic": traffic_from_profiles(wl),
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6800 GB/s", "kernel": "decode_kernel, fused-append mode (1-row quantise-append + split-K decode + split merge)",
-            "bytes_per_launch": step_kv_bytes(wl, [wl.lengths[0]]) / wl.layers,
-            "per_unit": f"{row_bytes(wl):.0f} B per (position, layer): Hkv*D*(bpv_K+bpv_V)"}
+            "frac": achieved / peak, "traffic": traffic_from_profiles(wl),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if peak_kind == "measured"
+            else "fallback 6800 GB/s",
+            "kernel": "decode_kernel, fused-append mode (1-row quantise-append + split-K decode + split merge)",
+            "bytes_per_launch": bpl,
+            "per_unit": f"{row_bytes(wl):.0f} B per (position, layer): Hkv*D*(bpv_K+bpv_V)",
+            "launch_us": head["decode_instep_us"],
+            "timing": "CUDA events over the timed region of event-free graph replays on the launching stream; "
+                      "the region holds only decode_kernel launches (one per layer), so region time / launches "
+                      "is the kernel's average in-step launch duration",
+            "serialised_events": {"launch_us": head.get("decode_us"), "achieved": head.get("decode_gbs"),
+                                  "frac": head["decode_gbs"] / peak if head.get("decode_gbs") else None,
+                                  "how": "CUDA events around every launch (event nodes serialise the launches)"},
+            "stamps": head.get("stamps")}
+    if head.get("stamps"):
+        sp = head["stamps"]["span_us_mean"]
+        roof["stamps"]["span_achieved"] = bpl / (sp * 1e-6) / 1e9
+        roof["stamps"]["span_frac"] = roof["stamps"]["span_achieved"] / peak
     e2e = head.pop("e2e")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -737,6 +924,10 @@ def main():
         "gpu_launches": wl.layers * args.steps, "clocks": clocks,
         "sweep": sweep, "chunk_quantise": chunk,
     }
+    # the per-cell table once more, compact and last (a reader of only the line's tail sees it)
+    cells = compact_cells(sweep, chunk)
+    line["config"]["cells"] = cells
+    line["cells"] = cells
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

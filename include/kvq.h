@@ -119,7 +119,7 @@
 extern "C" {
 #endif
 
-#define KVQ_ABI_VERSION 2
+#define KVQ_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define KVQ_API __attribute__((visibility("default")))
@@ -150,7 +150,9 @@ typedef enum {
 
 /* Device error word bits (kvq_cache_read_error). */
 #define KVQ_DEVERR_CAPACITY 0x1 /* an append found len + n_new > capacity on the device     */
-#define KVQ_DEVERR_TIMEOUT 0x2  /* a pipeline wait in a kernel gave up after its time limit */
+#define KVQ_DEVERR_TIMEOUT 0x2  /* a pipeline wait in a kernel gave up after its time limit:
+                                   the outputs of that launch are undefined (the workspace
+                                   counters are still left at zero)                        */
 
 typedef struct {
     int32_t batch;      /* B: sequences held by the cache (>= 1)                       */
@@ -204,8 +206,13 @@ KVQ_API kvq_status kvq_quantize_append(kvq_cache *cache, const float *k, const f
 KVQ_API kvq_status kvq_decode_auto_splits(const kvq_cache *cache, int32_t n_q_heads, int32_t *n_splits);
 
 /* Workspace bytes for kvq_decode_attention with this n_splits (0 = auto).  The workspace
- * holds split partials and per-(sequence, KV head) arrival counters; it must be zeroed
- * once before its first use, and every completed decode leaves the counters at zero. */
+ * holds per-(sequence, KV head, group of 8 query rows) arrival counters at its front,
+ * then split and group partials.  Zero it once before its first use; every completed
+ * decode leaves the counters at zero, including one whose waits timed out (a CTA that
+ * gives up still takes its arrivals).  The counters' places depend on the cache's batch
+ * and n_kv_heads and on n_q_heads (and n_q for draft verify) but not on n_splits, so one
+ * zeroed workspace serves every split count of those shapes; zero it again before using
+ * it for another shape. */
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache *cache, int32_t n_q_heads, int32_t n_splits,
                                      size_t *bytes);
 
@@ -338,10 +345,13 @@ KVQ_API kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *t
  * - The first call on a device looks up the array's device address for that device
  *   (cudaGetSymbolAddress, with that device current); make that first call before any
  *   stream capture.  Later calls only enqueue work.
- * - All calls share the one array, which keeps the contents of the last call: each call
- *   clears the arrival counters it relies on (an asynchronous memset on `stream`) before
- *   its kernel.  Calls that overlap on the GPU (different streams without ordering, or
- *   several host threads) race on the array and give wrong results.
+ * - All calls share the one array, which keeps the contents of the last call.  The arrival
+ *   counters at its front must start at zero: a call clears them (an asynchronous memset
+ *   on `stream`, before its kernel) when its counter region reaches past the previous
+ *   call's, whose split partials lie beyond that region; otherwise they are zero already,
+ *   since every finished decode leaves its counters at zero, and the call skips the clear.
+ *   Calls that overlap on the GPU (different streams without ordering, or several host
+ *   threads) race on the array and give wrong results.
  */
 #define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
 KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const float *q, int32_t n_q_heads,
@@ -378,6 +388,31 @@ typedef struct {
 } kvq_tier_choice;
 KVQ_API kvq_status kvq_select_tier(int64_t cells, int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
                                    uint64_t budget_bytes, kvq_tier_choice *out);
+
+/*
+ * Wait limit of the decode kernels' pipeline and merge waits, in SM clock cycles, for
+ * launches enqueued after this call (process-wide).  0 restores the default (4e9 cycles,
+ * about two seconds).  A wait that reaches the limit gives up: the kernel sets
+ * KVQ_DEVERR_TIMEOUT in the cache's error word, publishes an empty split triple for its
+ * CTA, still takes its merge arrivals and returns; the outputs of that launch are
+ * undefined, and a later call on the same workspace is correct again.  The wait for the
+ * kernel's own copies in flight before it reuses or releases shared memory keeps the
+ * default limit.  For failure handling and its tests: a short limit makes waits give up
+ * on a healthy GPU.  KVQ_ERR_INVALID_ARG for a negative value.
+ */
+KVQ_API kvq_status kvq_set_wait_limit(int64_t cycles);
+
+/*
+ * Launch timing for measurement (process-wide).  With buf non-NULL (device memory,
+ * 16-byte aligned, n_slots * ctas_per_slot * 2 uint64), every decode launch enqueued
+ * afterwards (decode, fused append + decode, partials, verify, window decode, no-alloc
+ * decode) takes the next of n_slots slots in turn, and CTA c of the launch (linear index
+ * x + X * (y + Y * z), only c < ctas_per_slot) writes the GPU's global nanosecond timer at
+ * its start to buf[slot][c][0] and at its exit to buf[slot][c][1].  A CUDA graph keeps the
+ * slots assigned at capture.  buf NULL stops the stamps.  KVQ_ERR_INVALID_ARG for bad
+ * sizes or alignment.
+ */
+KVQ_API kvq_status kvq_set_launch_stamps(void *buf, int32_t n_slots, int32_t ctas_per_slot);
 
 KVQ_API const char *kvq_status_string(kvq_status status);
 KVQ_API int32_t kvq_abi_version(void);

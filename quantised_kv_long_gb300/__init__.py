@@ -77,6 +77,10 @@ def _load():
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    L.kvq_set_wait_limit.argtypes = [ctypes.c_int64]
+    L.kvq_set_wait_limit.restype = ctypes.c_int
+    L.kvq_set_launch_stamps.argtypes = [vp, i32, i32]
+    L.kvq_set_launch_stamps.restype = ctypes.c_int
     L.kvq_select_tier.argtypes = [ctypes.c_int64, i32, i32, i32, ctypes.c_uint64, ctypes.POINTER(TierChoice)]
     L.kvq_select_tier.restype = ctypes.c_int
     L.kvq_block_bytes.argtypes = [ctypes.c_int]
@@ -164,6 +168,20 @@ class WindowedCache:
     def lengths(self):
         """(window lengths, tail lengths) from the host mirrors."""
         return self.window.lengths(), self.tail.lengths()
+
+
+def set_wait_limit(cycles: int = 0):
+    """Wait limit (SM clock cycles) of later decode launches' pipeline and merge waits
+    (kvq_set_wait_limit); 0 restores the default of about two seconds."""
+    _check(lib.kvq_set_wait_limit(int(cycles)), "kvq_set_wait_limit")
+
+
+def set_launch_stamps(buf=None, n_slots: int = 0, ctas_per_slot: int = 0):
+    """Per-CTA start/exit timer stamps of later decode launches (kvq_set_launch_stamps):
+    buf a uint64/int64 device tensor of n_slots * ctas_per_slot * 2 elements, or None to stop."""
+    if buf is not None:
+        assert buf.numel() >= n_slots * ctas_per_slot * 2 and buf.element_size() == 8 and buf.is_cuda
+    _check(lib.kvq_set_launch_stamps(_ptr(buf), n_slots, ctas_per_slot), "kvq_set_launch_stamps")
 
 
 def block_bytes(kv_type) -> int:

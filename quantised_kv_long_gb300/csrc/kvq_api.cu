@@ -1,5 +1,6 @@
 // kvq_api.cu -- the C ABI of libkvq (include/kvq.h): argument checks, the host handle,
 // the host mirror of the lengths and the launches.  No device memory is allocated here.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -78,9 +79,26 @@ kvq_status check_q_heads(const kvq_cache *c, int32_t n_q_heads, int32_t n_q = 1)
     return KVQ_OK;
 }
 
+// kvq_set_wait_limit (0: the default of about two seconds)
+std::atomic<long long> g_wait_cycles{kvq::kWaitCycles};
+
+// kvq_set_launch_stamps: each decode launch takes the next slot of the caller's buffer
+std::mutex g_stamp_mu;
+unsigned long long *g_stamp_buf = nullptr;
+int g_stamp_slots = 0, g_stamp_ctas = 0, g_stamp_next = 0;
+
+void take_stamp_slot(kvq::DecodeParams &p) {
+    std::lock_guard<std::mutex> lock(g_stamp_mu);
+    if (!g_stamp_buf || g_stamp_slots < 1) return;
+    p.stamps = g_stamp_buf + static_cast<size_t>(g_stamp_next) * g_stamp_ctas * 2;
+    p.stamp_ctas = g_stamp_ctas;
+    g_stamp_next = (g_stamp_next + 1) % g_stamp_slots;
+}
+
 kvq::DecodeParams base_params(const kvq_cache *c, const float *q, int32_t n_q_heads, float scale, int32_t splits,
                               int32_t n_q = 1) {
     kvq::DecodeParams p{};
+    p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
     p.k_codes = c->k_mem;
     p.k_scales = c->desc.type_k == KVQ_F16 ? nullptr : c->k_mem + c->k_code_bytes;
     p.v_codes = c->v_mem;
@@ -110,6 +128,10 @@ struct WsLayout {
     int n_groups_max;
 };
 
+// The arrival counters come first and their places depend only on the unit count
+// (sequences x KV heads x row groups), never on n_splits: a workspace zeroed once serves
+// every split count of the same cache shape and query rows, since each completed decode
+// leaves its counters at zero.  Split and group triples follow.
 WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits, int32_t n_q = 1) {
     WsLayout w{};
     const size_t G = n_q_heads / c->desc.n_kv_heads;
@@ -120,7 +142,7 @@ WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits, int32_
     w.n_groups_max = static_cast<int>(ng);
     w.counters = 0;
     w.counters1 = align256(units * 4);
-    w.part_m = w.counters1 + align256(units * ng * 4);
+    w.part_m = w.counters1 + align256(units * kvq::kGroupCounterStride * 4);
     w.part_l = w.part_m + align256(rows * splits * 4);
     w.part_o = w.part_l + align256(rows * splits * 4);
     w.grp_m = w.part_o + align256(rows * splits * c->desc.head_dim * 4);
@@ -132,6 +154,7 @@ WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits, int32_
 
 // Decode parameters: the arrival counters, split triples and group triples in `ws`.
 void set_workspace(kvq::DecodeParams &p, uint8_t *ws, const WsLayout &w) {
+    take_stamp_slot(p);
     p.counters = reinterpret_cast<int32_t *>(ws + w.counters);
     p.counters1 = reinterpret_cast<int32_t *>(ws + w.counters1);
     p.grp_m = reinterpret_cast<float *>(ws + w.grp_m);
@@ -192,6 +215,27 @@ bool track_launch(cudaStream_t stream, const kvq_cache *reads, const kvq_cache *
 extern "C" {
 
 int32_t kvq_abi_version(void) { return KVQ_ABI_VERSION; }
+
+kvq_status kvq_set_wait_limit(int64_t cycles) {
+    if (cycles < 0) return KVQ_ERR_INVALID_ARG;
+    g_wait_cycles.store(cycles == 0 ? kvq::kWaitCycles : static_cast<long long>(cycles), std::memory_order_relaxed);
+    return KVQ_OK;
+}
+
+kvq_status kvq_set_launch_stamps(void *buf, int32_t n_slots, int32_t ctas_per_slot) {
+    std::lock_guard<std::mutex> lock(g_stamp_mu);
+    if (buf == nullptr) {
+        g_stamp_buf = nullptr;
+        g_stamp_slots = g_stamp_ctas = g_stamp_next = 0;
+        return KVQ_OK;
+    }
+    if (n_slots < 1 || ctas_per_slot < 1 || !aligned16(buf)) return KVQ_ERR_INVALID_ARG;
+    g_stamp_buf = static_cast<unsigned long long *>(buf);
+    g_stamp_slots = n_slots;
+    g_stamp_ctas = ctas_per_slot;
+    g_stamp_next = 0;
+    return KVQ_OK;
+}
 
 const char *kvq_status_string(kvq_status s) {
     switch (s) {
@@ -471,6 +515,7 @@ kvq_status kvq_decode_partials(const kvq_cache *cache, const float *q, int32_t n
     p.part_o = part_o;
     p.part_m = part_m;
     p.part_l = part_l;
+    take_stamp_slot(p);
     p.early = track_launch(static_cast<cudaStream_t>(stream), cache, nullptr) ? 1 : 0;
     return cuda_status(
         kvq::launch_decode(cache->desc.type_k, cache->desc.type_v, p, false, static_cast<cudaStream_t>(stream)));
@@ -696,17 +741,18 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCR
 constexpr int kNoAllocDevices = 64;
 std::mutex g_noalloc_mutex;
 void *g_noalloc_addr[kNoAllocDevices] = {};
+// Bytes at the front of the array that hold zero once the last call's kernel has finished:
+// the counter region of that call (its split triples lie beyond it).
+size_t g_noalloc_zero[kNoAllocDevices] = {};
 
-// Device address of the scratch array for the current device, looked up once per device.
-kvq_status noalloc_scratch(void **addr) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
-    if (dev < 0 || dev >= kNoAllocDevices) return KVQ_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+// Device address of the scratch array for device `dev`, looked up once per device (the
+// caller holds g_noalloc_mutex and has made `dev` current).
+kvq_status noalloc_scratch(int dev, void **addr) {
     if (!g_noalloc_addr[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
         g_noalloc_addr[dev] = p;
+        g_noalloc_zero[dev] = 0;  // contents unknown until the first clear
     }
     *addr = g_noalloc_addr[dev];
     return KVQ_OK;
@@ -724,13 +770,24 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const float *q, 
     if (s == 0 && auto_splits(cache, n_q_heads, &s) != 0) return KVQ_ERR_CUDA;
     const WsLayout w = ws_layout(cache, n_q_heads, s);
     if (w.total > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_SCRATCH;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocDevices) return KVQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     void *base = nullptr;
-    st = noalloc_scratch(&base);
+    st = noalloc_scratch(dev, &base);
     if (st != KVQ_OK) return st;
     uint8_t *ws = static_cast<uint8_t *>(base);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // the arrival counters of both merge levels must start at zero; the rest is overwritten
-    if (cudaMemsetAsync(ws, 0, w.part_m, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+    // The arrival counters of both merge levels must start at zero; the rest is
+    // overwritten.  Every finished decode leaves its counters at zero, so the clear is
+    // needed only when this call's counter region reaches past the previous call's (whose
+    // split triples lie beyond it); skipping it keeps the programmatic launch overlap.
+    if (w.part_m > g_noalloc_zero[dev]) {
+        g_noalloc_zero[dev] = 0;
+        if (cudaMemsetAsync(ws, 0, w.part_m, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+    }
+    g_noalloc_zero[dev] = w.part_m;
     kvq::DecodeParams p = base_params(cache, q, n_q_heads, scale, s);
     p.out = out;
     p.lse = lse;

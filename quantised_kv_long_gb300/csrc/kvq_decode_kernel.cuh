@@ -356,14 +356,14 @@ __device__ void merge_cols(const float *po, const float *pm, const float *pl, in
     }
 }
 
-// Bounded wait (thread 0) until *counter >= target; false after about two seconds.
-__device__ __forceinline__ bool wait_count(const int32_t *counter, int target) {
+// Bounded wait (thread 0) until *counter >= target; false after `limit` SM clock cycles.
+__device__ __forceinline__ bool wait_count(const int32_t *counter, int target, long long limit) {
     const long long t0 = clock64();
     while (true) {
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(counter) : "memory");
         if (v >= target) return true;
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
         __nanosleep(64);
     }
 }
@@ -710,7 +710,7 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
         if (threadIdx.x == 0) {
             const int t = atomicAdd(cnt, 1);
             int role = t >= NP - P ? t - (NP - P) : -1;  // merger index, or -1
-            if (role >= 0 && t != NP - 1 && !wait_count(cnt, NP)) {
+            if (role >= 0 && t != NP - 1 && !wait_count(cnt, NP, p.wait_cycles)) {
                 atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
                 role = -2;  // a merger that gave up: no merge, but its second arrival counts
             }
@@ -739,7 +739,7 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
     const int n_groups = (NP + gs - 1) / gs;
     const int grp = slot / gs;
     const int gsize = min(gs, NP - grp * gs);
-    int32_t *cnt1 = p.counters1 + unit * p.n_groups_max + grp;
+    int32_t *cnt1 = p.counters1 + unit * kGroupCounterStride + grp;
     if (!arrive_last(cnt1, gsize, s_flag)) return;
     merge_rows(p.part_o, p.part_m, p.part_l, p.part_stride, grp * gs, gsize, row0, rows, D, nullptr, nullptr, p.grp_o,
                p.grp_m, p.grp_l, p.n_groups_max, grp);
@@ -876,7 +876,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
         int slot = k0 == C::STAGES ? 0 : k0, use = k0 == C::STAGES ? 1 : 0;
         for (int k = k0; k < n_stage; ++k) {
             bool ok_k = true;
-            if (lane == 0 && use > 0) ok_k = mbar_wait(empty + slot, (use - 1) & 1);
+            if (lane == 0 && use > 0) ok_k = mbar_wait(empty + slot, (use - 1) & 1, p.wait_cycles);
             if (!__shfl_sync(0xffffffffu, ok_k ? 1 : 0, 0)) {
                 ok = false;
                 break;
@@ -911,10 +911,13 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
         if (!ok && lane == 0) {
             atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
             s_timeout = 1;
-            // let the copies already issued land before the CTA can exit
+        }
+        // every copy this warp issued lands before the ring is reused or the CTA exits (the
+        // last use of each slot; a phase the consumers already saw completes at once).  This
+        // drain keeps the default limit whatever limit the other waits were given.
+        if (lane == 0)
             for (int i = 0; i < C::STAGES; ++i)
                 if (issued_use[i] >= 0) (void)mbar_wait(full + i, issued_use[i] & 1);
-        }
     } else {
         // ---------------- consumers ----------------
         if (early) grid_dep_wait();
@@ -977,7 +980,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
 
         int slot = 0, use = 0;
         for (int k = 0; k < n_stage; ++k) {
-            if (!dead && !mbar_wait(full + slot, use & 1)) {
+            if (!dead && !mbar_wait(full + slot, use & 1, p.wait_cycles)) {
                 dead = true;
                 atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
                 s_timeout = 1;
@@ -1228,23 +1231,40 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             if (dq == 0 && p.lse) p.lse[orow] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -CUDART_INF_F;
         } else {
+            // a CTA whose waits gave up publishes an empty triple (its tiles were not all
+            // read); the result is then undefined and the error word says so
             const size_t pr = (prow0 + g) * p.part_stride + p.part_base + split;
-            reinterpret_cast<float4 *>(p.part_o + pr * D)[dq] = acc;
+            reinterpret_cast<float4 *>(p.part_o + pr * D)[dq] = timed_out ? make_float4(0.f, 0.f, 0.f, 0.f) : acc;
             if (dq == 0) {
-                p.part_m[pr] = M == -CUDART_INF_F ? -CUDART_INF_F : M * kLn2;
-                p.part_l[pr] = lsum;
+                p.part_m[pr] = (M == -CUDART_INF_F || timed_out) ? -CUDART_INF_F : M * kLn2;
+                p.part_l[pr] = timed_out ? 0.f : lsum;
             }
         }
     }
-    if (!fused || single || timed_out) return;
+    // A CTA that timed out still takes its merge arrivals, so the arrival counters of the
+    // workspace end at zero once every CTA of the launch has finished.
+    if (!fused || single) return;
 
     const size_t unit = (static_cast<size_t>(bseq) * p.Hkv + h) * p.QG + qg;
     split_merge(p, p.merge_slots ? p.merge_slots : ns, p.part_base + split, rows, D, prow0, unit, rmap, s_flag, smem);
 }
 
+// Launch timing (p.stamps): thread 0 of a CTA writes %globaltimer when the CTA starts and
+// when it leaves the kernel (every path out of decode_body is CTA-uniform).
+__device__ __forceinline__ unsigned long long *cta_stamp(const DecodeParams &p) {
+    if (p.stamps == nullptr || threadIdx.x != 0) return nullptr;
+    const unsigned c = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (c >= static_cast<unsigned>(p.stamp_ctas)) return nullptr;
+    unsigned long long *st = p.stamps + 2 * static_cast<size_t>(c);
+    st[0] = global_timer_ns();
+    return st;
+}
+
 template <int KT, int VT, int NS, bool MQ>
 __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
+    unsigned long long *st = cta_stamp(p);
     decode_body<KT, VT, NS, MQ>(p, fused, blockIdx.x);
+    if (st) st[1] = global_timer_ns();
 }
 
 // One launch over an f16 window and a quantised tail of the same sequences: splits
@@ -1255,10 +1275,12 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     dual_kernel(const DecodeParams pw, const DecodeParams pt, const int nw) {
     constexpr int TWW = Cfg<KT, VT, NS>::TW;  // the window body runs with the tail's warp count
     static_assert(Cfg<KVQ_F16, KVQ_F16, NS, TWW>::THREADS == Cfg<KT, VT, NS>::THREADS, "one block size");
+    unsigned long long *st = cta_stamp(pt);
     if (static_cast<int>(blockIdx.x) < nw)
         decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x);
     else
         decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw);
+    if (st) st[1] = global_timer_ns();
 }
 
 constexpr int kMaxDevices = 64;

@@ -17,11 +17,14 @@ constexpr int kScaleTile = 128;  // scale bytes per (tile, slice): 16 rows x 4 b
 constexpr int kMaxSplits = 1024;
 
 // groups of the two-level split merge: at most ceil(sqrt(n_splits)) groups
-inline int max_merge_groups(int n_splits) {
+__host__ __device__ constexpr int max_merge_groups(int n_splits) {
     int g = 1;
     while (g * g < n_splits) ++g;
     return g + 1;
 }
+// first-level arrival counters per (sequence, KV head, row group): room for the largest
+// split count, so that the counter region of a workspace does not move with n_splits
+constexpr int kGroupCounterStride = max_merge_groups(kMaxSplits);
 constexpr int kMaxRowsPerGroup = 8;  // query heads of one KV head handled per CTA
 
 // per 16-row x 128-value tile slice: nibble types keep the q4_0 nibble layout (1024 B),
@@ -64,7 +67,7 @@ struct DecodeParams {
     float *part_o, *part_m, *part_l;  // [B][Hq][part_stride][D], [B][Hq][part_stride]
     int part_stride, part_base;       // triples per row; slot of this launch's split 0
     int32_t *counters;    // [B][Hkv][QG] (fused mode) or nullptr (partials mode)
-    int32_t *counters1;   // [B][Hkv][QG][n_groups_max]: first-level group arrivals
+    int32_t *counters1;   // [B][Hkv][QG][kGroupCounterStride]: first-level group arrivals
     float *grp_o, *grp_m, *grp_l;  // [B][Hq][n_groups_max][D], [B][Hq][n_groups_max]
     int n_groups_max;
     int B, Hkv, Hq, G, QG, D;
@@ -91,6 +94,13 @@ struct DecodeParams {
     // whose merge_slots splits all publish a triple (empty ones too) at part_base + split of
     // part_stride slots per row, merged as one set.
     int merge_slots;
+    // SM clock cycles a pipeline or merge wait may take before it gives up (kWaitCycles
+    // unless the caller set a limit with kvq_set_wait_limit)
+    long long wait_cycles;
+    // optional launch timing: CTA c (linear index < stamp_ctas) writes its %globaltimer at
+    // entry and at exit to stamps[2c], stamps[2c + 1]; nullptr: no stamps
+    unsigned long long *stamps;
+    int stamp_ctas;
 };
 
 struct AppendParams {
@@ -165,15 +175,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: gives up after ~kWaitCycles SM clock cycles and returns false.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up after `limit` SM clock cycles (default ~2 s) and returns false.
+// Limits below kPollWaitCycles (failure-handling tests) poll with the non-suspending test,
+// so that the give-up point does not depend on how long a suspended try_wait sleeps.
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+constexpr long long kPollWaitCycles = 1000000LL;
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit = kWaitCycles) {
+    if (limit < kPollWaitCycles) {
+        const long long t0 = clock64();
+        while (!mbar_test_wait(bar, parity))
+            if (clock64() - t0 > limit) return false;
+        return true;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
 }
 // 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes % 16 == 0).
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

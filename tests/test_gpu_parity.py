@@ -611,3 +611,40 @@ def test_back_to_back_launches_without_sync(kvq, order):
             ref, ref_lse = oracle.attention(tk, kc, ks, tv, vc, vs, n, qh[b], wl.scale)
             assert np.abs(out[b].cpu().numpy() - ref).max() <= TOL, (l, n, b)
             assert np.abs(lse[b].cpu().numpy() - ref_lse).max() <= TOL
+
+
+def test_one_workspace_serves_every_split_count(kvq):
+    """The workspace's arrival counters sit at places that do not depend on n_splits, so one
+    workspace zeroed once serves decodes with different split counts in turn: 3 splits (one
+    merge level), then 64 (8192 CTAs: the two-level merge), then 3 again (16 sequences, 8 KV
+    heads, G 5)."""
+    B, Hkv, G, D = 16, 8, 5, 128
+    lens = tuple(300 + 97 * b for b in range(B))
+    wl = syn.Workload("ws-reuse", 1, B, Hkv * G, Hkv, D, "q8_0", "q4_0", lens, seed=71)
+    cache = kvq.KVCache(B, Hkv, D, (max(lens) + 31) // 16 * 16, "q8_0", "q4_0")
+    Ks, Vs = [], []
+    for b in range(B):
+        K = torch.stack([syn.kv_rows(wl, syn.KIND_K, 0, b, h, 0, lens[b]) for h in range(Hkv)])
+        V = torch.stack([syn.kv_rows(wl, syn.KIND_V, 0, b, h, 0, lens[b]) for h in range(Hkv)])
+        cache.append(K[None].contiguous(), V[None].contiguous(), b0=b)
+        Ks.append(K.cpu().numpy())
+        Vs.append(V.cpu().numpy())
+    ws = torch.zeros(max(cache.workspace_bytes(wl.n_q_heads, s) for s in (3, 64)), dtype=torch.uint8,
+                     device="cuda")
+    refs = []
+    for step in range(3):
+        q = syn.queries(wl, 0, step=step)
+        qh = q.cpu().numpy()
+        r = []
+        for b in range(B):
+            kc, ks = oracle.quantize("q8_0", Ks[b])
+            vc, vs = oracle.quantize("q4_0", Vs[b])
+            r.append(oracle.attention("q8_0", kc, ks, "q4_0", vc, vs, lens[b], qh[b], wl.scale, n_threads=0))
+        refs.append((q, r))
+    for (q, r), splits in zip(refs, (3, 64, 3)):
+        out, lse = cache.decode(q, scale=wl.scale, n_splits=splits, workspace=ws)
+        torch.cuda.synchronize()
+        assert cache.read_error() == 0
+        for b in range(B):
+            assert np.abs(out[b].cpu().numpy() - r[b][0]).max() <= TOL, (splits, b)
+            assert np.abs(lse[b].cpu().numpy() - r[b][1]).max() <= TOL, (splits, b)

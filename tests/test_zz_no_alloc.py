@@ -4,14 +4,16 @@ Some callers cannot allocate device memory where they decode (a plugin that is h
 only input and output pointers, a server whose allocator has reserved all of HBM for
 cache pages, code that must not allocate during graph capture).  For them the library
 keeps a fixed scratch array of its own.  These checks call the entry point through the
-C ABI and compare it with kvq_decode_attention (caller workspace) on the same inputs,
-for two calls in a row, and check that an oversized request is refused.  This file is
-named to be collected last.
+C ABI and compare it with the CPU oracle (fp64 attention over the oracle's own
+quantisation of the same rows) and with kvq_decode_attention (caller workspace) on the
+same inputs, for two calls in a row, and check that an oversized request is refused.
+This file is named to be collected last.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import synthetic as syn
 
 pytestmark = pytest.mark.gpu
@@ -35,6 +37,29 @@ def filled_cache(kvq, wl):
     return cache
 
 
+def oracle_reference(wl, q):
+    """fp64 attention of every sequence by the CPU oracle, which quantises the same seeded
+    fp32 rows itself: (out [B, Hq, D], lse [B, Hq])."""
+    qh = q.cpu().numpy()
+    outs, lses = [], []
+    for b in range(wl.batch):
+        n = wl.lengths[b]
+        K = torch.stack([syn.kv_rows(wl, syn.KIND_K, 0, b, h, 0, n) for h in range(wl.n_kv_heads)]).cpu().numpy()
+        V = torch.stack([syn.kv_rows(wl, syn.KIND_V, 0, b, h, 0, n) for h in range(wl.n_kv_heads)]).cpu().numpy()
+        kc, ks = oracle.quantize(wl.type_k, K, n_threads=0)
+        vc, vs = oracle.quantize(wl.type_v, V, n_threads=0)
+        o, l = oracle.attention(wl.type_k, kc, ks, wl.type_v, vc, vs, n, qh[b], wl.scale, n_threads=0)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+def assert_close_to_oracle(out, lse, ref, ref_lse, what):
+    err = float(np.abs(out.cpu().numpy() - ref).max())
+    lerr = float(np.abs(lse.cpu().numpy() - ref_lse).max())
+    assert err <= TOL and lerr <= TOL, (what, err, lerr)
+
+
 @pytest.mark.parametrize("shape", [
     # (batch, Hq, Hkv, D, K type, V type, lengths)
     (1, 16, 2, 256, "q8_0", "q8_0", (3001,)),
@@ -46,13 +71,16 @@ def test_noalloc_matches_workspace_decode_twice(kvq, shape):
     wl = syn.Workload("noalloc", 1, B, Hq, Hkv, D, tk, tv, lens, seed=31)
     cache = filled_cache(kvq, wl)
     q = syn.queries(wl, 0)
-    ref, ref_lse = cache.decode(q, scale=wl.scale)
+    ws_out, ws_lse = cache.decode(q, scale=wl.scale)
     torch.cuda.synchronize()
+    ref, ref_lse = oracle_reference(wl, q)
+    assert_close_to_oracle(ws_out, ws_lse, ref, ref_lse, "workspace entry point")
     for call in range(2):
         out, lse = cache.decode_noalloc(q, scale=wl.scale)
         torch.cuda.synchronize()
-        err = float((out - ref).abs().max())
-        lerr = float((lse - ref_lse).abs().max())
+        assert_close_to_oracle(out, lse, ref, ref_lse, f"no-allocation call {call}")
+        err = float((out - ws_out).abs().max())
+        lerr = float((lse - ws_lse).abs().max())
         assert err <= TOL and lerr <= TOL, (call, err, lerr)
     assert cache.read_error() == 0
 
@@ -62,13 +90,33 @@ def test_noalloc_explicit_splits_and_new_queries(kvq):
     the previous call's contents; each call must not depend on them)."""
     wl = syn.Workload("noalloc2", 1, 1, 10, 2, 128, "q4_0", "q4_0", (1999,), seed=32)
     cache = filled_cache(kvq, wl)
-    for call, (splits, step) in enumerate([(64, 0), (7, 1)]):
+    for call, (splits, step) in enumerate([(64, 0), (7, 1), (300, 2)]):
         q = syn.queries(wl, 0, step=step)
-        ref, ref_lse = cache.decode(q, scale=wl.scale, n_splits=splits)
+        ref, ref_lse = oracle_reference(wl, q)
+        ws_out, ws_lse = cache.decode(q, scale=wl.scale, n_splits=splits)
         out, lse = cache.decode_noalloc(q, scale=wl.scale, n_splits=splits)
         torch.cuda.synchronize()
-        assert float((out - ref).abs().max()) <= TOL, call
-        assert float((lse - ref_lse).abs().max()) <= TOL, call
+        assert_close_to_oracle(out, lse, ref, ref_lse, call)
+        assert float((out - ws_out).abs().max()) <= TOL, call
+        assert float((lse - ws_lse).abs().max()) <= TOL, call
+
+
+def test_noalloc_after_a_larger_shape(kvq):
+    """A call whose counter region is smaller than the previous call's: the array's front is
+    still zero from the previous call (its counters ended at zero), so the clear is skipped;
+    then a larger one again, which must clear the previous call's split partials first."""
+    shapes = [(16, 40, 8, 128, "q8_0", "q4_0", tuple(300 + 37 * b for b in range(16))),
+              (1, 4, 2, 128, "q8_0", "q8_0", (900,)),
+              (4, 40, 8, 128, "q4_0", "q4_0", (1000, 17, 600, 2049))]
+    for i, (B, Hq, Hkv, D, tk, tv, lens) in enumerate(shapes):
+        wl = syn.Workload(f"noalloc4-{i}", 1, B, Hq, Hkv, D, tk, tv, lens, seed=40 + i)
+        cache = filled_cache(kvq, wl)
+        q = syn.queries(wl, 0)
+        out, lse = cache.decode_noalloc(q, scale=wl.scale)
+        torch.cuda.synchronize()
+        ref, ref_lse = oracle_reference(wl, q)
+        assert_close_to_oracle(out, lse, ref, ref_lse, i)
+        assert cache.read_error() == 0
 
 
 def test_noalloc_rejects_oversized_request(kvq):
