@@ -222,19 +222,30 @@ def launch_ctas(cell):
     return cell.splits * wl.n_kv_heads * wl.batch * ((wl.G + 7) // 8)
 
 
+STAMPS_PER_CTA = 4
+
+
 def stamp_spans(stamps, n_launch, layers, ctas):
-    """Per-launch timing from the CTA timer stamps of the last replay of each stamp graph:
+    """Per-launch timing from the CTA timer stamps of the last replay of each stamp graph
+    (per CTA: start, past the launch wait, triple published, exit; 0 = not reached):
     span = last CTA exit - first CTA start (includes the overlap with the neighbouring
     layers under programmatic dependent launch); gap = this launch's last exit - the
-    previous launch's last exit (the time a layer adds to the step)."""
-    st = stamps.view(n_launch, ctas, 2).double()
-    starts, ends = st[:, :, 0].min(dim=1).values, st[:, :, 1].max(dim=1).values
+    previous launch's last exit (the time a layer adds to the step); phases of a launch:
+    work = last triple published - first CTA past the wait, merge = last exit - last
+    triple published."""
+    st = stamps.view(n_launch, ctas, STAMPS_PER_CTA).double()
+    starts, ends = st[:, :, 0].min(dim=1).values, st[:, :, 3].max(dim=1).values
+    big = float(2 ** 62)
+    waited = st[:, :, 1].masked_fill(st[:, :, 1] == 0, big).min(dim=1).values
+    pub = st[:, :, 2].max(dim=1).values
     spans = ((ends - starts) * 1e-3).tolist()  # us
     gaps = []
     for g in range(n_launch // layers):
         e = ends[g * layers:(g + 1) * layers]
         gaps += ((e[1:] - e[:-1]) * 1e-3).tolist()
-    return spans, gaps
+    phases = {"work": ((pub - waited) * 1e-3).tolist(), "merge": ((ends - pub) * 1e-3).tolist(),
+              "pre_wait": ((waited - starts) * 1e-3).tolist()}
+    return spans, gaps, phases
 
 
 def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_event_graphs=16, n_stamp_graphs=4):
@@ -265,7 +276,7 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
     # graphs whose launches write per-CTA timer stamps (no events: the same schedule as g_plain)
     ctas = launch_ctas(cell)
     n_sg = min(steps, n_stamp_graphs)
-    stamps = torch.zeros(n_sg * L * ctas * 2, dtype=torch.int64, device=stream.device)
+    stamps = torch.zeros(n_sg * L * ctas * STAMPS_PER_CTA, dtype=torch.int64, device=stream.device)
     kvq.set_launch_stamps(stamps, n_sg * L, ctas)
     g_st = []
     try:
@@ -334,13 +345,17 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
     # the timed region / layers is the kernel's average in-step launch duration
     res["decode_instep_us"] = ms_step * 1e3 / L
     if n_sg:
-        spans, gaps = stamp_spans(stamps, n_sg * L, L, ctas)
+        spans, gaps, phases = stamp_spans(stamps, n_sg * L, L, ctas)
         res["stamps"] = {"span_us_mean": statistics.fmean(spans), "span_us_median": statistics.median(spans),
                          "gap_us_mean": statistics.fmean(gaps) if gaps else None,
+                         "phase_us_mean": {k: statistics.fmean(v) for k, v in phases.items()},
                          "launches": len(spans), "ms_per_step_stamp_pass": ms_stamp,
-                         "how": "%globaltimer at CTA start and exit in event-free graph replays; span = first "
-                                "start to last exit of a launch (overlaps its neighbours under programmatic "
-                                "dependent launch), gap = last exit of a launch - last exit of the previous one"}
+                         "how": "%globaltimer per CTA (start, past the launch wait, triple published, exit) in "
+                                "event-free graph replays; span = first start to last exit of a launch (overlaps "
+                                "its neighbours under programmatic dependent launch), gap = last exit of a launch - "
+                                "last exit of the previous one; phases: pre_wait = first CTA past the wait - first "
+                                "start, work = last triple published - first CTA past the wait, merge = last exit "
+                                "- last triple published"}
     if n_eg:
         durs = []
         for k in range(n_eg):
@@ -575,21 +590,35 @@ def chunk_quantise(kvq, torch, wl, reps=20, warmup=3):
     c = kvq.KVCache(1, wl.n_kv_heads, wl.head_dim, cap, wl.type_k, wl.type_v)
     K = torch.stack([syn.kv_rows(wl, syn.KIND_K, 0, 0, h, 0, n) for h in range(wl.n_kv_heads)])[None].contiguous()
     V = torch.stack([syn.kv_rows(wl, syn.KIND_V, 0, 0, h, 0, n) for h in range(wl.n_kv_heads)])[None].contiguous()
-    for _ in range(warmup):
-        c.append(K, V)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            c.append(K, V, stream=stream)
+    torch.cuda.synchronize()
+    # the timed appends form one CUDA graph, so that host launch overhead is not timed
+    c.set_lengths([0], stream=stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            c.append(K, V, stream=stream)
+    c.set_lengths([0], stream=stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        c.append(K, V)
-    e1.record()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
     e1.synchronize()
     ms = e0.elapsed_time(e1) / reps
+    err = c.read_error()
     rb = 2 * n * wl.n_kv_heads * wl.head_dim * 4
     wb = n * row_bytes(wl)
-    return {"rows": n, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "kv": f"{wl.type_k}/{wl.type_v}",
-            "us_per_chunk": ms * 1e3, "bytes_read": rb, "bytes_written": wb,
-            "gbs": (rb + wb) / (ms * 1e-3) / 1e9}
+    r = {"rows": n, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "kv": f"{wl.type_k}/{wl.type_v}",
+         "us_per_chunk": ms * 1e3, "bytes_read": rb, "bytes_written": wb,
+         "gbs": (rb + wb) / (ms * 1e-3) / 1e9, "timing": f"{reps} appends of one chunk in one CUDA graph"}
+    if err:
+        r["device_error"] = True
+    return r
 
 
 # ----------------------------------------------------------------------------------------

@@ -404,13 +404,14 @@ KVQ_API kvq_status kvq_set_wait_limit(int64_t cycles);
 
 /*
  * Launch timing for measurement (process-wide).  With buf non-NULL (device memory,
- * 16-byte aligned, n_slots * ctas_per_slot * 2 uint64), every decode launch enqueued
+ * 16-byte aligned, n_slots * ctas_per_slot * 4 uint64), every decode launch enqueued
  * afterwards (decode, fused append + decode, partials, verify, window decode, no-alloc
  * decode) takes the next of n_slots slots in turn, and CTA c of the launch (linear index
- * x + X * (y + Y * z), only c < ctas_per_slot) writes the GPU's global nanosecond timer at
- * its start to buf[slot][c][0] and at its exit to buf[slot][c][1].  A CUDA graph keeps the
- * slots assigned at capture.  buf NULL stops the stamps.  KVQ_ERR_INVALID_ARG for bad
- * sizes or alignment.
+ * x + X * (y + Y * z), only c < ctas_per_slot) writes the GPU's global nanosecond timer to
+ * buf[slot][c][0..3]: [0] when it starts, [1] once past the wait for the previous kernel
+ * of the stream (0 if it had no work), [2] once its split triple or output is written (0
+ * if it had no work), [3] when it exits.  A CUDA graph keeps the slots assigned at
+ * capture.  buf NULL stops the stamps.  KVQ_ERR_INVALID_ARG for bad sizes or alignment.
  */
 KVQ_API kvq_status kvq_set_launch_stamps(void *buf, int32_t n_slots, int32_t ctas_per_slot);
 

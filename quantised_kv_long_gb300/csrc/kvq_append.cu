@@ -12,30 +12,55 @@
 namespace kvq {
 namespace {
 
+// Items (row, KV head, slice) per warp and round: their fp32 values are all loaded before
+// any is quantised, so that several rows' loads are in flight per warp.
+constexpr int kAppendBatch = 8;
+constexpr int kAppendWarps = 8;  // warps per CTA
+
 template <int KT, int VT>
-__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(const AppendParams p) {
     __shared__ int s_last;
     const int lane = threadIdx.x & 31;
-    const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int NS = p.D / kSlice;
-    if (warp_global < p.total_warps) {
-        const int sl = warp_global % NS;
-        int rest = warp_global / NS;
-        const int row = rest % p.n_new;
-        rest /= p.n_new;
-        const int h = rest % p.Hkv;
-        const int bl = rest / p.Hkv;
-        const int bseq = p.b0 + bl;
-        const int L = __ldcg(p.len + bseq);
-        if (L >= 0 && L + p.n_new <= p.cap) {
-            const int pos = L + row;
-            const size_t tile = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + (pos >> 4);
-            const int kt = pos & 15;
-            const size_t src = ((static_cast<size_t>(bl) * p.Hkv + h) * p.n_new + row) * p.D + sl * kSlice + 4 * lane;
-            quantize_store<KT, false>(p.k + src, p.k_codes + (tile * NS + sl) * code_tile_bytes(KT),
-                                      p.k_scales + (tile * NS + sl) * scale_tile_bytes(KT), kt, lane);
-            quantize_store<VT, true>(p.v + src, p.v_codes + (tile * NS + sl) * code_tile_bytes(VT),
-                                     p.v_scales + (tile * NS + sl) * scale_tile_bytes(VT), kt, lane);
+    const int n_warps = gridDim.x * kAppendWarps;  // grid-stride over the items
+    for (int base = blockIdx.x * kAppendWarps + (threadIdx.x >> 5); base < p.total_warps;
+         base += kAppendBatch * n_warps) {
+        float4 xk[kAppendBatch], xv[kAppendBatch];
+        size_t tile_slice[kAppendBatch];
+        int kt[kAppendBatch];
+        bool ok[kAppendBatch];
+#pragma unroll
+        for (int u = 0; u < kAppendBatch; ++u) {
+            const int item = base + u * n_warps;
+            ok[u] = false;
+            if (item < p.total_warps) {
+                const int sl = item % NS;
+                int rest = item / NS;
+                const int row = rest % p.n_new;
+                rest /= p.n_new;
+                const int h = rest % p.Hkv;
+                const int bl = rest / p.Hkv;
+                const int bseq = p.b0 + bl;
+                const int L = __ldcg(p.len + bseq);
+                if (L >= 0 && L + p.n_new <= p.cap) {
+                    const int pos = L + row;
+                    tile_slice[u] = ((static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + (pos >> 4)) * NS + sl;
+                    kt[u] = pos & 15;
+                    const size_t src =
+                        ((static_cast<size_t>(bl) * p.Hkv + h) * p.n_new + row) * p.D + sl * kSlice + 4 * lane;
+                    xk[u] = __ldcs(reinterpret_cast<const float4 *>(p.k + src));
+                    xv[u] = __ldcs(reinterpret_cast<const float4 *>(p.v + src));
+                    ok[u] = true;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kAppendBatch; ++u) {
+            if (!ok[u]) continue;  // warp-uniform: every lane has the same item
+            quantize_store_vals<KT, false>(xk[u], p.k_codes + tile_slice[u] * code_tile_bytes(KT),
+                                           p.k_scales + tile_slice[u] * scale_tile_bytes(KT), kt[u], lane);
+            quantize_store_vals<VT, true>(xv[u], p.v_codes + tile_slice[u] * code_tile_bytes(VT),
+                                          p.v_scales + tile_slice[u] * scale_tile_bytes(VT), kt[u], lane);
         }
     }
     // the last CTA (all others have read len[] by now) advances the lengths
@@ -62,9 +87,13 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
 
 template <int KT, int VT>
 cudaError_t launch_append_t(const AppendParams &p, cudaStream_t stream) {
-    const int warps_per_block = 8;
-    const int blocks = (p.total_warps + warps_per_block - 1) / warps_per_block;
-    append_kernel<KT, VT><<<blocks, 32 * warps_per_block, 0, stream>>>(p);
+    // enough CTAs for about two rounds of batches on 152 SMs; small appends get one
+    // batch per warp (a one-row decode-step append is one CTA)
+    const long long per_cta = static_cast<long long>(kAppendWarps) * kAppendBatch;
+    long long blocks = (p.total_warps + per_cta - 1) / per_cta;
+    if (blocks > 8 * 152) blocks = 8 * 152;
+    if (blocks < 1) blocks = 1;
+    append_kernel<KT, VT><<<static_cast<unsigned>(blocks), 32 * kAppendWarps, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

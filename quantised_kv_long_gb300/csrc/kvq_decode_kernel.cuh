@@ -433,36 +433,46 @@ struct QFrag {
     uint32_t a[4];
 };
 
-// Scores of one tile over this warp's 128-value slice for keys A=2j, B=2j+1 (S-tile 0) and
-// C=8+2j, D=9+2j (S-tile 1), row g = lane/4, in log2 units (Q was prescaled).
-template <int KT>
+// Scores of NT consecutive tiles of a stage over this warp's 128-value slice: tile t's
+// codes at kc + t * KCB, its scales at ks + t * KSB; s[t] = scores of keys A=2j, B=2j+1
+// (S-tile 0) and C=8+2j, D=9+2j (S-tile 1), row g = lane/4, in log2 units (Q was
+// prescaled).  The loop over 32-value blocks is outermost, so each Q fragment is read from
+// shared memory once for all NT tiles.
+template <int KT, int NT, int KCB, int KSB>
 __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks, const uint8_t *qsm,
-                                            const uint8_t *kcor, int lane, int j, float (&s)[4]) {
+                                            const uint8_t *kcor, int lane, int j, float (&s)[NT][4]) {
     // Q fragment of chunk c (16 values), read from shared memory where it is used
     auto qa = [&](int c) {
         const uint4 v = lds128(qsm + (c * 32 + lane) * 16);
         return QFrag{{v.x, v.y, v.z, v.w}};
     };
     if constexpr (KT == KVQ_F16) {
-        float acc[2][4];
+        float acc[NT][2][4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const uint4 w0 = lds128(kc + (2 * b + 0) * 512 + lane * 16);
-            const uint4 w1 = lds128(kc + (2 * b + 1) * 512 + lane * 16);
-            if (b == 0) {
-                mma_16816_z(acc[0], qa(0).a, w0.x, w0.y);
-                mma_16816_z(acc[1], qa(0).a, w1.x, w1.y);
-            } else {
-                mma_16816(acc[0], qa(2 * b).a, w0.x, w0.y);
-                mma_16816(acc[1], qa(2 * b).a, w1.x, w1.y);
+            const QFrag q0 = qa(2 * b), q1 = qa(2 * b + 1);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint4 w0 = lds128(kc + t * KCB + (2 * b + 0) * 512 + lane * 16);
+                const uint4 w1 = lds128(kc + t * KCB + (2 * b + 1) * 512 + lane * 16);
+                if (b == 0) {
+                    mma_16816_z(acc[t][0], q0.a, w0.x, w0.y);
+                    mma_16816_z(acc[t][1], q0.a, w1.x, w1.y);
+                } else {
+                    mma_16816(acc[t][0], q0.a, w0.x, w0.y);
+                    mma_16816(acc[t][1], q0.a, w1.x, w1.y);
+                }
+                mma_16816(acc[t][0], q1.a, w0.z, w0.w);
+                mma_16816(acc[t][1], q1.a, w1.z, w1.w);
             }
-            mma_16816(acc[0], qa(2 * b + 1).a, w0.z, w0.w);
-            mma_16816(acc[1], qa(2 * b + 1).a, w1.z, w1.w);
         }
-        s[0] = acc[0][0] + acc[0][2];
-        s[1] = acc[0][1] + acc[0][3];
-        s[2] = acc[1][0] + acc[1][2];
-        s[3] = acc[1][1] + acc[1][3];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            s[t][0] = acc[t][0][0] + acc[t][0][2];
+            s[t][1] = acc[t][0][1] + acc[t][0][3];
+            s[t][2] = acc[t][1][0] + acc[t][1][2];
+            s[t][3] = acc[t][1][1] + acc[t][1][3];
+        }
     } else {
         // accumulators hold sum q * code in units of 2^-24 (q8_0, q5_0, q5_1) or, with the
         // low-nibble chunk of Q prescaled by 16, sum q * c in units of 2^-20 (q4_0, q4_1).
@@ -476,78 +486,101 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
             kcorr[2] = kc4.z;
             kcorr[3] = kc4.w;
         }
-        const uint4 sc0 = lds128(ks + j * 32), sc1 = lds128(ks + j * 32 + 16);
-        const uint32_t kscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
-        float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
-        uint4 wq4 = make_uint4(0, 0, 0, 0);
-        uint32_t hb = 0;
+        float2 s01[NT], s23[NT];
+        uint4 wq4[NT], scw[NT];
+        uint32_t hb[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            s01[t] = make_float2(0.f, 0.f);
+            s23[t] = make_float2(0.f, 0.f);
+            wq4[t] = make_uint4(0, 0, 0, 0);
+            scw[t] = make_uint4(0, 0, 0, 0);
+            hb[t] = 0;
+        }
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            float acc[2][4];
-            if constexpr (KT == KVQ_Q8_0) {
-                const uint4 w = lds128(kc + b * 512 + lane * 16);
-                mma_16816_z(acc[0], qa(2 * b).a, q8_02(w.x), q8_13(w.x));
-                mma_16816(acc[0], qa(2 * b + 1).a, q8_02(w.y), q8_13(w.y));
-                mma_16816_z(acc[1], qa(2 * b).a, q8_02(w.z), q8_13(w.z));
-                mma_16816(acc[1], qa(2 * b + 1).a, q8_02(w.w), q8_13(w.w));
-            } else if constexpr (!has_fifth_bit(KT)) {
-                if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
-                const uint32_t w0 = (b & 1) ? wq4.z : wq4.x, w0s = w0 >> 8;
-                const uint32_t w1 = (b & 1) ? wq4.w : wq4.y, w1s = w1 >> 8;
-                mma_16816_z(acc[0], qa(2 * b).a, w0 & kNibLo, w0s & kNibLo);
-                mma_16816(acc[0], qa(2 * b + 1).a, w0 & kNibHi, w0s & kNibHi);
-                mma_16816_z(acc[1], qa(2 * b).a, w1 & kNibLo, w1s & kNibLo);
-                mma_16816(acc[1], qa(2 * b + 1).a, w1 & kNibHi, w1s & kNibHi);
-            } else {
-                if ((b & 1) == 0) {
-                    wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
-                    hb = *reinterpret_cast<const uint32_t *>(kc + kNibbleBytes + (b >> 1) * 128 + lane * 4);
+            const QFrag q0 = qa(2 * b), q1 = qa(2 * b + 1);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint8_t *kct = kc + t * KCB;
+                const uint8_t *kst = ks + t * KSB;
+                float acc[2][4];
+                if constexpr (KT == KVQ_Q8_0) {
+                    const uint4 w = lds128(kct + b * 512 + lane * 16);
+                    mma_16816_z(acc[0], q0.a, q8_02(w.x), q8_13(w.x));
+                    mma_16816(acc[0], q1.a, q8_02(w.y), q8_13(w.y));
+                    mma_16816_z(acc[1], q0.a, q8_02(w.z), q8_13(w.z));
+                    mma_16816(acc[1], q1.a, q8_02(w.w), q8_13(w.w));
+                } else if constexpr (!has_fifth_bit(KT)) {
+                    if ((b & 1) == 0) wq4[t] = lds128(kct + (b >> 1) * 512 + lane * 16);
+                    const uint32_t w0 = (b & 1) ? wq4[t].z : wq4[t].x, w0s = w0 >> 8;
+                    const uint32_t w1 = (b & 1) ? wq4[t].w : wq4[t].y, w1s = w1 >> 8;
+                    mma_16816_z(acc[0], q0.a, w0 & kNibLo, w0s & kNibLo);
+                    mma_16816(acc[0], q1.a, w0 & kNibHi, w0s & kNibHi);
+                    mma_16816_z(acc[1], q0.a, w1 & kNibLo, w1s & kNibLo);
+                    mma_16816(acc[1], q1.a, w1 & kNibHi, w1s & kNibHi);
+                } else {
+                    if ((b & 1) == 0) {
+                        wq4[t] = lds128(kct + (b >> 1) * 512 + lane * 16);
+                        hb[t] = *reinterpret_cast<const uint32_t *>(kct + kNibbleBytes + (b >> 1) * 128 + lane * 4);
+                    }
+                    const int wi0 = 2 * (b & 1), wi1 = wi0 + 1;
+                    uint32_t c0[4], c1[4];
+                    fifth_bit_codes((b & 1) ? wq4[t].z : wq4[t].x, hb[t] >> wi0, c0);
+                    fifth_bit_codes((b & 1) ? wq4[t].w : wq4[t].y, hb[t] >> wi1, c1);
+                    mma_16816_z(acc[0], q0.a, c0[0], c0[1]);
+                    mma_16816(acc[0], q1.a, c0[2], c0[3]);
+                    mma_16816_z(acc[1], q0.a, c1[0], c1[1]);
+                    mma_16816(acc[1], q1.a, c1[2], c1[3]);
                 }
-                const int wi0 = 2 * (b & 1), wi1 = wi0 + 1;
-                uint32_t c0[4], c1[4];
-                fifth_bit_codes((b & 1) ? wq4.z : wq4.x, hb >> wi0, c0);
-                fifth_bit_codes((b & 1) ? wq4.w : wq4.y, hb >> wi1, c1);
-                mma_16816_z(acc[0], qa(2 * b).a, c0[0], c0[1]);
-                mma_16816(acc[0], qa(2 * b + 1).a, c0[2], c0[3]);
-                mma_16816_z(acc[1], qa(2 * b).a, c1[0], c1[1]);
-                mma_16816(acc[1], qa(2 * b + 1).a, c1[2], c1[3]);
-            }
-            const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
-            const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
-            float2 t01 = add2(make_float2(acc[0][0], acc[0][1]), make_float2(acc[0][2], acc[0][3]));
-            float2 t23 = add2(make_float2(acc[1][0], acc[1][1]), make_float2(acc[1][2], acc[1][3]));
-            if constexpr (KT == KVQ_Q4_0 || KT == KVQ_Q5_0) {
-                const float2 cb = make_float2(kcorr[b], kcorr[b]);
-                t01 = add2(t01, cb);
-                t23 = add2(t23, cb);
-            }
-            s01 = fma2(dab, t01, s01);
-            s23 = fma2(dcd, t23, s23);
-            if constexpr (has_min(KT)) {  // + lo * sum_b q
-                const uint2 lsc = *reinterpret_cast<const uint2 *>(ks + kScaleTile + j * 32 + b * 8);
-                const float2 cb = make_float2(kcorr[b], kcorr[b]);
-                s01 = fma2(__half22float2(u32_as_h2(lsc.x)), cb, s01);
-                s23 = fma2(__half22float2(u32_as_h2(lsc.y)), cb, s23);
+                // the scales of block b: keys (A,B) and (C,D) of this lane's pair j (one
+                // 16-byte load holds blocks b and b + 1)
+                if ((b & 1) == 0) scw[t] = lds128(kst + j * 32 + (b >> 1) * 16);
+                const float2 dab = __half22float2(u32_as_h2((b & 1) ? scw[t].z : scw[t].x));
+                const float2 dcd = __half22float2(u32_as_h2((b & 1) ? scw[t].w : scw[t].y));
+                float2 t01 = add2(make_float2(acc[0][0], acc[0][1]), make_float2(acc[0][2], acc[0][3]));
+                float2 t23 = add2(make_float2(acc[1][0], acc[1][1]), make_float2(acc[1][2], acc[1][3]));
+                if constexpr (KT == KVQ_Q4_0 || KT == KVQ_Q5_0) {
+                    const float2 cb = make_float2(kcorr[b], kcorr[b]);
+                    t01 = add2(t01, cb);
+                    t23 = add2(t23, cb);
+                }
+                s01[t] = fma2(dab, t01, s01[t]);
+                s23[t] = fma2(dcd, t23, s23[t]);
+                if constexpr (has_min(KT)) {  // + lo * sum_b q
+                    const uint2 lsc = *reinterpret_cast<const uint2 *>(kst + kScaleTile + j * 32 + b * 8);
+                    const float2 cb = make_float2(kcorr[b], kcorr[b]);
+                    s01[t] = fma2(__half22float2(u32_as_h2(lsc.x)), cb, s01[t]);
+                    s23[t] = fma2(__half22float2(u32_as_h2(lsc.y)), cb, s23[t]);
+                }
             }
         }
         constexpr float unit = (KT == KVQ_Q4_0 || KT == KVQ_Q4_1) ? kTwo20 : kTwo24;
-        s[0] = s01.x * unit;
-        s[1] = s01.y * unit;
-        s[2] = s23.x * unit;
-        s[3] = s23.y * unit;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            s[t][0] = s01[t].x * unit;
+            s[t][1] = s01[t].y * unit;
+            s[t][2] = s23[t].x * unit;
+            s[t][3] = s23[t].y * unit;
+        }
     }
 }
 
-// O += P V for one tile over this warp's slice.  pk: probabilities of keys A,B,C,D of row g;
-// vmask: which of A,B,C,D are inside the sequence (rows past the length may hold any bits).
+// O^T += V^T P^T for one tile over this warp's slice.  pk: probabilities of keys A,B,C,D
+// of row g; vmask: which of A,B,C,D are inside the sequence (rows past the length may hold
+// any bits).  The product is taken transposed: an mma's M rows are 16 values of the slice
+// (two of the fragment-native 8-value groups), N the 8 query rows, K the 16 keys, so the
+// hi and lo parts of P are two K steps into one accumulator and o holds 8 m-tiles x 4
+// (32 registers).  Lane (g, j) of m-tile mt = 2b + h holds rows 2j, 2j+1 of the values
+// 32b + 16h + 4(g/2) + 2(g%2) (c0, c1) and that value + 1 (c2, c3).
 template <int VT, bool PARTIAL>
 __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, const float (&pk)[4],
-                                        const bool (&vmask)[4], int lane, int j, float (&o)[16][4],
+                                        const bool (&vmask)[4], int lane, int j, float (&o)[8][4],
                                         uint32_t magic, float (&corr)[4]) {
     if constexpr (VT == KVQ_F16) {
-        uint32_t a[4];
-        split_hi_lo(pk[0], pk[1], a[0], a[1]);
-        split_hi_lo(pk[2], pk[3], a[2], a[3]);
+        uint32_t hab, lab, hcd, lcd;
+        split_hi_lo(pk[0], pk[1], hab, lab);
+        split_hi_lo(pk[2], pk[3], hcd, lcd);
         const uint32_t mab = (vmask[0] ? 0x0000ffffu : 0u) | (vmask[1] ? 0xffff0000u : 0u);
         const uint32_t mcd = (vmask[2] ? 0x0000ffffu : 0u) | (vmask[3] ? 0xffff0000u : 0u);
 #pragma unroll
@@ -564,17 +597,19 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
                 w1.z &= mab;
                 w1.w &= mcd;
             }
-            mma_16816(o[4 * b + 0], a, w0.x, w0.y);
-            mma_16816(o[4 * b + 1], a, w0.z, w0.w);
-            mma_16816(o[4 * b + 2], a, w1.x, w1.y);
-            mma_16816(o[4 * b + 3], a, w1.z, w1.w);
+            const uint32_t a0[4] = {w0.x, w0.z, w0.y, w0.w};
+            const uint32_t a1[4] = {w1.x, w1.z, w1.y, w1.w};
+            mma_16816(o[2 * b], a0, hab, hcd);
+            mma_16816(o[2 * b], a0, lab, lcd);
+            mma_16816(o[2 * b + 1], a1, hab, hcd);
+            mma_16816(o[2 * b + 1], a1, lab, lcd);
         }
     } else {
         // P' = p x scale per (key, block) as f16 hi + lo: p is split once per tile
         // (p = ph + pl), then per block  hi = ph*d,  err = fma(ph, d, -hi) (exact: the
         // rounding error of an f16 product), lo = fma(pl, d, err)  -- three packed f16 ops
         // per key pair, about 2^-21 relative.  The scale half2 words already pair keys
-        // (A,B) and (C,D), matching the A-fragment pairs.
+        // (A,B) and (C,D), matching the B-fragment pairs.
         uint32_t ph_ab, pl_ab, ph_cd, pl_cd;
         split_hi_lo(pk[0], pk[1], ph_ab, pl_ab);
         split_hi_lo(pk[2], pk[3], ph_cd, pl_cd);
@@ -595,20 +630,23 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
             const __half2 hcd = __hmul2(u32_as_h2(ph_cd), dcd);
             const __half2 eab = __hfma2(u32_as_h2(ph_ab), dab, __hneg2(hab));
             const __half2 ecd = __hfma2(u32_as_h2(ph_cd), dcd, __hneg2(hcd));
-            uint32_t a[4];
-            a[0] = h2_as_u32(hab);
-            a[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), dab, eab));
-            a[2] = h2_as_u32(hcd);
-            a[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), dcd, ecd));
+            const uint32_t bh0 = h2_as_u32(hab), bh1 = h2_as_u32(hcd);
+            const uint32_t bl0 = h2_as_u32(__hfma2(u32_as_h2(pl_ab), dab, eab));
+            const uint32_t bl1 = h2_as_u32(__hfma2(u32_as_h2(pl_cd), dcd, ecd));
             // q8_0: o accumulates sum P' * q in units of 2^-24; nibble types: exact f16 code
             // values by the magic-number route (nibble | 0x6400 is 1024 + c; a high nibble
             // gives 1024 + 16c, scaled by 1/16), less the offset (8 for q4_0, 16 for q5_0)
+            uint32_t a0[4], a1[4];
             if constexpr (VT == KVQ_Q8_0) {
                 const uint4 w = lds128(vc + b * 512 + lane * 16);
-                mma_16816(o[4 * b + 0], a, q8_02(w.x), q8_13(w.x));
-                mma_16816(o[4 * b + 1], a, q8_02(w.y), q8_13(w.y));
-                mma_16816(o[4 * b + 2], a, q8_02(w.z), q8_13(w.z));
-                mma_16816(o[4 * b + 3], a, q8_02(w.w), q8_13(w.w));
+                a0[0] = q8_02(w.x);
+                a0[1] = q8_02(w.y);
+                a0[2] = q8_13(w.x);
+                a0[3] = q8_13(w.y);
+                a1[0] = q8_02(w.z);
+                a1[1] = q8_02(w.w);
+                a1[2] = q8_13(w.z);
+                a1[3] = q8_13(w.w);
             } else if constexpr (!has_fifth_bit(VT)) {
                 if ((b & 1) == 0) wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
                 const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x, wq0s = wq0 >> 8;  // bytes 2n'   of the block
@@ -618,10 +656,14 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
                               khi = __float2half2_rn(-64.0f - off);
                 auto lo = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2((x & kNibLo) | magic), klo)); };
                 auto hi = [&](uint32_t x) { return h2_as_u32(__hfma2(u32_as_h2((x & kNibHi) | magic), k16th, khi)); };
-                mma_16816(o[4 * b + 0], a, lo(wq0), lo(wq0s));
-                mma_16816(o[4 * b + 2], a, hi(wq0), hi(wq0s));
-                mma_16816(o[4 * b + 1], a, lo(wq1), lo(wq1s));
-                mma_16816(o[4 * b + 3], a, hi(wq1), hi(wq1s));
+                a0[0] = lo(wq0);
+                a0[1] = lo(wq1);
+                a0[2] = lo(wq0s);
+                a0[3] = lo(wq1s);
+                a1[0] = hi(wq0);
+                a1[1] = hi(wq1);
+                a1[2] = hi(wq0s);
+                a1[3] = hi(wq1s);
             } else {
                 if ((b & 1) == 0) {
                     wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
@@ -632,14 +674,23 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
                 fifth_bit_codes((b & 1) ? wq4.w : wq4.y, hb >> (2 * (b & 1) + 1), c1);
                 const __half2 koff = __float2half2_rn(VT == KVQ_Q5_0 ? 1040.0f : 1024.0f);
                 auto val = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2(x | magic), koff)); };
-                mma_16816(o[4 * b + 0], a, val(c0[0]), val(c0[1]));
-                mma_16816(o[4 * b + 2], a, val(c0[2]), val(c0[3]));
-                mma_16816(o[4 * b + 1], a, val(c1[0]), val(c1[1]));
-                mma_16816(o[4 * b + 3], a, val(c1[2]), val(c1[3]));
+                a0[0] = val(c0[0]);
+                a0[1] = val(c1[0]);
+                a0[2] = val(c0[1]);
+                a0[3] = val(c1[1]);
+                a1[0] = val(c0[2]);
+                a1[1] = val(c1[2]);
+                a1[2] = val(c0[3]);
+                a1[3] = val(c1[3]);
             }
+            mma_16816(o[2 * b], a0, bh0, bh1);
+            mma_16816(o[2 * b], a0, bl0, bl1);
+            mma_16816(o[2 * b + 1], a1, bh0, bh1);
+            mma_16816(o[2 * b + 1], a1, bl0, bl1);
             if constexpr (has_min(VT)) {
                 // + p * lo for every value of the block: sum over keys of p * lo (f16 hi + lo
-                // like P') lands in column b of corr (B = 1.0 in column b); added at the end
+                // like P') lands in column b of corr (rows g: hi part, g + 8: lo part; B = 1.0
+                // in column b); added at the end
                 const uint2 lsc = *reinterpret_cast<const uint2 *>(vs + kScaleTile + j * 32 + b * 8);
                 const __half2 lab = u32_as_h2(lsc.x & mab), lcd = u32_as_h2(lsc.y & mcd);
                 const __half2 hab2 = __hmul2(u32_as_h2(ph_ab), lab), hcd2 = __hmul2(u32_as_h2(ph_cd), lcd);
@@ -648,7 +699,8 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
                 a2[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), lab, __hfma2(u32_as_h2(ph_ab), lab, __hneg2(hab2))));
                 a2[2] = h2_as_u32(hcd2);
                 a2[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), lcd, __hfma2(u32_as_h2(ph_cd), lcd, __hneg2(hcd2))));
-                const uint32_t one = (lane >> 2) == b ? 0x3c003c00u : 0u;
+                const int g = lane >> 2;
+                const uint32_t one = g == b ? 0x3c003c00u : 0u;
                 mma_16816(corr, a2, one, one);
             }
         }
@@ -750,10 +802,29 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
     if (threadIdx.x == 0) p.counters[unit] = 0;
 }
 
+// Launch timing (p.stamps): thread 0 of a CTA writes %globaltimer at four points, to
+// stamps[4c .. 4c + 3] for CTA c: start, past the programmatic-launch wait, once its split
+// triple (or its output) is written, and when it leaves the kernel (every path out of
+// decode_body is CTA-uniform).
+constexpr int kStamps = 4;
+__device__ __forceinline__ unsigned long long *cta_stamp(const DecodeParams &p) {
+    if (p.stamps == nullptr || threadIdx.x != 0) return nullptr;
+    const unsigned c = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (c >= static_cast<unsigned>(p.stamp_ctas)) return nullptr;
+    unsigned long long *st = p.stamps + kStamps * static_cast<size_t>(c);
+    st[0] = global_timer_ns();
+    st[1] = st[2] = 0;
+    return st;
+}
+__device__ __forceinline__ void stamp(unsigned long long *st, int k) {
+    if (st) st[k] = global_timer_ns();
+}
+
 // The decode of one CTA: split `split` of this launch's cache (blockIdx.y = KV head,
-// blockIdx.z = sequence x row group).
+// blockIdx.z = sequence x row group).  st: this CTA's timer stamps (thread 0) or nullptr.
 template <int KT, int VT, int NS, bool MQ, int TW_ = 0>
-__device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split) {
+__device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split,
+                                            unsigned long long *st) {
     using C = Cfg<KT, VT, NS, TW_>;
     constexpr int TPW = C::TPW;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -786,6 +857,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     if (!early) {
         if (threadIdx.x == 0) prefetch_split<C>(p, bseq, h, split, cap_rows, 0);
         grid_dep_wait();
+        stamp(st, 1);
     }
     int L_old = __ldcg(p.len + bseq);
     L_old = L_old < 0 ? 0 : (L_old > cap_rows ? cap_rows : L_old);
@@ -807,6 +879,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     // merge it runs on with an empty range (t_begin = t_end = T) and publishes an empty triple.
     if (split >= ns && p.merge_slots == 0) {
         if (early) grid_dep_wait();
+        if (early) stamp(st, 1);
         grid_dep_launch();
         if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
         if (!fused) {  // partials mode: splits beyond ns are empty triples
@@ -829,9 +902,9 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
 
     // per-consumer results kept until the merge
     float m_run = -CUDART_INF_F, l_acc = 0.f;
-    float o[16][4];
+    float o[8][4];  // O^T: 8 m-tiles of 16 values x (rows 2j, 2j+1), see tile_pv
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     int tw = 0, sl = 0;
 
     if (warp == 0) {
@@ -870,6 +943,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             }
             __syncwarp();
             grid_dep_wait();
+            stamp(st, 1);
         }
         grid_dep_launch();
         bool ok = true;
@@ -989,12 +1063,11 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             if (tA < t_end) {
                 const uint8_t *st = smem + slot * C::STAGE;
                 float sc[TPW][4];
-#pragma unroll
-                for (int t = 0; t < TPW; ++t) {
-                    const int ti = tw * TPW + t;  // tile index inside the stage
-                    tile_scores<KT>(st + ti * C::KC + sl * code_tile_bytes(KT),
-                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * scale_tile_bytes(KT), qsm, kcor_row, lane,
-                                    j, sc[t]);
+                {
+                    const int ti = tw * TPW;  // first tile of this warp inside the stage
+                    tile_scores<KT, TPW, C::KC, C::KS>(st + ti * C::KC + sl * code_tile_bytes(KT),
+                                                       st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * scale_tile_bytes(KT),
+                                                       qsm, kcor_row, lane, j, sc);
                 }
                 // f16 overflow guard: p = exp2(s - m_run) may reach 2^kTau before the running
                 // maximum is moved, so a tile pair holding a V scale with |scale| >= 256 (or
@@ -1089,12 +1162,15 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
 #pragma unroll
                         for (int i = 0; i < 4; ++i) corr[i] *= alpha;
                     }
+                    // o holds rows 2j and 2j+1, whose factors live in lanes 8j and 8j + 4
+                    const float a_r0 = __shfl_sync(0xffffffffu, alpha, 8 * j);
+                    const float a_r1 = __shfl_sync(0xffffffffu, alpha, 8 * j + 4);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        o[i][0] *= alpha;
-                        o[i][1] *= alpha;
-                        o[i][2] *= alpha;
-                        o[i][3] *= alpha;
+                    for (int i = 0; i < 8; ++i) {
+                        o[i][0] *= a_r0;
+                        o[i][1] *= a_r1;
+                        o[i][2] *= a_r0;
+                        o[i][3] *= a_r1;
                     }
                 }
                 float pk[TPW][4];
@@ -1135,29 +1211,31 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             }
         }
         // V types with a minimum: add sum of p * lo of each block to its values (corr column
-        // b, held by lane 4g + b/2 for the hi and lo rows)
+        // b of row r: hi part in lane 4r + b/2 at corr[b % 2], lo part at corr[2 + b % 2])
         if constexpr (has_min(VT)) {
             const float v0 = corr[0] + corr[2], v1 = corr[1] + corr[3];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                const float ct = __shfl_sync(0xffffffffu, (b & 1) ? v1 : v0, (lane & ~3) | (b >> 1));
+                const float src = (b & 1) ? v1 : v0;
+                const float ct0 = __shfl_sync(0xffffffffu, src, 8 * j + (b >> 1));      // row 2j
+                const float ct1 = __shfl_sync(0xffffffffu, src, 8 * j + 4 + (b >> 1));  // row 2j + 1
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    o[4 * b + i][0] += o[4 * b + i][2] + ct;
-                    o[4 * b + i][1] += o[4 * b + i][3] + ct;
-                    o[4 * b + i][2] = 0.f;
-                    o[4 * b + i][3] = 0.f;
+                for (int h = 0; h < 2; ++h) {
+                    o[2 * b + h][0] += ct0;
+                    o[2 * b + h][2] += ct0;
+                    o[2 * b + h][1] += ct1;
+                    o[2 * b + h][3] += ct1;
                 }
             }
         }
         // q8_0 V: o to real units
         if constexpr (VT == KVQ_Q8_0) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                o[i][0] = (o[i][0] + o[i][2]) * kTwo24;
-                o[i][1] = (o[i][1] + o[i][3]) * kTwo24;
-                o[i][2] = 0.f;
-                o[i][3] = 0.f;
+            for (int i = 0; i < 8; ++i) {
+                o[i][0] *= kTwo24;
+                o[i][1] *= kTwo24;
+                o[i][2] *= kTwo24;
+                o[i][3] *= kTwo24;
             }
         }
         // row sums over the four lanes of a row
@@ -1173,16 +1251,15 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     float *lb = mb + C::TW * kMaxRowsPerGroup;                     // [TW][8]
     if (warp > 0) {
         const int g = lane >> 2, j = lane & 3;
-        float *orow = Ob + (tw * kMaxRowsPerGroup + g) * D + sl * kSlice;
+        float *r0 = Ob + (tw * kMaxRowsPerGroup + 2 * j) * D + sl * kSlice;  // rows 2j, 2j + 1
+        float *r1 = r0 + D;
+        const int v0 = 4 * (g >> 1) + 2 * (g & 1);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            // thread holds d = 32b + 4j + {0..3} (ptiles 0,1 of block b) and +16 (ptiles 2,3)
-            const float4 lo4 = make_float4(o[4 * b + 0][0] + o[4 * b + 0][2], o[4 * b + 1][0] + o[4 * b + 1][2],
-                                           o[4 * b + 0][1] + o[4 * b + 0][3], o[4 * b + 1][1] + o[4 * b + 1][3]);
-            const float4 hi4 = make_float4(o[4 * b + 2][0] + o[4 * b + 2][2], o[4 * b + 3][0] + o[4 * b + 3][2],
-                                           o[4 * b + 2][1] + o[4 * b + 2][3], o[4 * b + 3][1] + o[4 * b + 3][3]);
-            *reinterpret_cast<float4 *>(orow + 32 * b + 4 * j) = lo4;
-            *reinterpret_cast<float4 *>(orow + 32 * b + 16 + 4 * j) = hi4;
+        for (int mt = 0; mt < 8; ++mt) {
+            // m-tile mt = 2b + h: values 32b + 16h + v0 (c0, c1) and + 1 (c2, c3)
+            const int v = 16 * mt + v0;
+            *reinterpret_cast<float2 *>(r0 + v) = make_float2(o[mt][0], o[mt][2]);
+            *reinterpret_cast<float2 *>(r1 + v) = make_float2(o[mt][1], o[mt][3]);
         }
         if (sl == 0 && j == 0) {
             mb[tw * kMaxRowsPerGroup + g] = m_run;
@@ -1241,6 +1318,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             }
         }
     }
+    stamp(st, 2);
     // A CTA that timed out still takes its merge arrivals, so the arrival counters of the
     // workspace end at zero once every CTA of the launch has finished.
     if (!fused || single) return;
@@ -1249,22 +1327,11 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     split_merge(p, p.merge_slots ? p.merge_slots : ns, p.part_base + split, rows, D, prow0, unit, rmap, s_flag, smem);
 }
 
-// Launch timing (p.stamps): thread 0 of a CTA writes %globaltimer when the CTA starts and
-// when it leaves the kernel (every path out of decode_body is CTA-uniform).
-__device__ __forceinline__ unsigned long long *cta_stamp(const DecodeParams &p) {
-    if (p.stamps == nullptr || threadIdx.x != 0) return nullptr;
-    const unsigned c = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-    if (c >= static_cast<unsigned>(p.stamp_ctas)) return nullptr;
-    unsigned long long *st = p.stamps + 2 * static_cast<size_t>(c);
-    st[0] = global_timer_ns();
-    return st;
-}
-
 template <int KT, int VT, int NS, bool MQ>
 __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
     unsigned long long *st = cta_stamp(p);
-    decode_body<KT, VT, NS, MQ>(p, fused, blockIdx.x);
-    if (st) st[1] = global_timer_ns();
+    decode_body<KT, VT, NS, MQ>(p, fused, blockIdx.x, st);
+    stamp(st, kStamps - 1);
 }
 
 // One launch over an f16 window and a quantised tail of the same sequences: splits
@@ -1277,10 +1344,10 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     static_assert(Cfg<KVQ_F16, KVQ_F16, NS, TWW>::THREADS == Cfg<KT, VT, NS>::THREADS, "one block size");
     unsigned long long *st = cta_stamp(pt);
     if (static_cast<int>(blockIdx.x) < nw)
-        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x);
+        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x, st);
     else
-        decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw);
-    if (st) st[1] = global_timer_ns();
+        decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw, st);
+    stamp(st, kStamps - 1);
 }
 
 constexpr int kMaxDevices = 64;
