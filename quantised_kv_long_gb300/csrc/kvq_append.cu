@@ -85,8 +85,107 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(const AppendP
     }
 }
 
+// Bulk appends (n_new >= 16 rows): whole 16-row tile slices are assembled in shared
+// memory and written out with 16-byte stores.  In the fragment-native layout the codes of
+// one row are interleaved with those of other rows of its tile (a V word holds four rows),
+// so writing row by row means byte stores scattered over the tile; assembling the tile
+// first turns them into coalesced stores.  One item = (sequence, KV head, slice, tile of
+// the append); a tile that the append covers only in part is first read back, so the rows
+// already in it are kept.  One warp per row of the tile.
+constexpr int kTileWarps = kTileRows;
+
+template <int KT, int VT>
+__global__ void __launch_bounds__(32 * kTileWarps) append_tiles_kernel(const AppendParams p, const int tiles_per_seq) {
+    constexpr int KC = code_tile_bytes(KT), VC = code_tile_bytes(VT);
+    constexpr int KS = scale_tile_bytes(KT), VS = scale_tile_bytes(VT);
+    constexpr int BYTES = KC + VC + KS + VS;
+    __shared__ __align__(16) uint8_t img[BYTES];
+    __shared__ int s_last;
+    const int lane = threadIdx.x & 31, kt = threadIdx.x >> 5;
+    const int NS = p.D / kSlice;
+    const long long items = static_cast<long long>(p.nb) * p.Hkv * NS * tiles_per_seq;
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const int ti = static_cast<int>(it % tiles_per_seq);
+        long long rest = it / tiles_per_seq;
+        const int sl = static_cast<int>(rest % NS);
+        rest /= NS;
+        const int h = static_cast<int>(rest % p.Hkv);
+        const int bl = static_cast<int>(rest / p.Hkv);
+        const int bseq = p.b0 + bl;
+        const int L = __ldcg(p.len + bseq);
+        if (L < 0 || L + p.n_new > p.cap) continue;  // block-uniform: the last CTA reports it
+        const int tile = (L >> 4) + ti;
+        const int r0 = tile * kTileRows;               // first position of the tile
+        if (r0 >= L + p.n_new) continue;               // past the append
+        const size_t ts = ((static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + tile) * NS + sl;
+        uint8_t *gk = p.k_codes + ts * KC, *gv = p.v_codes + ts * VC;
+        uint8_t *gks = KS ? p.k_scales + ts * KS : nullptr, *gvs = VS ? p.v_scales + ts * VS : nullptr;
+        auto region = [&](int o, uint8_t *&g, int &off) {  // global place of image byte o
+            if (o < KC) { g = gk; off = o; }
+            else if (o < KC + VC) { g = gv; off = o - KC; }
+            else if (o < KC + VC + KS) { g = gks; off = o - KC - VC; }
+            else { g = gvs; off = o - KC - VC - KS; }
+        };
+        const bool partial = r0 < L || r0 + kTileRows > L + p.n_new;
+        __syncthreads();  // the previous item's image has been written out
+        if (partial) {    // keep the rows of the tile that this append does not write
+            for (int o = threadIdx.x * 16; o < BYTES; o += blockDim.x * 16) {
+                uint8_t *g;
+                int off;
+                region(o, g, off);
+                *reinterpret_cast<uint4 *>(img + o) = __ldcg(reinterpret_cast<const uint4 *>(g + off));
+            }
+            __syncthreads();
+        }
+        const int pos = r0 + kt;
+        if (pos >= L && pos < L + p.n_new) {
+            const size_t src = ((static_cast<size_t>(bl) * p.Hkv + h) * p.n_new + (pos - L)) * p.D + sl * kSlice + 4 * lane;
+            const float4 xk = __ldcs(reinterpret_cast<const float4 *>(p.k + src));
+            const float4 xv = __ldcs(reinterpret_cast<const float4 *>(p.v + src));
+            quantize_store_vals<KT, false>(xk, img, img + KC + VC, kt, lane);
+            quantize_store_vals<VT, true>(xv, img + KC, img + KC + VC + KS, kt, lane);
+        }
+        __syncthreads();
+        for (int o = threadIdx.x * 16; o < BYTES; o += blockDim.x * 16) {
+            uint8_t *g;
+            int off;
+            region(o, g, off);
+            *reinterpret_cast<uint4 *>(g + off) = *reinterpret_cast<const uint4 *>(img + o);
+        }
+    }
+    // the last CTA (all others have read len[] by now) advances the lengths
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int t = atomicAdd(p.ticket, 1);
+        s_last = (t == static_cast<int>(gridDim.x) - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int i = threadIdx.x; i < p.nb; i += blockDim.x) {
+            const int bseq = p.b0 + i;
+            const int L = __ldcg(p.len + bseq);
+            if (L >= 0 && L + p.n_new <= p.cap)
+                p.len[bseq] = L + p.n_new;
+            else
+                atomicOr(p.err, KVQ_DEVERR_CAPACITY);
+        }
+        if (threadIdx.x == 0) *p.ticket = 0;
+    }
+}
+
 template <int KT, int VT>
 cudaError_t launch_append_t(const AppendParams &p, cudaStream_t stream) {
+    if (p.n_new >= kTileRows) {
+        // rows [L, L + n_new) cover (L % 16 + n_new - 1) / 16 + 1 tiles of a sequence, at
+        // most (n_new + 14) / 16 + 1 (L % 16 = 15); items past the append return at once
+        const int tiles_per_seq = (p.n_new + kTileRows - 2) / kTileRows + 1;
+        const long long items = static_cast<long long>(p.nb) * p.Hkv * (p.D / kSlice) * tiles_per_seq;
+        const long long blocks = items < 4 * 152 ? items : 4 * 152;
+        append_tiles_kernel<KT, VT><<<static_cast<unsigned>(blocks), 32 * kTileWarps, 0, stream>>>(p, tiles_per_seq);
+        return cudaGetLastError();
+    }
     // enough CTAs for about two rounds of batches on 152 SMs; small appends get one
     // batch per warp (a one-row decode-step append is one CTA)
     const long long per_cta = static_cast<long long>(kAppendWarps) * kAppendBatch;

@@ -356,13 +356,15 @@ __device__ void merge_cols(const float *po, const float *pm, const float *pl, in
     }
 }
 
-// Bounded wait (thread 0) until *counter >= target; false after `limit` SM clock cycles.
+// Bounded wait (thread 0) until the first-arrival count (low 16 bits) of *counter reaches
+// target; false after `limit` SM clock cycles.
+constexpr int kSecondArrival = 1 << 16;
 __device__ __forceinline__ bool wait_count(const int32_t *counter, int target, long long limit) {
     const long long t0 = clock64();
     while (true) {
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(counter) : "memory");
-        if (v >= target) return true;
+        if ((v & 0xffff) >= target) return true;
         if (clock64() - t0 > limit) return false;
         __nanosleep(64);
     }
@@ -710,6 +712,15 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
+// Tiles [t0, t1) of split `split` of a sequence with T tiles: shares of ceil(T / ns) tiles
+// (ns = min(n_splits, T); splits from ns on are empty).
+__device__ __forceinline__ void split_range(const DecodeParams &p, int T, int split, int &t0, int &t1) {
+    const int ns = max(1, min(p.n_splits, T));
+    const int tps = T > 0 ? (T + ns - 1) / ns : 0;
+    t0 = min(T, split * tps);
+    t1 = min(T, t0 + tps);
+}
+
 // Cache tiles this CTA starts with, pulled into L2 while the previous kernel of the stream
 // drains (called before the programmatic-launch wait).  Only a hint: the length read here
 // may be one append behind and the tiles may still be written; L2 is the coherence point,
@@ -723,10 +734,9 @@ __device__ __noinline__ void prefetch_split(const DecodeParams &p, int bseq, int
     if (p.k_new != nullptr) ++L;
     L = L < 0 ? 0 : (L > cap_rows ? cap_rows : L);
     const int T = (L + kTileRows - 1) / kTileRows;
-    const int ns = max(1, min(p.n_splits, T));
-    if (split >= ns || T == 0) return;
-    const int tps = (T + ns - 1) / ns;
-    const int t0 = min(T, split * tps + skip_tiles), t1 = min(T, split * tps + tps);
+    int t0, t1;
+    split_range(p, T, split, t0, t1);
+    t0 = min(t1, t0 + skip_tiles);
     const int nt = min(t1 - t0, kPrefetchBytes / C::TILE - skip_tiles);
     if (nt <= 0) return;
     const size_t bt = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + t0;
@@ -752,15 +762,19 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
                                             size_t unit, const RowMap &rmap, int &s_flag, uint8_t *smem) {
     const long long tbytes = static_cast<long long>(NP) * rows * (D + 2) * 4;
     if (p.wide && tbytes > kWideMinBytes) {
-        // the last P arrivals each merge a range of columns once every split has arrived;
-        // their second arrivals count P more, and the last of those clears the counter
+        // the last P arrivals each merge a range of columns once every split has arrived.
+        // The counter holds first arrivals in its low 16 bits and the mergers' second
+        // arrivals from bit 16 on, so that merger roles and the final clear stay exact even
+        // when a merger's wait gave up early and its second arrival came before the others'
+        // first ones: the clear is made by the second arrival that completes both counts
+        // (every non-merger arrives before the first merger does).
         const int C = rows * (D / 4);
         const int P = max(1, min(min(NP, C), static_cast<int>((tbytes + kWideBytes - 1) / kWideBytes)));
         int32_t *cnt = p.counters + unit;
         __threadfence();  // each thread publishes its own writes
         __syncthreads();
         if (threadIdx.x == 0) {
-            const int t = atomicAdd(cnt, 1);
+            const int t = atomicAdd(cnt, 1) & 0xffff;    // earlier first arrivals
             int role = t >= NP - P ? t - (NP - P) : -1;  // merger index, or -1
             if (role >= 0 && t != NP - 1 && !wait_count(cnt, NP, p.wait_cycles)) {
                 atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
@@ -777,7 +791,7 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
                        p.out, p.lse, rmap, p.ext_out, p.ext_lse, smem);
             __syncthreads();
         }
-        if (threadIdx.x == 0 && atomicAdd(cnt, 1) == NP + P - 1) atomicExch(cnt, 0);
+        if (threadIdx.x == 0 && atomicAdd(cnt, kSecondArrival) == NP + (P - 1) * kSecondArrival) atomicExch(cnt, 0);
         return;
     }
     if (tbytes <= kDirectMergeBytes) {
@@ -823,8 +837,8 @@ __device__ __forceinline__ void stamp(unsigned long long *st, int k) {
 // The decode of one CTA: split `split` of this launch's cache (blockIdx.y = KV head,
 // blockIdx.z = sequence x row group).  st: this CTA's timer stamps (thread 0) or nullptr.
 template <int KT, int VT, int NS, bool MQ, int TW_ = 0>
-__device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split,
-                                            unsigned long long *st) {
+__device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split, const int h,
+                                            const int z, unsigned long long *st) {
     using C = Cfg<KT, VT, NS, TW_>;
     constexpr int TPW = C::TPW;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -832,8 +846,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     __shared__ int s_timeout;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y;
-    const int bseq = blockIdx.z / p.QG, qg = blockIdx.z % p.QG;
+    const int bseq = z / p.QG, qg = z % p.QG;
     const int cap_rows = p.cap_tiles * kTileRows;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
     uint64_t *empty = full + C::STAGES;
@@ -867,7 +880,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     const int L = do_app ? L_old + 1 : L_old;
     const int T = (L + kTileRows - 1) / kTileRows;
     const int ns = max(1, min(p.n_splits, T));
-    const int tps = T > 0 ? (T + ns - 1) / ns : 0;
     const int n_q = MQ ? p.n_q : 1;     // queries per sequence (compile-time 1 for decode)
     const int unit_rows = n_q * p.G;    // query rows of this (sequence, KV head)
     const int rows = min(kMaxRowsPerGroup, unit_rows - qg * kMaxRowsPerGroup);
@@ -895,7 +907,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
         }
         return;
     }
-    const int t_begin = min(T, split * tps), t_end = min(T, t_begin + tps);
+    int t_begin, t_end;
+    split_range(p, T, split, t_begin, t_end);
     const int n_stage = (t_end - t_begin + C::TWT - 1) / C::TWT;
 
     const size_t bh_tile = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles;
@@ -1330,7 +1343,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
 template <int KT, int VT, int NS, bool MQ>
 __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
     unsigned long long *st = cta_stamp(p);
-    decode_body<KT, VT, NS, MQ>(p, fused, blockIdx.x, st);
+    decode_body<KT, VT, NS, MQ>(p, fused, blockIdx.x, blockIdx.y, blockIdx.z, st);
     stamp(st, kStamps - 1);
 }
 
@@ -1344,9 +1357,9 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     static_assert(Cfg<KVQ_F16, KVQ_F16, NS, TWW>::THREADS == Cfg<KT, VT, NS>::THREADS, "one block size");
     unsigned long long *st = cta_stamp(pt);
     if (static_cast<int>(blockIdx.x) < nw)
-        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x, st);
+        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x, blockIdx.y, blockIdx.z, st);
     else
-        decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw, st);
+        decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw, blockIdx.y, blockIdx.z, st);
     stamp(st, kStamps - 1);
 }
 
@@ -1413,6 +1426,7 @@ cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stre
     DecodeParams q = p;
     const long long ctas = static_cast<long long>(p.n_splits) * p.Hkv * p.B * p.QG;
     q.wide = (fused && ctas <= static_cast<long long>(occ) * sms) ? 1 : 0;
+
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B * p.QG);
     cfg.blockDim = dim3(C::THREADS);

@@ -98,7 +98,7 @@ struct DecodeParams {
     // unless the caller set a limit with kvq_set_wait_limit)
     long long wait_cycles;
     // optional launch timing: CTA c (linear index < stamp_ctas) writes its %globaltimer at
-    // entry and at exit to stamps[2c], stamps[2c + 1]; nullptr: no stamps
+    // four points to stamps[4c .. 4c + 3]; nullptr: no stamps
     unsigned long long *stamps;
     int stamp_ctas;
 };

@@ -75,6 +75,33 @@ def crafted_rows(n, D, rng):
     return x
 
 
+@pytest.mark.parametrize("tk,tv", [("q8_0", "q4_0"), ("f16", "q8_0"), ("q4_0", "f16")])
+@pytest.mark.parametrize("start", [0, 1, 7, 15])
+def test_bulk_append_tile_edges(kvq, tk, tv, start):
+    """Appends of 16 rows or more (assembled tile by tile) starting at every kind of offset
+    inside a tile, with lengths that end anywhere in a tile: the codes of the whole prefix
+    stay bit-exact (rows written before are kept) and lengths advance."""
+    H, D = 2, 128
+    rng = np.random.default_rng(start * 7 + len(tk))
+    cache = kvq.KVCache(1, H, D, 16 * 24, tk, tv)
+    chunks = [start, 16, 17, 31, 32, 47, 1, 63]
+    K = crafted_rows(H * sum(chunks), D, rng).reshape(H, sum(chunks), D)
+    V = crafted_rows(H * sum(chunks), D, rng).reshape(H, sum(chunks), D)
+    t = 0
+    for n in chunks:
+        if n:
+            cache.append(torch.from_numpy(K[None, :, t:t + n].copy()).cuda(),
+                         torch.from_numpy(V[None, :, t:t + n].copy()).cuda())
+        t += n
+    torch.cuda.synchronize()
+    assert cache.sync_lengths() == [t] and cache.read_error() == 0
+    kc, ksc, vc, vsc = read_natural(cache)
+    ok_c, ok_s = oracle.quantize(tk, K)
+    ov_c, ov_s = oracle.quantize(tv, V)
+    assert np.array_equal(kc[0, :, :t], ok_c) and np.array_equal(ksc[0, :, :t], ok_s)
+    assert np.array_equal(vc[0, :, :t], ov_c) and np.array_equal(vsc[0, :, :t], ov_s)
+
+
 @pytest.mark.parametrize("tk,tv", PAIRS)
 @pytest.mark.parametrize("D", [128, 256])
 def test_append_codes_bit_exact(kvq, tk, tv, D):
