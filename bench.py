@@ -814,6 +814,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None, help="run just this sweep workload (by name) as the timed cell")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling captures)")
+    ap.add_argument("--cell", choices=["verify4", "verify16", "window", "chunk"], default=None,
+                    help="time only this extra cell on the --only workload (default: the headline) and print it")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -868,6 +870,16 @@ def main():
     import quantised_kv_long_gb300 as kvq
 
     peak, peak_kind = measured_peaks()
+    if args.cell:  # one extra cell alone (profiling captures)
+        if args.cell.startswith("verify"):
+            r = run_verify_cell(kvq, torch, wl, int(args.cell[6:]), args.steps, args.warmup, peak)
+        elif args.cell == "window":
+            r = run_window_cell(kvq, torch, wl, 4096, args.steps, args.warmup, peak)
+        else:
+            r = chunk_quantise(kvq, torch, syn.multi_session(), reps=args.steps, warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"cell": args.cell, "result": r}), flush=True)
+        return 0
     gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] if world == 1 else str(local_rank)
     sampler = ClockSampler(gpu_id)
     sampler.start()

@@ -117,19 +117,24 @@ __device__ __forceinline__ int group_size(int ns) {
     return g;
 }
 
+// gpu-scope acquire-release fence.  After a CTA barrier, one thread's fence is cumulative
+// over the writes of the whole CTA (they happen before it through the barrier), so a CTA
+// publishes its results with one fence in thread 0 rather than one per thread.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;\n" ::: "memory"); }
+
 // All threads of the CTA call this after writing their results.  Returns true in the
 // CTA that is the target-th to arrive on *counter (it then sees every earlier write).
 __device__ __forceinline__ bool arrive_last(int32_t *counter, int target, int &s_flag) {
-    __threadfence();  // each thread publishes its own writes
     __syncthreads();
     if (threadIdx.x == 0) {
+        fence_acq_rel_gpu();  // release this CTA's writes
         const int t = atomicAdd(counter, 1);
-        s_flag = (t == target - 1);
+        const bool last = t == target - 1;
+        if (last) fence_acq_rel_gpu();  // acquire the others'
+        s_flag = last;
     }
     __syncthreads();
-    const bool last = s_flag != 0;
-    if (last) __threadfence();
-    return last;
+    return s_flag != 0;
 }
 
 // Query row (index into q, out, lse) of internal row `pr` (partial-triple row space, where
@@ -260,7 +265,7 @@ __device__ void merge_rows(const float *po, const float *pm, const float *pl, in
 // shared memory.  Memory for the reduction: 24 bytes per thread at `red`.
 constexpr int kWideMinBytes = kDirectMergeBytes;  // smaller row groups merge in one CTA
 constexpr int kWideBytes = 24 * 1024;     // triple bytes per merging CTA
-constexpr int kWideChunk = 8;
+constexpr int kWideChunk = 10;
 __device__ void merge_cols(const float *po, const float *pm, const float *pl, int stride, int NP, size_t row0,
                            int D, int c0, int c1, float *out, float *lse, const RowMap map, const float *ext_out,
                            const float *ext_lse, uint8_t *red) {
@@ -771,22 +776,22 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
         const int C = rows * (D / 4);
         const int P = max(1, min(min(NP, C), static_cast<int>((tbytes + kWideBytes - 1) / kWideBytes)));
         int32_t *cnt = p.counters + unit;
-        __threadfence();  // each thread publishes its own writes
         __syncthreads();
         if (threadIdx.x == 0) {
+            fence_acq_rel_gpu();  // release this CTA's triple
             const int t = atomicAdd(cnt, 1) & 0xffff;    // earlier first arrivals
             int role = t >= NP - P ? t - (NP - P) : -1;  // merger index, or -1
             if (role >= 0 && t != NP - 1 && !wait_count(cnt, NP, p.wait_cycles)) {
                 atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
                 role = -2;  // a merger that gave up: no merge, but its second arrival counts
             }
+            if (role >= 0) fence_acq_rel_gpu();  // acquire every triple
             s_flag = role;
         }
         __syncthreads();
         const int role = s_flag;
         if (role == -1) return;
         if (role >= 0) {
-            __threadfence();
             merge_cols(p.part_o, p.part_m, p.part_l, p.part_stride, NP, row0, D, role * C / P, (role + 1) * C / P,
                        p.out, p.lse, rmap, p.ext_out, p.ext_lse, smem);
             __syncthreads();
@@ -795,9 +800,10 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
         return;
     }
     if (tbytes <= kDirectMergeBytes) {
+        // the last arrival merges all splits, several threads per output column
         if (!arrive_last(p.counters + unit, NP, s_flag)) return;
-        merge_rows(p.part_o, p.part_m, p.part_l, p.part_stride, 0, NP, row0, rows, D, p.out, p.lse, nullptr, nullptr,
-                   nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
+        merge_cols(p.part_o, p.part_m, p.part_l, p.part_stride, NP, row0, D, 0, rows * (D / 4), p.out, p.lse, rmap,
+                   p.ext_out, p.ext_lse, smem);
         if (threadIdx.x == 0) p.counters[unit] = 0;
         return;
     }
