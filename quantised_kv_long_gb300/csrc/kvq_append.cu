@@ -91,17 +91,162 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kernel(const AppendP
 // so writing row by row means byte stores scattered over the tile; assembling the tile
 // first turns them into coalesced stores.  One item = (sequence, KV head, slice, tile of
 // the append); a tile that the append covers only in part is first read back, so the rows
-// already in it are kept.  One warp per row of the tile.
-constexpr int kTileWarps = kTileRows;
+// already in it are kept.  One thread quantises one 32-value block (of K or of V) of one
+// row: its maximum search and its two divisions are done once per block, with no shuffles.
+// The arithmetic is that of quantize_store_vals, operation for operation.
+template <int T, bool IS_V>
+__device__ __forceinline__ void quantize_block_store(const float (&x)[kBlock], uint8_t *codes, uint8_t *scales,
+                                                     int kt, int b) {
+    const int n = kt & 7, st = kt >> 3;
+    int j, pos;
+    pair_slot(kt, j, pos);
+    if constexpr (T == KVQ_F16) {
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4) {
+            const __half h0 = __float2half_rn(x[4 * g4]), h1 = __float2half_rn(x[4 * g4 + 1]);
+            const __half h2 = __float2half_rn(x[4 * g4 + 2]), h3 = __float2half_rn(x[4 * g4 + 3]);
+            if constexpr (!IS_V) {
+                const uint2 w = make_uint2(h2_as_u32(__halves2half2(h0, h2)), h2_as_u32(__halves2half2(h1, h3)));
+                *reinterpret_cast<uint2 *>(codes + (2 * b + st) * 512 + (4 * n + (g4 & 3)) * 16 + (g4 >> 2) * 8) = w;
+            } else {
+                const __half hv[4] = {h0, h1, h2, h3};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 4 * g4 + e, r = i & 15, hh = i >> 4, n2 = r >> 1;
+                    *reinterpret_cast<__half *>(codes + (2 * b + hh) * 512 + (4 * n2 + j) * 16 + (r & 1) * 8 + pos * 2) =
+                        hv[e];
+                }
+            }
+        }
+        return;
+    }
+    if constexpr (T == KVQ_Q8_0) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < kBlock; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+        uint32_t c[kBlock];
+#pragma unroll
+        for (int i = 0; i < kBlock; ++i) {  // stored as a sign-magnitude byte
+            const int q = static_cast<int>(round_half_away(__fmul_rn(x[i], id)));
+            c[i] = static_cast<uint32_t>(q < 0 ? (0x80 | -q) : q) & 0xffu;
+        }
+        if constexpr (!IS_V) {
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4)
+                *reinterpret_cast<uint32_t *>(codes + b * 512 + (4 * n + (g4 & 3)) * 16 + (2 * st + (g4 >> 2)) * 4) =
+                    c[4 * g4] | (c[4 * g4 + 1] << 8) | (c[4 * g4 + 2] << 16) | (c[4 * g4 + 3] << 24);
+        } else {
+            const int vb = vword_byte(pos);
+#pragma unroll
+            for (int i = 0; i < kBlock; ++i) {
+                const int r = i & 15, hv = i >> 4, n2 = r >> 1;
+                codes[b * 512 + (4 * n2 + j) * 16 + ((r & 1) + 2 * hv) * 4 + vb] = static_cast<uint8_t>(c[i]);
+            }
+        }
+        *reinterpret_cast<__half *>(scales + j * 32 + b * 8 + pos * 2) = __float2half_rn(d);
+        return;
+    }
+    if constexpr (is_nibble_type(T)) {
+        int c[kBlock];
+        float d, lo = 0.f;
+        if constexpr (!has_min(T)) {
+            // value of largest magnitude, the lowest index on ties; d = m / -K; codes
+            // min(2K - 1, trunc(x / d + K + 1/2)) with K = 8 (q4_0) or 16 (q5_0)
+            constexpr float K = T == KVQ_Q4_0 ? 8.0f : 16.0f;
+            constexpr int cmax = T == KVQ_Q4_0 ? 15 : 31;
+            float best = x[0], ba = fabsf(x[0]);
+#pragma unroll
+            for (int i = 1; i < kBlock; ++i) {
+                const float a = fabsf(x[i]);
+                if (a > ba) {
+                    ba = a;
+                    best = x[i];
+                }
+            }
+            d = __fdiv_rn(best, -K);
+            const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < kBlock; ++i) {
+                const int t = static_cast<int>(__fadd_rn(__fmul_rn(x[i], id), K + 0.5f));  // truncation
+                c[i] = t < cmax ? t : cmax;
+            }
+        } else {
+            // lo = min, hi = max, d = (hi - lo) / L, codes min(L, trunc((x - lo) / d + 1/2))
+            constexpr int L = T == KVQ_Q4_1 ? 15 : 31;
+            float hi = x[0];
+            lo = x[0];
+#pragma unroll
+            for (int i = 1; i < kBlock; ++i) {
+                lo = fminf(lo, x[i]);
+                hi = fmaxf(hi, x[i]);
+            }
+            d = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(L));
+            const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < kBlock; ++i) {
+                const int t = static_cast<int>(__fadd_rn(__fmul_rn(__fsub_rn(x[i], lo), id), 0.5f));
+                c[i] = t < L ? t : L;
+            }
+        }
+        // low 4 bits in the nibble bytes (value i in the low nibble, i + 16 in the high one);
+        // for 5-bit types the fifth bits in the plane after the nibbles (bit positions as in
+        // quantize_store_vals; other rows' bits of a word are kept)
+        uint32_t *hb_chunk = reinterpret_cast<uint32_t *>(codes + kNibbleBytes + (b >> 1) * 128);
+        if constexpr (!IS_V) {
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4) {
+                uint32_t w = 0, mask = 0, bits = 0;
+                const int wi = 2 * (b & 1) + st;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int lo_c = c[4 * g4 + e], hi_c = c[4 * g4 + 16 + e];
+                    w |= (uint32_t(lo_c & 15) | (uint32_t(hi_c & 15) << 4)) << (8 * e);
+                    mask |= (1u << (8 * e + 4 + wi)) | (1u << (8 * e + wi));
+                    bits |= (uint32_t(lo_c >> 4) << (8 * e + 4 + wi)) | (uint32_t(hi_c >> 4) << (8 * e + wi));
+                }
+                *reinterpret_cast<uint32_t *>(codes + (b >> 1) * 512 + (4 * n + g4) * 16 + (2 * (b & 1) + st) * 4) = w;
+                if constexpr (has_fifth_bit(T)) {
+                    atomicAnd(hb_chunk + (4 * n + g4), ~mask);
+                    atomicOr(hb_chunk + (4 * n + g4), bits);
+                }
+            }
+        } else {
+            const int vb = vword_byte(pos);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int n2 = i >> 1, qq = i & 1;
+                codes[(b >> 1) * 512 + (4 * n2 + j) * 16 + (2 * (b & 1) + qq) * 4 + vb] =
+                    static_cast<uint8_t>(uint32_t(c[i] & 15) | (uint32_t(c[i + 16] & 15) << 4));
+                if constexpr (has_fifth_bit(T)) {
+                    const int wi = 2 * (b & 1) + qq;
+                    const uint32_t mask = (1u << (8 * vb + 4 + wi)) | (1u << (8 * vb + wi));
+                    const uint32_t bits = (uint32_t(c[i] >> 4) << (8 * vb + 4 + wi)) | (uint32_t(c[i + 16] >> 4) << (8 * vb + wi));
+                    atomicAnd(hb_chunk + (4 * n2 + j), ~mask);
+                    atomicOr(hb_chunk + (4 * n2 + j), bits);
+                }
+            }
+        }
+        *reinterpret_cast<__half *>(scales + j * 32 + b * 8 + pos * 2) = __float2half_rn(d);
+        if constexpr (has_min(T)) *reinterpret_cast<__half *>(scales + kScaleTile + j * 32 + b * 8 + pos * 2) = __float2half_rn(lo);
+        return;
+    }
+}
+
+// threads of a tile CTA: one per (K or V, row, block): 2 x 16 x 4
+constexpr int kTileThreads = 2 * kTileRows * (kSlice / kBlock);
 
 template <int KT, int VT>
-__global__ void __launch_bounds__(32 * kTileWarps) append_tiles_kernel(const AppendParams p, const int tiles_per_seq) {
+__global__ void __launch_bounds__(kTileThreads) append_tiles_kernel(const AppendParams p, const int tiles_per_seq) {
     constexpr int KC = code_tile_bytes(KT), VC = code_tile_bytes(VT);
     constexpr int KS = scale_tile_bytes(KT), VS = scale_tile_bytes(VT);
     constexpr int BYTES = KC + VC + KS + VS;
     __shared__ __align__(16) uint8_t img[BYTES];
     __shared__ int s_last;
-    const int lane = threadIdx.x & 31, kt = threadIdx.x >> 5;
+    const bool is_v = threadIdx.x >= kTileThreads / 2;  // warp-uniform
+    const int rb = threadIdx.x % (kTileThreads / 2);
+    const int kt = rb >> 2, b = rb & 3;                 // row of the tile, block of the slice
     const int NS = p.D / kSlice;
     const long long items = static_cast<long long>(p.nb) * p.Hkv * NS * tiles_per_seq;
     for (long long it = blockIdx.x; it < items; it += gridDim.x) {
@@ -139,11 +284,21 @@ __global__ void __launch_bounds__(32 * kTileWarps) append_tiles_kernel(const App
         }
         const int pos = r0 + kt;
         if (pos >= L && pos < L + p.n_new) {
-            const size_t src = ((static_cast<size_t>(bl) * p.Hkv + h) * p.n_new + (pos - L)) * p.D + sl * kSlice + 4 * lane;
-            const float4 xk = __ldcs(reinterpret_cast<const float4 *>(p.k + src));
-            const float4 xv = __ldcs(reinterpret_cast<const float4 *>(p.v + src));
-            quantize_store_vals<KT, false>(xk, img, img + KC + VC, kt, lane);
-            quantize_store_vals<VT, true>(xv, img + KC, img + KC + VC + KS, kt, lane);
+            const size_t src = ((static_cast<size_t>(bl) * p.Hkv + h) * p.n_new + (pos - L)) * p.D + sl * kSlice + kBlock * b;
+            const float4 *x4 = reinterpret_cast<const float4 *>((is_v ? p.v : p.k) + src);
+            float x[kBlock];
+#pragma unroll
+            for (int i = 0; i < kBlock / 4; ++i) {
+                const float4 v = __ldcs(x4 + i);
+                x[4 * i] = v.x;
+                x[4 * i + 1] = v.y;
+                x[4 * i + 2] = v.z;
+                x[4 * i + 3] = v.w;
+            }
+            if (!is_v)
+                quantize_block_store<KT, false>(x, img, img + KC + VC, kt, b);
+            else
+                quantize_block_store<VT, true>(x, img + KC, img + KC + VC + KS, kt, b);
         }
         __syncthreads();
         for (int o = threadIdx.x * 16; o < BYTES; o += blockDim.x * 16) {
@@ -182,8 +337,8 @@ cudaError_t launch_append_t(const AppendParams &p, cudaStream_t stream) {
         // most (n_new + 14) / 16 + 1 (L % 16 = 15); items past the append return at once
         const int tiles_per_seq = (p.n_new + kTileRows - 2) / kTileRows + 1;
         const long long items = static_cast<long long>(p.nb) * p.Hkv * (p.D / kSlice) * tiles_per_seq;
-        const long long blocks = items < 4 * 152 ? items : 4 * 152;
-        append_tiles_kernel<KT, VT><<<static_cast<unsigned>(blocks), 32 * kTileWarps, 0, stream>>>(p, tiles_per_seq);
+        const long long blocks = items < 12 * 152 ? items : 12 * 152;
+        append_tiles_kernel<KT, VT><<<static_cast<unsigned>(blocks), kTileThreads, 0, stream>>>(p, tiles_per_seq);
         return cudaGetLastError();
     }
     // enough CTAs for about two rounds of batches on 152 SMs; small appends get one
