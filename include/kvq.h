@@ -291,6 +291,19 @@ KVQ_API kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int
                                      void *stream);
 
 /*
+ * Kernel choice of kvq_decode_verify (process-wide; the result is the same exact attention
+ * either way, within the same tolerance).  0 (default): when a (sequence, KV head) has 49
+ * to 128 query rows (n_q * Hq / Hkv), all of them form one 128-row tile on the tensor cores
+ * with accumulators in tensor memory (tcgen05): each key chunk is dequantised once for all
+ * rows; otherwise groups of 8 rows run the register-operand MMA kernel of
+ * kvq_decode_attention.  1: always the groups of 8.  2: the 128-row tile whenever the rows
+ * fit it.  Workspace sizes and automatic split counts follow the choice
+ * in force when they are computed: size the workspace after choosing.
+ * KVQ_ERR_INVALID_ARG for another value.
+ */
+KVQ_API kvq_status kvq_set_verify_path(int32_t path);
+
+/*
  * Position-axis mixed cache: an f16 window of the most recent tokens in front of a
  * quantised tail, "HAL #582 -- per-layer KV compression study", section 5 P2.  Two caches
  * of one shape (batch, n_kv_heads, head_dim) make the pair: `window` must be f16/f16, its

@@ -79,6 +79,8 @@ def _load():
         fn.restype = ctypes.c_int
     L.kvq_set_wait_limit.argtypes = [ctypes.c_int64]
     L.kvq_set_wait_limit.restype = ctypes.c_int
+    L.kvq_set_verify_path.argtypes = [i32]
+    L.kvq_set_verify_path.restype = ctypes.c_int
     L.kvq_set_launch_stamps.argtypes = [vp, i32, i32]
     L.kvq_set_launch_stamps.restype = ctypes.c_int
     L.kvq_select_tier.argtypes = [ctypes.c_int64, i32, i32, i32, ctypes.c_uint64, ctypes.POINTER(TierChoice)]
@@ -174,6 +176,12 @@ def set_wait_limit(cycles: int = 0):
     """Wait limit (SM clock cycles) of later decode launches' pipeline and merge waits
     (kvq_set_wait_limit); 0 restores the default of about two seconds."""
     _check(lib.kvq_set_wait_limit(int(cycles)), "kvq_set_wait_limit")
+
+
+def set_verify_path(path: int = 0):
+    """Kernel of kvq_decode_verify (kvq_set_verify_path): 0 automatic, 1 groups of 8 rows on
+    the register-operand MMA, 2 one 128-row tile on the tensor cores with tensor memory."""
+    _check(lib.kvq_set_verify_path(int(path)), "kvq_set_verify_path")
 
 
 def set_launch_stamps(buf=None, n_slots: int = 0, ctas_per_slot: int = 0):

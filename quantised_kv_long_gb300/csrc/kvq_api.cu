@@ -49,13 +49,36 @@ size_t state_bytes_for(int32_t batch) { return ((static_cast<size_t>(batch) + 2)
 
 kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
+// kvq_set_verify_path: 0 automatic, 1 register-operand MMA, 2 tensor-memory MMA
+std::atomic<int> g_verify_path{0};
+
+// Draft verify on the 128-row tensor-memory tile: base types, more than one group of 8 rows
+// and at most 128 rows per (sequence, KV head), unless the caller chose a path.
+// Automatic choice: the 128-row tile costs about the same for any row count, the groups of 8
+// about one single-query pass each; measured on the 65,536-position hybrid layers (D = 256,
+// G = 8), 4 groups (32 rows) were faster on the register-operand kernel and 16 groups (128
+// rows) on the tile, so the tile is taken from 7 groups (49 rows) up.
+constexpr int kVerifyTcMinRows = 6 * kvq::kMaxRowsPerGroup + 1;
+
+bool verify_on_tc(const kvq_cache *c, int32_t n_q_heads, int32_t n_q) {
+    const int rows = n_q * (n_q_heads / c->desc.n_kv_heads);
+    if (rows > kvq::kVerifyTileRows || !kvq::is_base_type(c->desc.type_k) || !kvq::is_base_type(c->desc.type_v))
+        return false;
+    const int path = g_verify_path.load(std::memory_order_relaxed);
+    return path == 2 || (path == 0 && rows >= kVerifyTcMinRows);
+}
+
 int auto_splits(const kvq_cache *c, int n_q_heads, int *out, int n_q = 1) {
     int ctas = 0, sms = 0;
     if (kvq::decode_occupancy(c->desc.type_k, c->desc.type_v, c->desc.head_dim, &ctas, &sms) != cudaSuccess)
         return -1;
     if (ctas < 1) ctas = 1;
     const int G = n_q_heads / c->desc.n_kv_heads;
-    const int QG = (n_q * G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
+    // the tensor-memory verify holds every query row of a (sequence, KV head) in one CTA, one
+    // CTA per SM (its shared and tensor memory)
+    const bool tc = n_q > 1 && verify_on_tc(c, n_q_heads, n_q);
+    if (tc) ctas = 1;
+    const int QG = tc ? 1 : (n_q * G + kvq::kMaxRowsPerGroup - 1) / kvq::kMaxRowsPerGroup;
     const long long units = static_cast<long long>(c->desc.batch) * c->desc.n_kv_heads * QG;
     // one full wave of CTAs, rounded down so that a unit count that does not divide the
     // wave does not spill into a partial second one; with several sequences (lengths may
@@ -563,7 +586,18 @@ kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int32_t n_q
     p.lse = lse;
     set_workspace(p, ws, w);
     p.early = track_launch(static_cast<cudaStream_t>(stream), cache, nullptr) ? 1 : 0;
+    if (verify_on_tc(cache, n_q_heads, n_q)) {
+        p.QG = 1;
+        return cuda_status(
+            kvq::launch_verify_tc(cache->desc.type_k, cache->desc.type_v, p, static_cast<cudaStream_t>(stream)));
+    }
     return cuda_status(kvq::launch_verify(cache->desc.type_k, cache->desc.type_v, p, static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_set_verify_path(int32_t path) {
+    if (path < 0 || path > 2) return KVQ_ERR_INVALID_ARG;
+    g_verify_path.store(path, std::memory_order_relaxed);
+    return KVQ_OK;
 }
 
 // ---- rolling f16 window + quantised tail ----

@@ -457,6 +457,10 @@ namespace kvq {
 cudaError_t launch_append(int type_k, int type_v, const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_window_append(int tail_k, int tail_v, const WindowParams &p, cudaStream_t stream);
 cudaError_t launch_verify(int type_k, int type_v, const DecodeParams &p, cudaStream_t stream);
+// draft verify with all query rows of a (sequence, KV head) in one 128-row tensor-core tile
+// (p.QG = 1, at most 128 rows); grid (n_splits, Hkv, B)
+cudaError_t launch_verify_tc(int type_k, int type_v, const DecodeParams &p, cudaStream_t stream);
+constexpr int kVerifyTileRows = 128;
 cudaError_t launch_decode_ext(int type_k, int type_v, const DecodeParams &p, bool fused, cudaStream_t stream);
 // one launch over an f16 window (params pw, splits [0, nw)) and a quantised tail (pt, the
 // remaining pt.merge_slots - nw splits); cudaErrorNotSupported where it is not built

@@ -18,7 +18,8 @@ TOL = 1e-3
 @pytest.fixture(scope="module")
 def kvq():
     import quantised_kv_long_gb300 as m
-    return m
+    yield m
+    m.set_verify_path(0)
 
 
 def filled(kvq, wl, cap):
@@ -61,7 +62,11 @@ def check(wl, K, V, q, out, lse, n_q):
     (3, 2, 2, 128, "q4_0", "q8_0", (5, 17, 40), 8, 0),     # a sequence shorter than the draft
     (1, 2, 5, 128, "q8_0", "q4_0", (1,), 1, 0),
 ])
-def test_verify_matches_oracle(kvq, shape):
+@pytest.mark.parametrize("path", [0, 1, 2])
+def test_verify_matches_oracle(kvq, shape, path):
+    """Every verify kernel: automatic choice (0), groups of 8 rows on the register-operand
+    MMA (1), one 128-row tile on the tensor cores with tensor memory (2)."""
+    kvq.set_verify_path(path)
     B, H, G, D, tk, tv, lens, n_q, splits = shape
     wl = syn.Workload("verify", 1, B, H * G, H, D, tk, tv, tuple(lens), seed=sum(lens) + n_q)
     cache, K, V = filled(kvq, wl, (max(lens) + 15) // 16 * 16 + 16)
@@ -90,3 +95,42 @@ def test_verify_rejects_bad_arguments(kvq):
     assert kvq.lib.kvq_verify_workspace_size(cache.handle, 0, 8, 0, __import__("ctypes").byref(b)) == 1
     assert kvq.lib.kvq_verify_workspace_size(cache.handle, 17, 8, 0, __import__("ctypes").byref(b)) == 1
     assert kvq.lib.kvq_verify_workspace_size(cache.handle, 16, 8, 0, __import__("ctypes").byref(b)) == 0
+
+
+@pytest.mark.parametrize("tk,tv", [("q8_0", "q8_0"), ("q4_0", "q4_0"), ("q8_0", "q4_0"), ("q4_0", "q8_0")])
+@pytest.mark.parametrize("D", [128, 256])
+def test_verify_tensor_tile_large_values(kvq, tk, tv, D):
+    """The 128-row tensor-memory kernel carries dequantised values as f16 hi + lo times a
+    per-chunk power of two; blocks of values up to ~1e5 (scales near the f16 range) beside
+    ordinary ones must stay exact.  Outputs of rows that attend to a huge V block are of
+    that size, so the output check is relative to the row's largest reference value."""
+    kvq.set_verify_path(2)
+    B, H, G, n_q, L = 1, 2, 8, 16, 700
+    rng = np.random.default_rng(D + len(tk + tv))
+    K = rng.standard_normal((H, L, D)).astype(np.float32)
+    V = rng.standard_normal((H, L, D)).astype(np.float32)
+    for h in range(H):  # a few rows with huge blocks, spread over the chunks
+        for r in range(3, L, 97):
+            K[h, r, 32:64] *= 3e4
+            V[h, r, 64:96] *= 3e4
+            V[h, r + 1, :32] *= 9e4 if tv != "q4_0" else 1.0
+    cache = kvq.KVCache(B, H, D, (L + 15) // 16 * 16, tk, tv)
+    cache.append(torch.from_numpy(K[None]).cuda(), torch.from_numpy(V[None]).cuda())
+    # the huge K block (values 32..63) changes the chunks' exponent but not the scores: Q has
+    # no weight there, so scores stay O(1) and lse keeps its absolute tolerance
+    qn = rng.standard_normal((B, n_q, H * G, D)).astype(np.float32)
+    qn[..., 32:64] = 0.0
+    q = torch.from_numpy(qn).cuda()
+    scale = 1.0 / np.sqrt(D)
+    out, lse = cache.verify(q, scale=scale)
+    torch.cuda.synchronize()
+    assert cache.read_error() == 0
+    kc, ks = oracle.quantize(tk, K)
+    vc, vs = oracle.quantize(tv, V)
+    qh, oh, lh = q.cpu().numpy(), out.cpu().numpy(), lse.cpu().numpy()
+    for i in range(n_q):
+        n = L - n_q + i + 1
+        ref, ref_lse = oracle.attention(tk, kc, ks, tv, vc, vs, n, qh[0, i], scale)
+        err = np.abs(oh[0, i] - ref).max() / max(1.0, np.abs(ref).max())
+        assert err <= TOL, (i, err)
+        assert np.abs(lh[0, i] - ref_lse).max() <= TOL, i
