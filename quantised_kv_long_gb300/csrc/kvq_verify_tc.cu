@@ -19,10 +19,10 @@
 // formed as p * 2^e_v, both exact.  Products are hi*hi + hi*lo + lo*hi (the lo*lo term is
 // below 2^-21 relative); accumulation is fp32.
 //
-// Warp roles (384 threads): warp 0 streams the chunks' tiles into a shared-memory ring
+// Warp roles (512 threads): warp 0 streams the chunks' tiles into a shared-memory ring
 // with 1-D bulk copies (as the decode kernel); warp 1 owns the tensor memory and one of its
 // threads issues every MMA; warps 2-5 hold one query row per thread (softmax, P, the
-// rescale of O, the epilogue); warps 6-11 convert codes into K^ and V^.  Every wait is
+// rescale of O, the epilogue); warps 6-15 convert codes into K^ and V^.  Every wait is
 // bounded and reports KVQ_DEVERR_TIMEOUT.
 #include "kvq_decode_kernel.cuh"
 
@@ -116,14 +116,18 @@ struct TcCfg {
     static constexpr int VHAT = D * NK * 2;   // one of V^ hi / lo, K-major (values x keys)
     static constexpr bool K_LO = KT != KVQ_F16;  // f16 codes are exact f16 values
     static constexpr bool V_LO = VT != KVQ_F16;
-    static constexpr int OPS = QHI + 2 * (K_LO ? 2 : 1) * KHAT + (V_LO ? 2 : 1) * VHAT;
-    static constexpr int BUDGET = 229 * 1024;  // dynamic shared memory of one CTA
-    static constexpr int STAGES = (BUDGET - OPS - 1024) / STAGE >= 3 ? 3 : 2;
+    static constexpr int QT_ROW = 80;             // Q lo transpose rows: 32 halves + 16 bytes of padding
+    static constexpr int QT = 4 * 32 * QT_ROW;      // one 32-row block per softmax warp
+    static constexpr int OPS = QHI + 2 * (K_LO ? 2 : 1) * KHAT + (V_LO ? 2 : 1) * VHAT + QT;
+    static constexpr int O_ROW = D * 4 + 16;       // epilogue staging of O (padded rows)
+    static constexpr int BUDGET = 232448 - 512;  // shared memory of one CTA (227 KiB) less the static variables
+    static constexpr int STAGES = (BUDGET - OPS - 512) / STAGE >= 3 ? 3 : 2;  // 512: barriers
     static constexpr int RING = STAGES * STAGE;
     static constexpr int OFF_Q = RING;
     static constexpr int OFF_K = OFF_Q + QHI;                      // [buffer 0, 1][hi, lo]
     static constexpr int OFF_V = OFF_K + 2 * (K_LO ? 2 : 1) * KHAT;  // [hi, lo]
-    static constexpr int OFF_BAR = (OFF_V + (V_LO ? 2 : 1) * VHAT + 15) / 16 * 16;
+    static constexpr int OFF_QT = OFF_V + (V_LO ? 2 : 1) * VHAT;
+    static constexpr int OFF_BAR = (OFF_QT + QT + 15) / 16 * 16;
     // barriers: full[STAGES], empty[STAGES], k_ready[2], v_ready, s_done[2], s_free (+1 spare),
     // p_ready[2], pv_done, e_ready[4], q_ready, drain; then e values [4][2] and the
     // tensor-memory address
@@ -135,11 +139,13 @@ struct TcCfg {
     // Q hi K^ lo), P [D + 2 NK, D + 4 NK) as [buffer][hi NK / 2, lo NK / 2], Q lo [D + 4 NK, D + 4 NK + D / 2)
     static constexpr int T_O = 0, T_S = D, T_P = D + 2 * NK, T_Q = D + 4 * NK;
     static constexpr int TCOLS = 512;
-    // warps 6 .. 11; 12 warps leave 168 registers a thread (an SM sub-partition holds 3 warps)
-    static constexpr int CONV_THREADS = 192;
+    // warps 6 .. 15; 16 warps leave 128 registers a thread (an SM sub-partition holds 4 warps)
+    static constexpr int CONV_THREADS = 320;
     static constexpr int THREADS = 6 * 32 + CONV_THREADS;
     static_assert(T_Q + D / 2 <= TCOLS, "tensor memory");
-    static_assert(SMEM <= 232448, "shared memory");
+    static_assert(SMEM <= BUDGET, "shared memory");
+    static_assert(M * O_ROW <= OFF_QT, "epilogue staging fits the operand memory");
+    static_assert((K_LO ? 2 : 1) * KHAT + (V_LO ? 2 : 1) * VHAT >= 4 * 32 * QT_ROW, "Q transpose blocks of the converters");
     static_assert(NK * M <= TCOLS * 128, "tiles");
 };
 
@@ -147,8 +153,10 @@ struct TcCfg {
 // 2 tiles x NSL slices x 128 bytes; lane l takes the 16 bytes at 16 l, which hold blocks 2h,
 // 2h + 1 (h = l & 1) of keys 2j, 2j + 1 (first word of each pair) and 8 + 2j, 9 + 2j (second),
 // j = (l % 8) / 2, of tile l / (8 NSL).
+// Returns 0 without the reduction when no scale needs an exponent (cmax * |d| <= 2^14 for
+// every one: the common case), so that the warp votes once instead of reducing.
 template <int NSL>
-__device__ __forceinline__ float chunk_scale_max(const uint8_t *sc, int nvalid_keys) {
+__device__ __forceinline__ float chunk_scale_max(const uint8_t *sc, int nvalid_keys, float cmax) {
     constexpr int NG = 2 * NSL * kScaleTile / 16;
     const int lane = threadIdx.x & 31;
     uint32_t m = 0u;  // packed |f16| pair
@@ -165,9 +173,11 @@ __device__ __forceinline__ float chunk_scale_max(const uint8_t *sc, int nvalid_k
         const __half2 b = __hmax2(__habs2(u32_as_h2(w.z)), __habs2(u32_as_h2(w.w)));
         m = h2_as_u32(__hmax2(a, b));
     }
+    float2 f = __half22float2(u32_as_h2(m));
+    if (!__any_sync(0xffffffffu, cmax * fmaxf(f.x, f.y) > 16384.f)) return 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = h2_as_u32(__hmax2(u32_as_h2(m), u32_as_h2(__shfl_xor_sync(0xffffffffu, m, o))));
-    const float2 f = __half22float2(u32_as_h2(m));
+    f = __half22float2(u32_as_h2(m));
     return fmaxf(f.x, f.y);
 }
 
@@ -209,7 +219,7 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
         mbar_init(s_free, 4);
         mbar_init(v_ready, 1);
         mbar_init(pv_done, 1);
-        mbar_init(q_ready, 4);
+        mbar_init(q_ready, 8);
         mbar_init(drain, 1);
         for (int i = 0; i < 4; ++i) mbar_init(e_ready + i, 1);
         fence_mbar_init();
@@ -253,6 +263,67 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
     auto khat = [&](int buf, int lo) { return smem + C::OFF_K + (buf * (C::K_LO ? 2 : 1) + lo) * C::KHAT; };
     auto vhat = [&](int lo) { return smem + C::OFF_V + lo * C::VHAT; };
     constexpr uint32_t IDESC_S = tc_idesc(M, NK), IDESC_S2 = tc_idesc(M, C::K_LO ? 2 * NK : NK), IDESC_O = tc_idesc(M, D);
+
+    // Q: scaled to log2 units, hi into shared memory (A of S), lo into tensor memory.  Two
+    // warps share the 32 rows of each tensor-memory lane quarter (a softmax warp takes the
+    // first half of the values, a converter warp the second).  A warp loads its rows with
+    // coalesced 16-byte requests (one covers 4 rows x 32 values), writes hi straight to the
+    // operand and lo through a padded row-major block `qt`, from which every lane takes its
+    // own row for the tensor-memory store.
+    auto stage_q = [&](int quarter, int d_begin, int d_end, uint8_t *qt) {
+        const int R0 = 32 * quarter;
+        const uint32_t trow = tbase + (static_cast<uint32_t>(R0) << 16);
+        const float sl = p.scale_log2;
+        // the rows of this lane's requests, R0 + 4i + lane / 8: row = G qi + g of the KV head is
+        // query head h G + g of draft position qi
+        const float4 *qsrc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int row = R0 + 4 * i + (lane >> 3);
+            const size_t qrow = (static_cast<size_t>(bseq) * n_q + row / p.G) * p.Hq + static_cast<size_t>(h) * p.G + row % p.G;
+            qsrc[i] = row < R ? reinterpret_cast<const float4 *>(p.q + qrow * D) + (lane & 7) : nullptr;
+        }
+        // loads of the next 32 values are in flight while this block is converted
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = qsrc[i] ? __ldg(qsrc[i] + d_begin / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int kb0 = d_begin; kb0 < d_end; kb0 += 32) {
+            float4 nv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                nv[i] = (qsrc[i] && kb0 + 32 < d_end) ? __ldg(qsrc[i] + (kb0 + 32) / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 x = v[i];
+                const int row = R0 + 4 * i + (lane >> 3), dim = kb0 + 4 * (lane & 7);
+                uint32_t h0, h1, l0, l1;
+                split_hi_lo(x.x * sl, x.y * sl, h0, l0);
+                split_hi_lo(x.z * sl, x.w * sl, h1, l1);
+                *reinterpret_cast<uint2 *>(qhi + kmaj(row, dim, D)) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(qt + (4 * i + (lane >> 3)) * C::QT_ROW + 8 * (lane & 7)) = make_uint2(l0, l1);
+            }
+            __syncwarp();
+            uint32_t lo32[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(qt + lane * C::QT_ROW + 16 * j);
+                lo32[4 * j] = w.x;
+                lo32[4 * j + 1] = w.y;
+                lo32[4 * j + 2] = w.z;
+                lo32[4 * j + 3] = w.w;
+            }
+            __syncwarp();
+            tc_st16(trow + C::T_Q + kb0 / 2, lo32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = nv[i];
+        }
+        tc_wait_st();
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready);
+    };
 
     if (warp == 0) {
         // ---------------- producer: one ring stage = one chunk (two tiles) ----------------
@@ -299,14 +370,15 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
                 if (!mbar_wait(k_ready + kb, (c >> 1) & 1, limit)) return false;
                 if (c >= 1 && !mbar_wait(s_free, (c - 1) & 1, limit)) return false;
                 tc_fence_after();
-                const uint32_t d = tbase + C::T_S;
-                const uint32_t qa = smem_u32(qhi), kh = smem_u32(khat(kb, 0));
-#pragma unroll 1
+                // descriptors built once; a 16-dim step moves the start address by 256 bytes,
+                // i.e. 16 in the descriptor's address field (the issue loop is the bottleneck
+                // of small-N instructions, so it does no more than add and issue)
+                const uint32_t d = tbase + C::T_S, tq = tbase + C::T_Q;
+                const uint64_t a0 = tc_desc(smem_u32(qhi), 128, D * 16), b0 = tc_desc(smem_u32(khat(kb, 0)), 128, D * 16);
+#pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t a = tc_desc(qa + ks * 256, 128, D * 16);
-                    const uint64_t bh = tc_desc(kh + ks * 256, 128, D * 16);
-                    tc_mma_ss(d, a, bh, IDESC_S2, ks > 0);
-                    tc_mma_ts(d, tbase + C::T_Q + ks * 8, bh, IDESC_S, 1);
+                    tc_mma_ss(d, a0 + 16 * ks, b0 + 16 * ks, IDESC_S2, ks > 0 ? 1 : 0);
+                    tc_mma_ts(d, tq + ks * 8, b0 + 16 * ks, IDESC_S, 1);
                 }
                 tc_commit(s_done + kb);
                 return true;
@@ -324,14 +396,14 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
                     break;
                 }
                 tc_fence_after();
-                const uint32_t vh = smem_u32(vhat(0)), vl = smem_u32(vhat(C::V_LO ? 1 : 0));
+                const uint64_t vh0 = tc_desc(smem_u32(vhat(0)), 128, NK * 16);
+                const uint64_t vl0 = tc_desc(smem_u32(vhat(C::V_LO ? 1 : 0)), 128, NK * 16);
 #pragma unroll
                 for (int kk = 0; kk < NK / 16; ++kk) {
                     const uint32_t ph = tbase + C::T_P + pb * NK + kk * 8, pl = ph + NK / 2;
-                    const uint64_t bh = tc_desc(vh + kk * 256, 128, NK * 16);
-                    tc_mma_ts(tbase + C::T_O, ph, bh, IDESC_O, (c > 0 || kk > 0) ? 1 : 0);
-                    if constexpr (C::V_LO) tc_mma_ts(tbase + C::T_O, ph, tc_desc(vl + kk * 256, 128, NK * 16), IDESC_O, 1);
-                    tc_mma_ts(tbase + C::T_O, pl, bh, IDESC_O, 1);
+                    tc_mma_ts(tbase + C::T_O, ph, vh0 + 16 * kk, IDESC_O, (c > 0 || kk > 0) ? 1 : 0);
+                    if constexpr (C::V_LO) tc_mma_ts(tbase + C::T_O, ph, vl0 + 16 * kk, IDESC_O, 1);
+                    tc_mma_ts(tbase + C::T_O, pl, vh0 + 16 * kk, IDESC_O, 1);
                 }
                 tc_commit(pv_done);
             }
@@ -379,10 +451,10 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
             if (c >= 2) okc = mbar_wait(s_done + kb, ((c >> 1) - 1) & 1, limit) && okc;
             // the chunk's exponents (largest scale of its valid keys), found by every converter
             // warp on its own
-            float mk = 0.f, mv = 0.f;
-            if constexpr (KT != KVQ_F16) mk = chunk_scale_max<NS>(kss, nvalid);
-            if constexpr (VT != KVQ_F16) mv = chunk_scale_max<NS>(vss, nvalid);
             constexpr float cmaxk = KT == KVQ_Q8_0 ? 127.f : 8.f, cmaxv = VT == KVQ_Q8_0 ? 127.f : 8.f;
+            float mk = 0.f, mv = 0.f;
+            if constexpr (KT != KVQ_F16) mk = chunk_scale_max<NS>(kss, nvalid, cmaxk);
+            if constexpr (VT != KVQ_F16) mv = chunk_scale_max<NS>(vss, nvalid, cmaxv);
             const int ek = chunk_exp(cmaxk * mk), ev = chunk_exp(cmaxv * mv);
             const __half2 fk = __float2half2_rn(pow2i(-ek));
             if (ct == 0) {
@@ -591,6 +663,10 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
             return okc;
         };
 
+        // warps 6 .. 9 (lane quarters 2, 3, 0, 1) stage the second half of Q first; their
+        // transpose blocks sit in K^ buffer 1 and V^, which no conversion writes before the
+        // first chunk's K^ is complete (every converter passes its closing barrier)
+        if (cw < 4) stage_q(warp & 3, D / 2, D, smem + C::OFF_K + (C::K_LO ? 2 : 1) * C::KHAT + cw * 32 * C::QT_ROW);
         bool ok = true;
         if (NC > 0) ok = convert_k(0);
         for (int c = 0; c < NC; ++c) {
@@ -609,39 +685,7 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
         const bool rv = r < R;
         const int qi = rv ? r / p.G : 0;       // draft query of the row
         const int lim = L - n_q + qi;          // last position the row attends to
-        // Q row: scaled to log2 units, hi into shared memory (A of S), lo into tensor memory.
-        // 64 values (16 loads of 16 bytes) are in flight at a time: the rows are strided, so
-        // the loads are latency-bound and want as many outstanding as the registers allow.
-        {
-            const float4 *q4 = reinterpret_cast<const float4 *>(p.q + rmap.out_row(prow0 + (rv ? r : 0)) * D);
-            const float sl = p.scale_log2;
-#pragma unroll 1
-            for (int k0 = 0; k0 < D; k0 += 64) {
-                float4 v[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) v[u] = rv ? __ldg(q4 + k0 / 4 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t lo32[16];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 a = v[hf * 8 + 2 * e], b = v[hf * 8 + 2 * e + 1];
-                        uint32_t hw[4];
-                        split_hi_lo(a.x * sl, a.y * sl, hw[0], lo32[4 * e]);
-                        split_hi_lo(a.z * sl, a.w * sl, hw[1], lo32[4 * e + 1]);
-                        split_hi_lo(b.x * sl, b.y * sl, hw[2], lo32[4 * e + 2]);
-                        split_hi_lo(b.z * sl, b.w * sl, hw[3], lo32[4 * e + 3]);
-                        *reinterpret_cast<uint4 *>(qhi + kmaj(r, k0 + 32 * hf + 8 * e, D)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    }
-                    tc_st16(trow + C::T_Q + (k0 + 32 * hf) / 2, lo32);
-                }
-            }
-            tc_wait_st();
-            fence_async_smem();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(q_ready);
+        stage_q(quarter, 0, D / 2, smem + C::OFF_QT + quarter * 32 * C::QT_ROW);
         float m_run = -CUDART_INF_F, l_acc = 0.f;
         bool ok = true;
         for (int c = 0; c < NC; ++c) {
@@ -650,31 +694,34 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
             okc = mbar_wait(e_ready + (c & 3), (c >> 2) & 1, limit) && okc;
             okc = __all_sync(0xffffffffu, okc);
             tc_fence_after();
-            uint32_t sraw[32];
-            tc_ld32(trow + C::T_S, sraw);
-            if constexpr (C::K_LO) {  // S = (Q hi K^ hi + Q lo K^ hi) + Q hi K^ lo
-                uint32_t slo[32];
-                tc_ld32(trow + C::T_S + NK, slo);
-                tc_wait_ld();
-#pragma unroll
-                for (int jk = 0; jk < 32; ++jk) sraw[jk] = __float_as_uint(__uint_as_float(sraw[jk]) + __uint_as_float(slo[jk]));
-            } else {
-                tc_wait_ld();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);  // the S columns may take the next chunk
             const int ek = e_val[(c & 3) * 2], ev = e_val[(c & 3) * 2 + 1];
             const float fk = pow2i(ek), fv = pow2i(ev);
             const int key0 = (t_begin + 2 * c) * kTileRows;
             float s[32], mx = -CUDART_INF_F;
 #pragma unroll
-            for (int jk = 0; jk < 32; ++jk) {
-                const int key = key0 + jk;
-                const bool valid = rv && key < key_end && key <= lim;
-                s[jk] = valid ? __uint_as_float(sraw[jk]) * fk : -CUDART_INF_F;
-                mx = fmaxf(mx, s[jk]);
+            for (int h2 = 0; h2 < 2; ++h2) {  // 16 keys at a time
+                uint32_t a[16];
+                tc_ld16(trow + C::T_S + 16 * h2, a);
+                if constexpr (C::K_LO) {  // S = (Q hi K^ hi + Q lo K^ hi) + Q hi K^ lo
+                    uint32_t b[16];
+                    tc_ld16(trow + C::T_S + NK + 16 * h2, b);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(b[j]));
+                } else {
+                    tc_wait_ld();
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int key = key0 + 16 * h2 + j;
+                    const bool valid = rv && key < key_end && key <= lim;
+                    s[16 * h2 + j] = valid ? __uint_as_float(a[j]) * fk : -CUDART_INF_F;
+                    mx = fmaxf(mx, s[16 * h2 + j]);
+                }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);  // the S columns may take the next chunk
             // lazy rescale: only when the row maximum grows by more than 2^6 (p * 2^e_v stays
             // below 2^15 in f16); O is rescaled in tensor memory once the previous PV is done
             const bool need = mx > m_run + 6.f;
@@ -723,18 +770,32 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
             atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
             s_timeout = 1;
         }
-        for (int k0 = 0; k0 < D; k0 += 32) {
-            uint32_t o[32];
-            tc_ld32(trow + C::T_O + k0, o);
-            tc_wait_ld();
-            if (rv) {
-                const size_t pr = (prow0 + r) * p.part_stride + p.part_base + split;
-                float4 *dst = reinterpret_cast<float4 *>(p.part_o + pr * D + k0);
+        // O leaves through shared memory: each thread writes its row (the operands are no
+        // longer read: every MMA has completed), then the warp stores its 32 rows with
+        // coalesced 16-byte writes, half a row per request.
+        {
+            uint8_t *ost = smem + static_cast<size_t>(r) * C::O_ROW;
+#pragma unroll 1
+            for (int k0 = 0; k0 < D; k0 += 16) {
+                uint32_t o[16];
+                tc_ld16(trow + C::T_O + k0, o);
+                tc_wait_ld();
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    dst[u] = NC > 0 ? make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
-                                                  __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4 *>(ost + (k0 + 4 * u) * 4) =
+                        NC > 0 ? make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+            const int R0 = 32 * quarter;
+#pragma unroll 1
+            for (int i = 0; i < 32; ++i) {
+                const int row = R0 + i;
+                if (row >= R) break;
+                const size_t pr = (prow0 + row) * p.part_stride + p.part_base + split;
+                float4 *dst = reinterpret_cast<float4 *>(p.part_o + pr * D);
+                const uint8_t *srow = smem + static_cast<size_t>(row) * C::O_ROW;
+#pragma unroll
+                for (int c4 = lane; c4 < D / 4; c4 += 32) dst[c4] = *reinterpret_cast<const float4 *>(srow + 16 * c4);
             }
         }
         if (rv) {
