@@ -222,30 +222,22 @@ def launch_ctas(cell):
     return cell.splits * wl.n_kv_heads * wl.batch * ((wl.G + 7) // 8)
 
 
-STAMPS_PER_CTA = 4
+STAMPS_PER_CTA = 2
 
 
 def stamp_spans(stamps, n_launch, layers, ctas):
     """Per-launch timing from the CTA timer stamps of the last replay of each stamp graph
-    (per CTA: start, past the launch wait, triple published, exit; 0 = not reached):
-    span = last CTA exit - first CTA start (includes the overlap with the neighbouring
-    layers under programmatic dependent launch); gap = this launch's last exit - the
-    previous launch's last exit (the time a layer adds to the step); phases of a launch:
-    work = last triple published - first CTA past the wait, merge = last exit - last
-    triple published."""
+    (per CTA: start, exit): span = last CTA exit - first CTA start (includes the overlap
+    with the neighbouring layers under programmatic dependent launch); gap = this launch's
+    last exit - the previous launch's last exit (the time a layer adds to the step)."""
     st = stamps.view(n_launch, ctas, STAMPS_PER_CTA).double()
-    starts, ends = st[:, :, 0].min(dim=1).values, st[:, :, 3].max(dim=1).values
-    big = float(2 ** 62)
-    waited = st[:, :, 1].masked_fill(st[:, :, 1] == 0, big).min(dim=1).values
-    pub = st[:, :, 2].max(dim=1).values
+    starts, ends = st[:, :, 0].min(dim=1).values, st[:, :, 1].max(dim=1).values
     spans = ((ends - starts) * 1e-3).tolist()  # us
     gaps = []
     for g in range(n_launch // layers):
         e = ends[g * layers:(g + 1) * layers]
         gaps += ((e[1:] - e[:-1]) * 1e-3).tolist()
-    phases = {"work": ((pub - waited) * 1e-3).tolist(), "merge": ((ends - pub) * 1e-3).tolist(),
-              "pre_wait": ((waited - starts) * 1e-3).tolist()}
-    return spans, gaps, phases
+    return spans, gaps
 
 
 def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_event_graphs=16, n_stamp_graphs=4):
@@ -345,17 +337,13 @@ def run_cell(kvq, torch, wl, steps, warmup, peak, sampler=None, e2e=False, n_eve
     # the timed region / layers is the kernel's average in-step launch duration
     res["decode_instep_us"] = ms_step * 1e3 / L
     if n_sg:
-        spans, gaps, phases = stamp_spans(stamps, n_sg * L, L, ctas)
+        spans, gaps = stamp_spans(stamps, n_sg * L, L, ctas)
         res["stamps"] = {"span_us_mean": statistics.fmean(spans), "span_us_median": statistics.median(spans),
                          "gap_us_mean": statistics.fmean(gaps) if gaps else None,
-                         "phase_us_mean": {k: statistics.fmean(v) for k, v in phases.items()},
                          "launches": len(spans), "ms_per_step_stamp_pass": ms_stamp,
-                         "how": "%globaltimer per CTA (start, past the launch wait, triple published, exit) in "
-                                "event-free graph replays; span = first start to last exit of a launch (overlaps "
-                                "its neighbours under programmatic dependent launch), gap = last exit of a launch - "
-                                "last exit of the previous one; phases: pre_wait = first CTA past the wait - first "
-                                "start, work = last triple published - first CTA past the wait, merge = last exit "
-                                "- last triple published"}
+                         "how": "%globaltimer per CTA (start, exit) in event-free graph replays; span = first "
+                                "start to last exit of a launch (overlaps its neighbours under programmatic "
+                                "dependent launch), gap = last exit of a launch - last exit of the previous one"}
     if n_eg:
         durs = []
         for k in range(n_eg):
@@ -944,7 +932,7 @@ def main():
                                   "frac": head["decode_gbs"] / peak if head.get("decode_gbs") else None,
                                   "how": "CUDA events around every launch (event nodes serialise the launches)"},
             "stamps": head.get("stamps")}
-    if head.get("stamps"):
+    if head.get("stamps") and head["stamps"]["span_us_mean"] > 0:  # 0: the kernel wrote no stamps
         sp = head["stamps"]["span_us_mean"]
         roof["stamps"]["span_achieved"] = bpl / (sp * 1e-6) / 1e9
         roof["stamps"]["span_frac"] = roof["stamps"]["span_achieved"] / peak

@@ -150,9 +150,10 @@ typedef enum {
 
 /* Device error word bits (kvq_cache_read_error). */
 #define KVQ_DEVERR_CAPACITY 0x1 /* an append found len + n_new > capacity on the device     */
-#define KVQ_DEVERR_TIMEOUT 0x2  /* a pipeline wait in a kernel gave up after its time limit:
-                                   the outputs of that launch are undefined (the workspace
-                                   counters are still left at zero)                        */
+#define KVQ_DEVERR_TIMEOUT 0x2  /* a pipeline or merge wait in a kernel took longer than its
+                                   limit (kvq_set_wait_limit) or gave up: the outputs of that
+                                   launch are undefined (the workspace counters are still
+                                   left at zero)                                             */
 
 typedef struct {
     int32_t batch;      /* B: sequences held by the cache (>= 1)                       */
@@ -403,28 +404,30 @@ KVQ_API kvq_status kvq_select_tier(int64_t cells, int32_t n_layers, int32_t n_kv
                                    uint64_t budget_bytes, kvq_tier_choice *out);
 
 /*
- * Wait limit of the decode kernels' pipeline and merge waits, in SM clock cycles, for
- * launches enqueued after this call (process-wide).  0 restores the default (4e9 cycles,
- * about two seconds).  A wait that reaches the limit gives up: the kernel sets
- * KVQ_DEVERR_TIMEOUT in the cache's error word, publishes an empty split triple for its
- * CTA, still takes its merge arrivals and returns; the outputs of that launch are
- * undefined, and a later call on the same workspace is correct again.  The wait for the
- * kernel's own copies in flight before it reuses or releases shared memory keeps the
- * default limit.  For failure handling and its tests: a short limit makes waits give up
- * on a healthy GPU.  KVQ_ERR_INVALID_ARG for a negative value.
+ * Wait limit of the kernels' pipeline and merge waits, in SM clock cycles, for launches
+ * enqueued after this call (process-wide).  0 restores the default (4e9 cycles, about two
+ * seconds).  In the split-K decode kernels (decode, append-decode, partials, window + tail,
+ * the 8-row verify groups) a wait that takes longer than the limit sets KVQ_DEVERR_TIMEOUT
+ * in the cache's error word and goes on waiting; it gives up only at the default bound,
+ * after which its CTA publishes an empty split triple, still takes its merge arrivals and
+ * returns.  The 128-row verify tile gives up at the limit itself (its copies in flight land
+ * first).  Either way the outputs of that launch are undefined, the workspace counters end
+ * at zero and a later call on the same workspace is correct again.  For failure handling
+ * and its tests: a short limit makes the error word report slow waits on a healthy GPU.
+ * KVQ_ERR_INVALID_ARG for a negative value.
  */
 KVQ_API kvq_status kvq_set_wait_limit(int64_t cycles);
 
 /*
  * Launch timing for measurement (process-wide).  With buf non-NULL (device memory,
- * 16-byte aligned, n_slots * ctas_per_slot * 4 uint64), every decode launch enqueued
- * afterwards (decode, fused append + decode, partials, verify, window decode, no-alloc
- * decode) takes the next of n_slots slots in turn, and CTA c of the launch (linear index
- * x + X * (y + Y * z), only c < ctas_per_slot) writes the GPU's global nanosecond timer to
- * buf[slot][c][0..3]: [0] when it starts, [1] once past the wait for the previous kernel
- * of the stream (0 if it had no work), [2] once its split triple or output is written (0
- * if it had no work), [3] when it exits.  A CUDA graph keeps the slots assigned at
- * capture.  buf NULL stops the stamps.  KVQ_ERR_INVALID_ARG for bad sizes or alignment.
+ * 16-byte aligned, n_slots * ctas_per_slot * 2 uint64), every split-K decode launch
+ * enqueued afterwards (decode, fused append + decode, partials, 8-row verify groups,
+ * no-alloc decode) takes the next of n_slots slots in turn, and CTA c of the launch
+ * (linear index x + X * (y + Y * z), only c < ctas_per_slot) writes the GPU's global
+ * nanosecond timer to buf[slot][c][0] when it starts and to buf[slot][c][1] when it exits.
+ * Window + tail launches and the 128-row verify tile take a slot but write nothing.  A CUDA
+ * graph keeps the slots assigned at capture.  buf NULL stops the stamps.
+ * KVQ_ERR_INVALID_ARG for bad sizes or alignment.
  */
 KVQ_API kvq_status kvq_set_launch_stamps(void *buf, int32_t n_slots, int32_t ctas_per_slot);
 

@@ -113,7 +113,7 @@ int g_stamp_slots = 0, g_stamp_ctas = 0, g_stamp_next = 0;
 void take_stamp_slot(kvq::DecodeParams &p) {
     std::lock_guard<std::mutex> lock(g_stamp_mu);
     if (!g_stamp_buf || g_stamp_slots < 1) return;
-    p.stamps = g_stamp_buf + static_cast<size_t>(g_stamp_next) * g_stamp_ctas * 4;
+    p.stamps = g_stamp_buf + static_cast<size_t>(g_stamp_next) * g_stamp_ctas * 2;
     p.stamp_ctas = g_stamp_ctas;
     g_stamp_next = (g_stamp_next + 1) % g_stamp_slots;
 }

@@ -117,24 +117,19 @@ __device__ __forceinline__ int group_size(int ns) {
     return g;
 }
 
-// gpu-scope acquire-release fence.  After a CTA barrier, one thread's fence is cumulative
-// over the writes of the whole CTA (they happen before it through the barrier), so a CTA
-// publishes its results with one fence in thread 0 rather than one per thread.
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;\n" ::: "memory"); }
-
 // All threads of the CTA call this after writing their results.  Returns true in the
 // CTA that is the target-th to arrive on *counter (it then sees every earlier write).
 __device__ __forceinline__ bool arrive_last(int32_t *counter, int target, int &s_flag) {
+    __threadfence();  // each thread publishes its own writes
     __syncthreads();
     if (threadIdx.x == 0) {
-        fence_acq_rel_gpu();  // release this CTA's writes
         const int t = atomicAdd(counter, 1);
-        const bool last = t == target - 1;
-        if (last) fence_acq_rel_gpu();  // acquire the others'
-        s_flag = last;
+        s_flag = (t == target - 1);
     }
     __syncthreads();
-    return s_flag != 0;
+    const bool last = s_flag != 0;
+    if (last) __threadfence();
+    return last;
 }
 
 // Query row (index into q, out, lse) of internal row `pr` (partial-triple row space, where
@@ -265,7 +260,7 @@ __device__ void merge_rows(const float *po, const float *pm, const float *pl, in
 // shared memory.  Memory for the reduction: 24 bytes per thread at `red`.
 constexpr int kWideMinBytes = kDirectMergeBytes;  // smaller row groups merge in one CTA
 constexpr int kWideBytes = 24 * 1024;     // triple bytes per merging CTA
-constexpr int kWideChunk = 10;
+constexpr int kWideChunk = 8;
 __device__ void merge_cols(const float *po, const float *pm, const float *pl, int stride, int NP, size_t row0,
                            int D, int c0, int c1, float *out, float *lse, const RowMap map, const float *ext_out,
                            const float *ext_lse, uint8_t *red) {
@@ -361,16 +356,16 @@ __device__ void merge_cols(const float *po, const float *pm, const float *pl, in
     }
 }
 
-// Bounded wait (thread 0) until the first-arrival count (low 16 bits) of *counter reaches
-// target; false after `limit` SM clock cycles.
+// Wait (thread 0) until the first-arrival count (low 16 bits) of *counter reaches target:
+// 0 within `report` SM cycles, 1 later (reported), 2 not within kWaitCycles (gave up).
 constexpr int kSecondArrival = 1 << 16;
-__device__ __forceinline__ bool wait_count(const int32_t *counter, int target, long long limit) {
+__device__ __forceinline__ int wait_count(const int32_t *counter, int target, long long report) {
     const long long t0 = clock64();
     while (true) {
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(counter) : "memory");
-        if ((v & 0xffff) >= target) return true;
-        if (clock64() - t0 > limit) return false;
+        if ((v & 0xffff) >= target) return clock64() - t0 > report ? 1 : 0;
+        if (clock64() - t0 > kWaitCycles) return 2;
         __nanosleep(64);
     }
 }
@@ -440,46 +435,36 @@ struct QFrag {
     uint32_t a[4];
 };
 
-// Scores of NT consecutive tiles of a stage over this warp's 128-value slice: tile t's
-// codes at kc + t * KCB, its scales at ks + t * KSB; s[t] = scores of keys A=2j, B=2j+1
-// (S-tile 0) and C=8+2j, D=9+2j (S-tile 1), row g = lane/4, in log2 units (Q was
-// prescaled).  The loop over 32-value blocks is outermost, so each Q fragment is read from
-// shared memory once for all NT tiles.
-template <int KT, int NT, int KCB, int KSB>
+// Scores of one tile over this warp's 128-value slice for keys A=2j, B=2j+1 (S-tile 0) and
+// C=8+2j, D=9+2j (S-tile 1), row g = lane/4, in log2 units (Q was prescaled).
+template <int KT>
 __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks, const uint8_t *qsm,
-                                            const uint8_t *kcor, int lane, int j, float (&s)[NT][4]) {
+                                            const uint8_t *kcor, int lane, int j, float (&s)[4]) {
     // Q fragment of chunk c (16 values), read from shared memory where it is used
     auto qa = [&](int c) {
         const uint4 v = lds128(qsm + (c * 32 + lane) * 16);
         return QFrag{{v.x, v.y, v.z, v.w}};
     };
     if constexpr (KT == KVQ_F16) {
-        float acc[NT][2][4];
+        float acc[2][4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const QFrag q0 = qa(2 * b), q1 = qa(2 * b + 1);
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const uint4 w0 = lds128(kc + t * KCB + (2 * b + 0) * 512 + lane * 16);
-                const uint4 w1 = lds128(kc + t * KCB + (2 * b + 1) * 512 + lane * 16);
-                if (b == 0) {
-                    mma_16816_z(acc[t][0], q0.a, w0.x, w0.y);
-                    mma_16816_z(acc[t][1], q0.a, w1.x, w1.y);
-                } else {
-                    mma_16816(acc[t][0], q0.a, w0.x, w0.y);
-                    mma_16816(acc[t][1], q0.a, w1.x, w1.y);
-                }
-                mma_16816(acc[t][0], q1.a, w0.z, w0.w);
-                mma_16816(acc[t][1], q1.a, w1.z, w1.w);
+            const uint4 w0 = lds128(kc + (2 * b + 0) * 512 + lane * 16);
+            const uint4 w1 = lds128(kc + (2 * b + 1) * 512 + lane * 16);
+            if (b == 0) {
+                mma_16816_z(acc[0], qa(0).a, w0.x, w0.y);
+                mma_16816_z(acc[1], qa(0).a, w1.x, w1.y);
+            } else {
+                mma_16816(acc[0], qa(2 * b).a, w0.x, w0.y);
+                mma_16816(acc[1], qa(2 * b).a, w1.x, w1.y);
             }
+            mma_16816(acc[0], qa(2 * b + 1).a, w0.z, w0.w);
+            mma_16816(acc[1], qa(2 * b + 1).a, w1.z, w1.w);
         }
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            s[t][0] = acc[t][0][0] + acc[t][0][2];
-            s[t][1] = acc[t][0][1] + acc[t][0][3];
-            s[t][2] = acc[t][1][0] + acc[t][1][2];
-            s[t][3] = acc[t][1][1] + acc[t][1][3];
-        }
+        s[0] = acc[0][0] + acc[0][2];
+        s[1] = acc[0][1] + acc[0][3];
+        s[2] = acc[1][0] + acc[1][2];
+        s[3] = acc[1][1] + acc[1][3];
     } else {
         // accumulators hold sum q * code in units of 2^-24 (q8_0, q5_0, q5_1) or, with the
         // low-nibble chunk of Q prescaled by 16, sum q * c in units of 2^-20 (q4_0, q4_1).
@@ -493,101 +478,78 @@ __device__ __forceinline__ void tile_scores(const uint8_t *kc, const uint8_t *ks
             kcorr[2] = kc4.z;
             kcorr[3] = kc4.w;
         }
-        float2 s01[NT], s23[NT];
-        uint4 wq4[NT], scw[NT];
-        uint32_t hb[NT];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            s01[t] = make_float2(0.f, 0.f);
-            s23[t] = make_float2(0.f, 0.f);
-            wq4[t] = make_uint4(0, 0, 0, 0);
-            scw[t] = make_uint4(0, 0, 0, 0);
-            hb[t] = 0;
-        }
+        const uint4 sc0 = lds128(ks + j * 32), sc1 = lds128(ks + j * 32 + 16);
+        const uint32_t kscale[4][2] = {{sc0.x, sc0.y}, {sc0.z, sc0.w}, {sc1.x, sc1.y}, {sc1.z, sc1.w}};
+        float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+        uint4 wq4 = make_uint4(0, 0, 0, 0);
+        uint32_t hb = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const QFrag q0 = qa(2 * b), q1 = qa(2 * b + 1);
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const uint8_t *kct = kc + t * KCB;
-                const uint8_t *kst = ks + t * KSB;
-                float acc[2][4];
-                if constexpr (KT == KVQ_Q8_0) {
-                    const uint4 w = lds128(kct + b * 512 + lane * 16);
-                    mma_16816_z(acc[0], q0.a, q8_02(w.x), q8_13(w.x));
-                    mma_16816(acc[0], q1.a, q8_02(w.y), q8_13(w.y));
-                    mma_16816_z(acc[1], q0.a, q8_02(w.z), q8_13(w.z));
-                    mma_16816(acc[1], q1.a, q8_02(w.w), q8_13(w.w));
-                } else if constexpr (!has_fifth_bit(KT)) {
-                    if ((b & 1) == 0) wq4[t] = lds128(kct + (b >> 1) * 512 + lane * 16);
-                    const uint32_t w0 = (b & 1) ? wq4[t].z : wq4[t].x, w0s = w0 >> 8;
-                    const uint32_t w1 = (b & 1) ? wq4[t].w : wq4[t].y, w1s = w1 >> 8;
-                    mma_16816_z(acc[0], q0.a, w0 & kNibLo, w0s & kNibLo);
-                    mma_16816(acc[0], q1.a, w0 & kNibHi, w0s & kNibHi);
-                    mma_16816_z(acc[1], q0.a, w1 & kNibLo, w1s & kNibLo);
-                    mma_16816(acc[1], q1.a, w1 & kNibHi, w1s & kNibHi);
-                } else {
-                    if ((b & 1) == 0) {
-                        wq4[t] = lds128(kct + (b >> 1) * 512 + lane * 16);
-                        hb[t] = *reinterpret_cast<const uint32_t *>(kct + kNibbleBytes + (b >> 1) * 128 + lane * 4);
-                    }
-                    const int wi0 = 2 * (b & 1), wi1 = wi0 + 1;
-                    uint32_t c0[4], c1[4];
-                    fifth_bit_codes((b & 1) ? wq4[t].z : wq4[t].x, hb[t] >> wi0, c0);
-                    fifth_bit_codes((b & 1) ? wq4[t].w : wq4[t].y, hb[t] >> wi1, c1);
-                    mma_16816_z(acc[0], q0.a, c0[0], c0[1]);
-                    mma_16816(acc[0], q1.a, c0[2], c0[3]);
-                    mma_16816_z(acc[1], q0.a, c1[0], c1[1]);
-                    mma_16816(acc[1], q1.a, c1[2], c1[3]);
+            float acc[2][4];
+            if constexpr (KT == KVQ_Q8_0) {
+                const uint4 w = lds128(kc + b * 512 + lane * 16);
+                mma_16816_z(acc[0], qa(2 * b).a, q8_02(w.x), q8_13(w.x));
+                mma_16816(acc[0], qa(2 * b + 1).a, q8_02(w.y), q8_13(w.y));
+                mma_16816_z(acc[1], qa(2 * b).a, q8_02(w.z), q8_13(w.z));
+                mma_16816(acc[1], qa(2 * b + 1).a, q8_02(w.w), q8_13(w.w));
+            } else if constexpr (!has_fifth_bit(KT)) {
+                if ((b & 1) == 0) wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
+                const uint32_t w0 = (b & 1) ? wq4.z : wq4.x, w0s = w0 >> 8;
+                const uint32_t w1 = (b & 1) ? wq4.w : wq4.y, w1s = w1 >> 8;
+                mma_16816_z(acc[0], qa(2 * b).a, w0 & kNibLo, w0s & kNibLo);
+                mma_16816(acc[0], qa(2 * b + 1).a, w0 & kNibHi, w0s & kNibHi);
+                mma_16816_z(acc[1], qa(2 * b).a, w1 & kNibLo, w1s & kNibLo);
+                mma_16816(acc[1], qa(2 * b + 1).a, w1 & kNibHi, w1s & kNibHi);
+            } else {
+                if ((b & 1) == 0) {
+                    wq4 = lds128(kc + (b >> 1) * 512 + lane * 16);
+                    hb = *reinterpret_cast<const uint32_t *>(kc + kNibbleBytes + (b >> 1) * 128 + lane * 4);
                 }
-                // the scales of block b: keys (A,B) and (C,D) of this lane's pair j (one
-                // 16-byte load holds blocks b and b + 1)
-                if ((b & 1) == 0) scw[t] = lds128(kst + j * 32 + (b >> 1) * 16);
-                const float2 dab = __half22float2(u32_as_h2((b & 1) ? scw[t].z : scw[t].x));
-                const float2 dcd = __half22float2(u32_as_h2((b & 1) ? scw[t].w : scw[t].y));
-                float2 t01 = add2(make_float2(acc[0][0], acc[0][1]), make_float2(acc[0][2], acc[0][3]));
-                float2 t23 = add2(make_float2(acc[1][0], acc[1][1]), make_float2(acc[1][2], acc[1][3]));
-                if constexpr (KT == KVQ_Q4_0 || KT == KVQ_Q5_0) {
-                    const float2 cb = make_float2(kcorr[b], kcorr[b]);
-                    t01 = add2(t01, cb);
-                    t23 = add2(t23, cb);
-                }
-                s01[t] = fma2(dab, t01, s01[t]);
-                s23[t] = fma2(dcd, t23, s23[t]);
-                if constexpr (has_min(KT)) {  // + lo * sum_b q
-                    const uint2 lsc = *reinterpret_cast<const uint2 *>(kst + kScaleTile + j * 32 + b * 8);
-                    const float2 cb = make_float2(kcorr[b], kcorr[b]);
-                    s01[t] = fma2(__half22float2(u32_as_h2(lsc.x)), cb, s01[t]);
-                    s23[t] = fma2(__half22float2(u32_as_h2(lsc.y)), cb, s23[t]);
-                }
+                const int wi0 = 2 * (b & 1), wi1 = wi0 + 1;
+                uint32_t c0[4], c1[4];
+                fifth_bit_codes((b & 1) ? wq4.z : wq4.x, hb >> wi0, c0);
+                fifth_bit_codes((b & 1) ? wq4.w : wq4.y, hb >> wi1, c1);
+                mma_16816_z(acc[0], qa(2 * b).a, c0[0], c0[1]);
+                mma_16816(acc[0], qa(2 * b + 1).a, c0[2], c0[3]);
+                mma_16816_z(acc[1], qa(2 * b).a, c1[0], c1[1]);
+                mma_16816(acc[1], qa(2 * b + 1).a, c1[2], c1[3]);
+            }
+            const float2 dab = __half22float2(u32_as_h2(kscale[b][0]));
+            const float2 dcd = __half22float2(u32_as_h2(kscale[b][1]));
+            float2 t01 = add2(make_float2(acc[0][0], acc[0][1]), make_float2(acc[0][2], acc[0][3]));
+            float2 t23 = add2(make_float2(acc[1][0], acc[1][1]), make_float2(acc[1][2], acc[1][3]));
+            if constexpr (KT == KVQ_Q4_0 || KT == KVQ_Q5_0) {
+                const float2 cb = make_float2(kcorr[b], kcorr[b]);
+                t01 = add2(t01, cb);
+                t23 = add2(t23, cb);
+            }
+            s01 = fma2(dab, t01, s01);
+            s23 = fma2(dcd, t23, s23);
+            if constexpr (has_min(KT)) {  // + lo * sum_b q
+                const uint2 lsc = *reinterpret_cast<const uint2 *>(ks + kScaleTile + j * 32 + b * 8);
+                const float2 cb = make_float2(kcorr[b], kcorr[b]);
+                s01 = fma2(__half22float2(u32_as_h2(lsc.x)), cb, s01);
+                s23 = fma2(__half22float2(u32_as_h2(lsc.y)), cb, s23);
             }
         }
         constexpr float unit = (KT == KVQ_Q4_0 || KT == KVQ_Q4_1) ? kTwo20 : kTwo24;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            s[t][0] = s01[t].x * unit;
-            s[t][1] = s01[t].y * unit;
-            s[t][2] = s23[t].x * unit;
-            s[t][3] = s23[t].y * unit;
-        }
+        s[0] = s01.x * unit;
+        s[1] = s01.y * unit;
+        s[2] = s23.x * unit;
+        s[3] = s23.y * unit;
     }
 }
 
-// O^T += V^T P^T for one tile over this warp's slice.  pk: probabilities of keys A,B,C,D
-// of row g; vmask: which of A,B,C,D are inside the sequence (rows past the length may hold
-// any bits).  The product is taken transposed: an mma's M rows are 16 values of the slice
-// (two of the fragment-native 8-value groups), N the 8 query rows, K the 16 keys, so the
-// hi and lo parts of P are two K steps into one accumulator and o holds 8 m-tiles x 4
-// (32 registers).  Lane (g, j) of m-tile mt = 2b + h holds rows 2j, 2j+1 of the values
-// 32b + 16h + 4(g/2) + 2(g%2) (c0, c1) and that value + 1 (c2, c3).
+// O += P V for one tile over this warp's slice.  pk: probabilities of keys A,B,C,D of row g;
+// vmask: which of A,B,C,D are inside the sequence (rows past the length may hold any bits).
 template <int VT, bool PARTIAL>
 __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, const float (&pk)[4],
-                                        const bool (&vmask)[4], int lane, int j, float (&o)[8][4],
+                                        const bool (&vmask)[4], int lane, int j, float (&o)[16][4],
                                         uint32_t magic, float (&corr)[4]) {
     if constexpr (VT == KVQ_F16) {
-        uint32_t hab, lab, hcd, lcd;
-        split_hi_lo(pk[0], pk[1], hab, lab);
-        split_hi_lo(pk[2], pk[3], hcd, lcd);
+        uint32_t a[4];
+        split_hi_lo(pk[0], pk[1], a[0], a[1]);
+        split_hi_lo(pk[2], pk[3], a[2], a[3]);
         const uint32_t mab = (vmask[0] ? 0x0000ffffu : 0u) | (vmask[1] ? 0xffff0000u : 0u);
         const uint32_t mcd = (vmask[2] ? 0x0000ffffu : 0u) | (vmask[3] ? 0xffff0000u : 0u);
 #pragma unroll
@@ -604,19 +566,17 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
                 w1.z &= mab;
                 w1.w &= mcd;
             }
-            const uint32_t a0[4] = {w0.x, w0.z, w0.y, w0.w};
-            const uint32_t a1[4] = {w1.x, w1.z, w1.y, w1.w};
-            mma_16816(o[2 * b], a0, hab, hcd);
-            mma_16816(o[2 * b], a0, lab, lcd);
-            mma_16816(o[2 * b + 1], a1, hab, hcd);
-            mma_16816(o[2 * b + 1], a1, lab, lcd);
+            mma_16816(o[4 * b + 0], a, w0.x, w0.y);
+            mma_16816(o[4 * b + 1], a, w0.z, w0.w);
+            mma_16816(o[4 * b + 2], a, w1.x, w1.y);
+            mma_16816(o[4 * b + 3], a, w1.z, w1.w);
         }
     } else {
         // P' = p x scale per (key, block) as f16 hi + lo: p is split once per tile
         // (p = ph + pl), then per block  hi = ph*d,  err = fma(ph, d, -hi) (exact: the
         // rounding error of an f16 product), lo = fma(pl, d, err)  -- three packed f16 ops
         // per key pair, about 2^-21 relative.  The scale half2 words already pair keys
-        // (A,B) and (C,D), matching the B-fragment pairs.
+        // (A,B) and (C,D), matching the A-fragment pairs.
         uint32_t ph_ab, pl_ab, ph_cd, pl_cd;
         split_hi_lo(pk[0], pk[1], ph_ab, pl_ab);
         split_hi_lo(pk[2], pk[3], ph_cd, pl_cd);
@@ -637,23 +597,20 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
             const __half2 hcd = __hmul2(u32_as_h2(ph_cd), dcd);
             const __half2 eab = __hfma2(u32_as_h2(ph_ab), dab, __hneg2(hab));
             const __half2 ecd = __hfma2(u32_as_h2(ph_cd), dcd, __hneg2(hcd));
-            const uint32_t bh0 = h2_as_u32(hab), bh1 = h2_as_u32(hcd);
-            const uint32_t bl0 = h2_as_u32(__hfma2(u32_as_h2(pl_ab), dab, eab));
-            const uint32_t bl1 = h2_as_u32(__hfma2(u32_as_h2(pl_cd), dcd, ecd));
+            uint32_t a[4];
+            a[0] = h2_as_u32(hab);
+            a[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), dab, eab));
+            a[2] = h2_as_u32(hcd);
+            a[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), dcd, ecd));
             // q8_0: o accumulates sum P' * q in units of 2^-24; nibble types: exact f16 code
             // values by the magic-number route (nibble | 0x6400 is 1024 + c; a high nibble
             // gives 1024 + 16c, scaled by 1/16), less the offset (8 for q4_0, 16 for q5_0)
-            uint32_t a0[4], a1[4];
             if constexpr (VT == KVQ_Q8_0) {
                 const uint4 w = lds128(vc + b * 512 + lane * 16);
-                a0[0] = q8_02(w.x);
-                a0[1] = q8_02(w.y);
-                a0[2] = q8_13(w.x);
-                a0[3] = q8_13(w.y);
-                a1[0] = q8_02(w.z);
-                a1[1] = q8_02(w.w);
-                a1[2] = q8_13(w.z);
-                a1[3] = q8_13(w.w);
+                mma_16816(o[4 * b + 0], a, q8_02(w.x), q8_13(w.x));
+                mma_16816(o[4 * b + 1], a, q8_02(w.y), q8_13(w.y));
+                mma_16816(o[4 * b + 2], a, q8_02(w.z), q8_13(w.z));
+                mma_16816(o[4 * b + 3], a, q8_02(w.w), q8_13(w.w));
             } else if constexpr (!has_fifth_bit(VT)) {
                 if ((b & 1) == 0) wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
                 const uint32_t wq0 = (b & 1) ? wq4.z : wq4.x, wq0s = wq0 >> 8;  // bytes 2n'   of the block
@@ -663,14 +620,10 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
                               khi = __float2half2_rn(-64.0f - off);
                 auto lo = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2((x & kNibLo) | magic), klo)); };
                 auto hi = [&](uint32_t x) { return h2_as_u32(__hfma2(u32_as_h2((x & kNibHi) | magic), k16th, khi)); };
-                a0[0] = lo(wq0);
-                a0[1] = lo(wq1);
-                a0[2] = lo(wq0s);
-                a0[3] = lo(wq1s);
-                a1[0] = hi(wq0);
-                a1[1] = hi(wq1);
-                a1[2] = hi(wq0s);
-                a1[3] = hi(wq1s);
+                mma_16816(o[4 * b + 0], a, lo(wq0), lo(wq0s));
+                mma_16816(o[4 * b + 2], a, hi(wq0), hi(wq0s));
+                mma_16816(o[4 * b + 1], a, lo(wq1), lo(wq1s));
+                mma_16816(o[4 * b + 3], a, hi(wq1), hi(wq1s));
             } else {
                 if ((b & 1) == 0) {
                     wq4 = lds128(vc + (b >> 1) * 512 + lane * 16);
@@ -681,23 +634,14 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
                 fifth_bit_codes((b & 1) ? wq4.w : wq4.y, hb >> (2 * (b & 1) + 1), c1);
                 const __half2 koff = __float2half2_rn(VT == KVQ_Q5_0 ? 1040.0f : 1024.0f);
                 auto val = [&](uint32_t x) { return h2_as_u32(__hsub2(u32_as_h2(x | magic), koff)); };
-                a0[0] = val(c0[0]);
-                a0[1] = val(c1[0]);
-                a0[2] = val(c0[1]);
-                a0[3] = val(c1[1]);
-                a1[0] = val(c0[2]);
-                a1[1] = val(c1[2]);
-                a1[2] = val(c0[3]);
-                a1[3] = val(c1[3]);
+                mma_16816(o[4 * b + 0], a, val(c0[0]), val(c0[1]));
+                mma_16816(o[4 * b + 2], a, val(c0[2]), val(c0[3]));
+                mma_16816(o[4 * b + 1], a, val(c1[0]), val(c1[1]));
+                mma_16816(o[4 * b + 3], a, val(c1[2]), val(c1[3]));
             }
-            mma_16816(o[2 * b], a0, bh0, bh1);
-            mma_16816(o[2 * b], a0, bl0, bl1);
-            mma_16816(o[2 * b + 1], a1, bh0, bh1);
-            mma_16816(o[2 * b + 1], a1, bl0, bl1);
             if constexpr (has_min(VT)) {
                 // + p * lo for every value of the block: sum over keys of p * lo (f16 hi + lo
-                // like P') lands in column b of corr (rows g: hi part, g + 8: lo part; B = 1.0
-                // in column b); added at the end
+                // like P') lands in column b of corr (B = 1.0 in column b); added at the end
                 const uint2 lsc = *reinterpret_cast<const uint2 *>(vs + kScaleTile + j * 32 + b * 8);
                 const __half2 lab = u32_as_h2(lsc.x & mab), lcd = u32_as_h2(lsc.y & mcd);
                 const __half2 hab2 = __hmul2(u32_as_h2(ph_ab), lab), hcd2 = __hmul2(u32_as_h2(ph_cd), lcd);
@@ -706,8 +650,7 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
                 a2[1] = h2_as_u32(__hfma2(u32_as_h2(pl_ab), lab, __hfma2(u32_as_h2(ph_ab), lab, __hneg2(hab2))));
                 a2[2] = h2_as_u32(hcd2);
                 a2[3] = h2_as_u32(__hfma2(u32_as_h2(pl_cd), lcd, __hfma2(u32_as_h2(ph_cd), lcd, __hneg2(hcd2))));
-                const int g = lane >> 2;
-                const uint32_t one = g == b ? 0x3c003c00u : 0u;
+                const uint32_t one = (lane >> 2) == b ? 0x3c003c00u : 0u;
                 mma_16816(corr, a2, one, one);
             }
         }
@@ -717,8 +660,6 @@ __device__ __forceinline__ void tile_pv(const uint8_t *vc, const uint8_t *vs, co
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
-// Tiles [t0, t1) of split `split` of a sequence with T tiles: shares of ceil(T / ns) tiles
-// (ns = min(n_splits, T); splits from ns on are empty).
 __device__ __forceinline__ void split_range(const DecodeParams &p, int T, int split, int &t0, int &t1) {
     const int ns = max(1, min(p.n_splits, T));
     const int tps = T > 0 ? (T + ns - 1) / ns : 0;
@@ -739,9 +680,10 @@ __device__ __noinline__ void prefetch_split(const DecodeParams &p, int bseq, int
     if (p.k_new != nullptr) ++L;
     L = L < 0 ? 0 : (L > cap_rows ? cap_rows : L);
     const int T = (L + kTileRows - 1) / kTileRows;
-    int t0, t1;
-    split_range(p, T, split, t0, t1);
-    t0 = min(t1, t0 + skip_tiles);
+    const int ns = max(1, min(p.n_splits, T));
+    if (split >= ns || T == 0) return;
+    const int tps = (T + ns - 1) / ns;
+    const int t0 = min(T, split * tps + skip_tiles), t1 = min(T, split * tps + tps);
     const int nt = min(t1 - t0, kPrefetchBytes / C::TILE - skip_tiles);
     if (nt <= 0) return;
     const size_t bt = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + t0;
@@ -776,22 +718,21 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
         const int C = rows * (D / 4);
         const int P = max(1, min(min(NP, C), static_cast<int>((tbytes + kWideBytes - 1) / kWideBytes)));
         int32_t *cnt = p.counters + unit;
+        __threadfence();  // each thread publishes its own writes
         __syncthreads();
         if (threadIdx.x == 0) {
-            fence_acq_rel_gpu();  // release this CTA's triple
             const int t = atomicAdd(cnt, 1) & 0xffff;    // earlier first arrivals
             int role = t >= NP - P ? t - (NP - P) : -1;  // merger index, or -1
-            if (role >= 0 && t != NP - 1 && !wait_count(cnt, NP, p.wait_cycles)) {
-                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
-                role = -2;  // a merger that gave up: no merge, but its second arrival counts
-            }
-            if (role >= 0) fence_acq_rel_gpu();  // acquire every triple
+            const int w = role >= 0 && t != NP - 1 ? wait_count(cnt, NP, p.wait_cycles) : 0;
+            if (w) atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
+            if (w == 2) role = -2;  // a merger that gave up: no merge, but its second arrival counts
             s_flag = role;
         }
         __syncthreads();
         const int role = s_flag;
         if (role == -1) return;
         if (role >= 0) {
+            __threadfence();
             merge_cols(p.part_o, p.part_m, p.part_l, p.part_stride, NP, row0, D, role * C / P, (role + 1) * C / P,
                        p.out, p.lse, rmap, p.ext_out, p.ext_lse, smem);
             __syncthreads();
@@ -800,10 +741,9 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
         return;
     }
     if (tbytes <= kDirectMergeBytes) {
-        // the last arrival merges all splits, several threads per output column
         if (!arrive_last(p.counters + unit, NP, s_flag)) return;
-        merge_cols(p.part_o, p.part_m, p.part_l, p.part_stride, NP, row0, D, 0, rows * (D / 4), p.out, p.lse, rmap,
-                   p.ext_out, p.ext_lse, smem);
+        merge_rows(p.part_o, p.part_m, p.part_l, p.part_stride, 0, NP, row0, rows, D, p.out, p.lse, nullptr, nullptr,
+                   nullptr, 0, 0, rmap, p.ext_out, p.ext_lse);
         if (threadIdx.x == 0) p.counters[unit] = 0;
         return;
     }
@@ -822,29 +762,25 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
     if (threadIdx.x == 0) p.counters[unit] = 0;
 }
 
-// Launch timing (p.stamps): thread 0 of a CTA writes %globaltimer at four points, to
-// stamps[4c .. 4c + 3] for CTA c: start, past the programmatic-launch wait, once its split
-// triple (or its output) is written, and when it leaves the kernel (every path out of
-// decode_body is CTA-uniform).
-constexpr int kStamps = 4;
-__device__ __forceinline__ unsigned long long *cta_stamp(const DecodeParams &p) {
-    if (p.stamps == nullptr || threadIdx.x != 0) return nullptr;
+// Launch timing (p.stamps): thread 0 of a CTA writes %globaltimer when it starts and when it
+// leaves the kernel, to stamps[2c], stamps[2c + 1] for CTA c (every path out of decode_body
+// is CTA-uniform).  Stamps inside the body cost registers in the decode loop; two-region
+// (window + tail) launches, whose two inlined bodies are tighter still, write none.
+constexpr int kStamps = 2;
+// Stamp k of this CTA (thread 0), or nothing.  The address is formed at each use, so that no
+// register holds it through the decode loop.
+__device__ __forceinline__ void stamp(const DecodeParams &sp, int k) {
+    if (sp.stamps == nullptr || threadIdx.x != 0) return;
     const unsigned c = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-    if (c >= static_cast<unsigned>(p.stamp_ctas)) return nullptr;
-    unsigned long long *st = p.stamps + kStamps * static_cast<size_t>(c);
-    st[0] = global_timer_ns();
-    st[1] = st[2] = 0;
-    return st;
-}
-__device__ __forceinline__ void stamp(unsigned long long *st, int k) {
-    if (st) st[k] = global_timer_ns();
+    if (c >= static_cast<unsigned>(sp.stamp_ctas)) return;
+    unsigned long long *st = sp.stamps + kStamps * static_cast<size_t>(c);
+    st[k] = global_timer_ns();
 }
 
 // The decode of one CTA: split `split` of this launch's cache (blockIdx.y = KV head,
-// blockIdx.z = sequence x row group).  st: this CTA's timer stamps (thread 0) or nullptr.
+// blockIdx.z = sequence x row group).
 template <int KT, int VT, int NS, bool MQ, int TW_ = 0>
-__device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split, const int h,
-                                            const int z, unsigned long long *st) {
+__device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split) {
     using C = Cfg<KT, VT, NS, TW_>;
     constexpr int TPW = C::TPW;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -852,7 +788,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     __shared__ int s_timeout;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bseq = z / p.QG, qg = z % p.QG;
+    const int h = blockIdx.y;
+    const int bseq = blockIdx.z / p.QG, qg = blockIdx.z % p.QG;
     const int cap_rows = p.cap_tiles * kTileRows;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
     uint64_t *empty = full + C::STAGES;
@@ -876,7 +813,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     if (!early) {
         if (threadIdx.x == 0) prefetch_split<C>(p, bseq, h, split, cap_rows, 0);
         grid_dep_wait();
-        stamp(st, 1);
     }
     int L_old = __ldcg(p.len + bseq);
     L_old = L_old < 0 ? 0 : (L_old > cap_rows ? cap_rows : L_old);
@@ -886,6 +822,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     const int L = do_app ? L_old + 1 : L_old;
     const int T = (L + kTileRows - 1) / kTileRows;
     const int ns = max(1, min(p.n_splits, T));
+    const int tps = T > 0 ? (T + ns - 1) / ns : 0;
     const int n_q = MQ ? p.n_q : 1;     // queries per sequence (compile-time 1 for decode)
     const int unit_rows = n_q * p.G;    // query rows of this (sequence, KV head)
     const int rows = min(kMaxRowsPerGroup, unit_rows - qg * kMaxRowsPerGroup);
@@ -897,7 +834,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     // merge it runs on with an empty range (t_begin = t_end = T) and publishes an empty triple.
     if (split >= ns && p.merge_slots == 0) {
         if (early) grid_dep_wait();
-        if (early) stamp(st, 1);
         grid_dep_launch();
         if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
         if (!fused) {  // partials mode: splits beyond ns are empty triples
@@ -913,17 +849,16 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
         }
         return;
     }
-    int t_begin, t_end;
-    split_range(p, T, split, t_begin, t_end);
+    const int t_begin = min(T, split * tps), t_end = min(T, t_begin + tps);
     const int n_stage = (t_end - t_begin + C::TWT - 1) / C::TWT;
 
     const size_t bh_tile = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles;
 
     // per-consumer results kept until the merge
     float m_run = -CUDART_INF_F, l_acc = 0.f;
-    float o[8][4];  // O^T: 8 m-tiles of 16 values x (rows 2j, 2j+1), see tile_pv
+    float o[16][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     int tw = 0, sl = 0;
 
     if (warp == 0) {
@@ -962,14 +897,17 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             }
             __syncwarp();
             grid_dep_wait();
-            stamp(st, 1);
         }
         grid_dep_launch();
         bool ok = true;
         int slot = k0 == C::STAGES ? 0 : k0, use = k0 == C::STAGES ? 1 : 0;
         for (int k = k0; k < n_stage; ++k) {
             bool ok_k = true;
-            if (lane == 0 && use > 0) ok_k = mbar_wait(empty + slot, (use - 1) & 1, p.wait_cycles);
+            if (lane == 0 && use > 0) {
+                const int w = mbar_wait_timed(empty + slot, (use - 1) & 1, p.wait_cycles);
+                if (w) atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
+                ok_k = w != 2;
+            }
             if (!__shfl_sync(0xffffffffu, ok_k ? 1 : 0, 0)) {
                 ok = false;
                 break;
@@ -1002,15 +940,11 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
         // the length advance of a fused append, off the consumers' critical path
         if (appending && lane == 0) grid_ticket(p, cap_rows);
         if (!ok && lane == 0) {
-            atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
             s_timeout = 1;
-        }
-        // every copy this warp issued lands before the ring is reused or the CTA exits (the
-        // last use of each slot; a phase the consumers already saw completes at once).  This
-        // drain keeps the default limit whatever limit the other waits were given.
-        if (lane == 0)
+            // let the copies already issued land before the CTA can exit
             for (int i = 0; i < C::STAGES; ++i)
                 if (issued_use[i] >= 0) (void)mbar_wait(full + i, issued_use[i] & 1);
+        }
     } else {
         // ---------------- consumers ----------------
         if (early) grid_dep_wait();
@@ -1073,20 +1007,24 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
 
         int slot = 0, use = 0;
         for (int k = 0; k < n_stage; ++k) {
-            if (!dead && !mbar_wait(full + slot, use & 1, p.wait_cycles)) {
-                dead = true;
-                atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
-                s_timeout = 1;
+            if (!dead) {
+                const int w = mbar_wait_timed(full + slot, use & 1, p.wait_cycles);
+                if (w) atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
+                if (w == 2) {  // gave up: this CTA publishes an empty triple
+                    dead = true;
+                    s_timeout = 1;
+                }
             }
             const int tA = t_begin + (k * C::TW + tw) * TPW;  // first tile of this warp in the stage
             if (tA < t_end) {
                 const uint8_t *st = smem + slot * C::STAGE;
                 float sc[TPW][4];
-                {
-                    const int ti = tw * TPW;  // first tile of this warp inside the stage
-                    tile_scores<KT, TPW, C::KC, C::KS>(st + ti * C::KC + sl * code_tile_bytes(KT),
-                                                       st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * scale_tile_bytes(KT),
-                                                       qsm, kcor_row, lane, j, sc);
+#pragma unroll
+                for (int t = 0; t < TPW; ++t) {
+                    const int ti = tw * TPW + t;  // tile index inside the stage
+                    tile_scores<KT>(st + ti * C::KC + sl * code_tile_bytes(KT),
+                                    st + C::TWT * (C::KC + C::VC) + ti * C::KS + sl * scale_tile_bytes(KT), qsm, kcor_row, lane,
+                                    j, sc[t]);
                 }
                 // f16 overflow guard: p = exp2(s - m_run) may reach 2^kTau before the running
                 // maximum is moved, so a tile pair holding a V scale with |scale| >= 256 (or
@@ -1181,15 +1119,12 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
 #pragma unroll
                         for (int i = 0; i < 4; ++i) corr[i] *= alpha;
                     }
-                    // o holds rows 2j and 2j+1, whose factors live in lanes 8j and 8j + 4
-                    const float a_r0 = __shfl_sync(0xffffffffu, alpha, 8 * j);
-                    const float a_r1 = __shfl_sync(0xffffffffu, alpha, 8 * j + 4);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        o[i][0] *= a_r0;
-                        o[i][1] *= a_r1;
-                        o[i][2] *= a_r0;
-                        o[i][3] *= a_r1;
+                    for (int i = 0; i < 16; ++i) {
+                        o[i][0] *= alpha;
+                        o[i][1] *= alpha;
+                        o[i][2] *= alpha;
+                        o[i][3] *= alpha;
                     }
                 }
                 float pk[TPW][4];
@@ -1230,31 +1165,29 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             }
         }
         // V types with a minimum: add sum of p * lo of each block to its values (corr column
-        // b of row r: hi part in lane 4r + b/2 at corr[b % 2], lo part at corr[2 + b % 2])
+        // b, held by lane 4g + b/2 for the hi and lo rows)
         if constexpr (has_min(VT)) {
             const float v0 = corr[0] + corr[2], v1 = corr[1] + corr[3];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                const float src = (b & 1) ? v1 : v0;
-                const float ct0 = __shfl_sync(0xffffffffu, src, 8 * j + (b >> 1));      // row 2j
-                const float ct1 = __shfl_sync(0xffffffffu, src, 8 * j + 4 + (b >> 1));  // row 2j + 1
+                const float ct = __shfl_sync(0xffffffffu, (b & 1) ? v1 : v0, (lane & ~3) | (b >> 1));
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    o[2 * b + h][0] += ct0;
-                    o[2 * b + h][2] += ct0;
-                    o[2 * b + h][1] += ct1;
-                    o[2 * b + h][3] += ct1;
+                for (int i = 0; i < 4; ++i) {
+                    o[4 * b + i][0] += o[4 * b + i][2] + ct;
+                    o[4 * b + i][1] += o[4 * b + i][3] + ct;
+                    o[4 * b + i][2] = 0.f;
+                    o[4 * b + i][3] = 0.f;
                 }
             }
         }
         // q8_0 V: o to real units
         if constexpr (VT == KVQ_Q8_0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                o[i][0] *= kTwo24;
-                o[i][1] *= kTwo24;
-                o[i][2] *= kTwo24;
-                o[i][3] *= kTwo24;
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] = (o[i][0] + o[i][2]) * kTwo24;
+                o[i][1] = (o[i][1] + o[i][3]) * kTwo24;
+                o[i][2] = 0.f;
+                o[i][3] = 0.f;
             }
         }
         // row sums over the four lanes of a row
@@ -1270,15 +1203,16 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     float *lb = mb + C::TW * kMaxRowsPerGroup;                     // [TW][8]
     if (warp > 0) {
         const int g = lane >> 2, j = lane & 3;
-        float *r0 = Ob + (tw * kMaxRowsPerGroup + 2 * j) * D + sl * kSlice;  // rows 2j, 2j + 1
-        float *r1 = r0 + D;
-        const int v0 = 4 * (g >> 1) + 2 * (g & 1);
+        float *orow = Ob + (tw * kMaxRowsPerGroup + g) * D + sl * kSlice;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            // m-tile mt = 2b + h: values 32b + 16h + v0 (c0, c1) and + 1 (c2, c3)
-            const int v = 16 * mt + v0;
-            *reinterpret_cast<float2 *>(r0 + v) = make_float2(o[mt][0], o[mt][2]);
-            *reinterpret_cast<float2 *>(r1 + v) = make_float2(o[mt][1], o[mt][3]);
+        for (int b = 0; b < 4; ++b) {
+            // thread holds d = 32b + 4j + {0..3} (ptiles 0,1 of block b) and +16 (ptiles 2,3)
+            const float4 lo4 = make_float4(o[4 * b + 0][0] + o[4 * b + 0][2], o[4 * b + 1][0] + o[4 * b + 1][2],
+                                           o[4 * b + 0][1] + o[4 * b + 0][3], o[4 * b + 1][1] + o[4 * b + 1][3]);
+            const float4 hi4 = make_float4(o[4 * b + 2][0] + o[4 * b + 2][2], o[4 * b + 3][0] + o[4 * b + 3][2],
+                                           o[4 * b + 2][1] + o[4 * b + 2][3], o[4 * b + 3][1] + o[4 * b + 3][3]);
+            *reinterpret_cast<float4 *>(orow + 32 * b + 4 * j) = lo4;
+            *reinterpret_cast<float4 *>(orow + 32 * b + 16 + 4 * j) = hi4;
         }
         if (sl == 0 && j == 0) {
             mb[tw * kMaxRowsPerGroup + g] = m_run;
@@ -1337,7 +1271,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             }
         }
     }
-    stamp(st, 2);
     // A CTA that timed out still takes its merge arrivals, so the arrival counters of the
     // workspace end at zero once every CTA of the launch has finished.
     if (!fused || single) return;
@@ -1348,9 +1281,9 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
 
 template <int KT, int VT, int NS, bool MQ>
 __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN_CTAS) decode_kernel(const DecodeParams p, const int fused) {
-    unsigned long long *st = cta_stamp(p);
-    decode_body<KT, VT, NS, MQ>(p, fused, blockIdx.x, blockIdx.y, blockIdx.z, st);
-    stamp(st, kStamps - 1);
+    stamp(p, 0);
+    decode_body<KT, VT, NS, MQ>(p, fused, blockIdx.x);
+    stamp(p, kStamps - 1);
 }
 
 // One launch over an f16 window and a quantised tail of the same sequences: splits
@@ -1361,12 +1294,10 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     dual_kernel(const DecodeParams pw, const DecodeParams pt, const int nw) {
     constexpr int TWW = Cfg<KT, VT, NS>::TW;  // the window body runs with the tail's warp count
     static_assert(Cfg<KVQ_F16, KVQ_F16, NS, TWW>::THREADS == Cfg<KT, VT, NS>::THREADS, "one block size");
-    unsigned long long *st = cta_stamp(pt);
     if (static_cast<int>(blockIdx.x) < nw)
-        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x, blockIdx.y, blockIdx.z, st);
+        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x);
     else
-        decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw, blockIdx.y, blockIdx.z, st);
-    stamp(st, kStamps - 1);
+        decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw);
 }
 
 constexpr int kMaxDevices = 64;
@@ -1432,7 +1363,6 @@ cudaError_t launch_decode_t(const DecodeParams &p, bool fused, cudaStream_t stre
     DecodeParams q = p;
     const long long ctas = static_cast<long long>(p.n_splits) * p.Hkv * p.B * p.QG;
     q.wide = (fused && ctas <= static_cast<long long>(occ) * sms) ? 1 : 0;
-
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B * p.QG);
     cfg.blockDim = dim3(C::THREADS);

@@ -190,17 +190,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 constexpr long long kPollWaitCycles = 1000000LL;
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit = kWaitCycles) {
-    if (limit < kPollWaitCycles) {
-        const long long t0 = clock64();
-        while (!mbar_test_wait(bar, parity))
-            if (clock64() - t0 > limit) return false;
-        return true;
-    }
-    if (mbar_try_wait(bar, parity)) return true;
-    long long t0 = clock64();
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    const bool poll = limit < kPollWaitCycles;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > limit) return false;
+    }
+}
+
+// Wait of the split-K decode kernels: 0 when the phase completed within `report` SM cycles,
+// 1 when it completed later (the caller reports it), 2 when it did not complete within
+// kWaitCycles (the caller gives up).  A short `report` limit thus flags a slow wait without
+// abandoning it, so no copy is ever left in flight by a reported wait.
+__device__ __forceinline__ int mbar_wait_timed(uint64_t *bar, uint32_t parity, long long report) {
+    if (mbar_test_wait(bar, parity)) return 0;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return clock64() - t0 > report ? 1 : 0;
+        if (clock64() - t0 > kWaitCycles) return 2;
     }
 }
 

@@ -1,12 +1,13 @@
 """Failure handling of the decode kernels on the GPU, without faulting or hanging it.
 
-Every pipeline and merge wait in the decode kernels is bounded.  kvq_set_wait_limit
-shortens the bound (here to a few dozen SM cycles), so that waits give up on a healthy
-GPU: the kernel must then return, set KVQ_DEVERR_TIMEOUT in the cache's error word, and
-leave the workspace's arrival counters at zero, so that the next call on the same
-workspace (with the default limit restored) matches the oracle again.  Each merge form is
-covered: one split, the last arrival merging all splits, the column merge of a grid that
-is resident at once, and the two-level merge of a larger grid.
+Every pipeline and merge wait in the decode kernels is bounded (about two seconds).
+kvq_set_wait_limit sets the time after which a wait is reported (here a few dozen SM
+cycles, so that waits on a healthy GPU exceed it): the kernel must then return, set
+KVQ_DEVERR_TIMEOUT in the cache's error word, and leave the workspace's arrival counters
+at zero, so that the next call on the same workspace (with the default limit restored)
+matches the oracle again.  Each merge form is covered: one split, the last arrival merging
+all splits, the column merge of a grid that is resident at once, and the two-level merge
+of a larger grid.
 """
 import numpy as np
 import pytest
@@ -90,7 +91,7 @@ def test_wait_timeout_reported_and_recovered(kvq, name):
     torch.cuda.synchronize()  # the kernel returned
     err = cache.read_error()
     assert err == kvq.DEVERR_TIMEOUT, err
-    # a CTA that gave up still took its arrivals: the counters are back at zero
+    # every CTA took its arrivals: the counters are back at zero
     assert int(ws[:counter_bytes(wl)].count_nonzero()) == 0
     # the next call on the same workspace, with the default limit, is exact again
     out2, lse2 = cache.decode(q, scale=wl.scale, n_splits=splits, workspace=ws)
