@@ -56,17 +56,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
                  : "memory");
 }
-// 32 consecutive columns of this thread's lane (the warp's quarter of the 128 lanes)
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
@@ -128,20 +117,21 @@ struct TcCfg {
     static constexpr int OFF_V = OFF_K + 2 * (K_LO ? 2 : 1) * KHAT;  // [hi, lo]
     static constexpr int OFF_QT = OFF_V + (V_LO ? 2 : 1) * VHAT;
     static constexpr int OFF_BAR = (OFF_QT + QT + 15) / 16 * 16;
-    // barriers: full[STAGES], empty[STAGES], k_ready[2], v_ready, s_done[2], s_free (+1 spare),
-    // p_ready[2], pv_done, e_ready[4], q_ready, drain; then e values [4][2] and the
-    // tensor-memory address
-    static constexpr int NBAR = 2 * STAGES + 2 + 1 + 2 + 2 + 2 + 1 + 4 + 2;
+    // barriers: full[STAGES], empty[STAGES], k_ready[2], v_ready, s_done[2] (Q hi stream),
+    // s_done_b[2] (Q lo stream), s_free (+1 spare), p_ready (+1 spare), pv_done, e_ready[4],
+    // q_ready, drain; then e values [4][2] and the tensor-memory address
+    static constexpr int NBAR = 2 * STAGES + 2 + 1 + 2 + 2 + 2 + 2 + 1 + 4 + 2;
     static constexpr int OFF_E = OFF_BAR + NBAR * 8;
     static constexpr int OFF_TADDR = OFF_E + 4 * 2 * 4;
     static constexpr int SMEM = OFF_TADDR + 16;
-    // tensor memory columns: O [0, D), S [D, D + 2 NK) as [hi NK, lo NK] (the lo columns hold
-    // Q hi K^ lo), P [D + 2 NK, D + 4 NK) as [buffer][hi NK / 2, lo NK / 2], Q lo [D + 4 NK, D + 4 NK + D / 2)
-    static constexpr int T_O = 0, T_S = D, T_P = D + 2 * NK, T_Q = D + 4 * NK;
+    // tensor memory columns: O [0, D), S [D, D + 2 NK) as [Q hi K^ hi, Q hi K^ lo], S2 [D + 2 NK,
+    // D + 3 NK) (Q lo K^ hi), P [D + 3 NK, D + 4 NK) as [hi NK / 2, lo NK / 2], Q lo [D + 4 NK, D + 4 NK + D / 2)
+    static constexpr int T_O = 0, T_S = D, T_S2 = D + 2 * NK, T_P = D + 3 * NK, T_Q = D + 4 * NK;
     static constexpr int TCOLS = 512;
-    // warps 6 .. 15; 16 warps leave 128 registers a thread (an SM sub-partition holds 4 warps)
-    static constexpr int CONV_THREADS = 320;
-    static constexpr int THREADS = 6 * 32 + CONV_THREADS;
+    // converters: warps 6 .. 13; warps 14 and 15 issue the Q lo and P V^ instructions.  16
+    // warps leave 128 registers a thread (an SM sub-partition holds 4 warps)
+    static constexpr int CONV_THREADS = 256;
+    static constexpr int THREADS = 6 * 32 + CONV_THREADS + 64;
     static_assert(T_Q + D / 2 <= TCOLS, "tensor memory");
     static_assert(SMEM <= BUDGET, "shared memory");
     static_assert(M * O_ROW <= OFF_QT, "epilogue staging fits the operand memory");
@@ -200,7 +190,8 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
     const int split = blockIdx.x, h = blockIdx.y, bseq = blockIdx.z;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *full = bars, *empty = full + C::STAGES, *k_ready = empty + C::STAGES, *v_ready = k_ready + 2;
-    uint64_t *s_done = v_ready + 1, *s_free = s_done + 2, *p_ready = s_free + 2, *pv_done = p_ready + 2;
+    uint64_t *s_done = v_ready + 1, *s_done_b = s_done + 2, *s_free = s_done_b + 2, *p_ready = s_free + 2;
+    uint64_t *pv_done = p_ready + 2;
     uint64_t *e_ready = pv_done + 1, *q_ready = e_ready + 4, *drain = q_ready + 1;
     int *e_val = reinterpret_cast<int *>(smem + C::OFF_E);  // [4][2]: e_k, e_v of chunk c at slot c % 4
     uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TADDR);
@@ -214,13 +205,14 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
         for (int i = 0; i < 2; ++i) {
             mbar_init(k_ready + i, 1);
             mbar_init(s_done + i, 1);
-            mbar_init(p_ready + i, 4);
+            mbar_init(s_done_b + i, 1);
         }
         mbar_init(s_free, 4);
+        mbar_init(p_ready, 4);
         mbar_init(v_ready, 1);
         mbar_init(pv_done, 1);
         mbar_init(q_ready, 8);
-        mbar_init(drain, 1);
+        mbar_init(drain, 3);
         for (int i = 0; i < 4; ++i) mbar_init(e_ready + i, 1);
         fence_mbar_init();
         s_timeout = 0;
@@ -357,55 +349,57 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
             for (int i = 0; i < C::STAGES; ++i)  // every copy lands before the CTA reuses or frees its memory
                 if (issued_use[i] >= 0) (void)mbar_wait(full + i, issued_use[i] & 1);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issue (one thread) ----------------
-        // Order: S(c + 1) as soon as K^(c + 1) is converted and the softmax warps have read
-        // S(c) (one S region), then O += P(c) V^(c).  S = Q K^T is two instructions per
-        // 16-dim step: Q hi (shared memory) times [K^ hi; K^ lo] (N = 2 NK, so the Q operand
-        // is read once for both), and Q lo (tensor memory) times K^ hi into the hi columns.
+    } else if (warp == 1 || warp >= 14) {
+        // ---------------- MMA issue: three threads, one instruction stream each ----------------
+        // An issuing thread waits about 120 cycles per small-N instruction, so the streams run
+        // in parallel: warp 1 issues S = Q hi [K^ hi; K^ lo]^T (N = 2 NK: Q hi read once for
+        // both halves), warp 14 S2 = Q lo K^ hi^T, warp 15 O += P V^.  S and S2 of chunk c + 1
+        // are issued as soon as K^(c + 1) is converted and the softmax warps have read S(c)
+        // and S2(c); O += P(c) V^(c) once P(c) and V^(c) are written.
         if (lane == 0) {
-            bool ok = true;
-            auto issue_s = [&](int c) {
-                const int kb = c & 1;
-                if (!mbar_wait(k_ready + kb, (c >> 1) & 1, limit)) return false;
-                if (c >= 1 && !mbar_wait(s_free, (c - 1) & 1, limit)) return false;
-                tc_fence_after();
-                // descriptors built once; a 16-dim step moves the start address by 256 bytes,
-                // i.e. 16 in the descriptor's address field (the issue loop is the bottleneck
-                // of small-N instructions, so it does no more than add and issue)
-                const uint32_t d = tbase + C::T_S, tq = tbase + C::T_Q;
-                const uint64_t a0 = tc_desc(smem_u32(qhi), 128, D * 16), b0 = tc_desc(smem_u32(khat(kb, 0)), 128, D * 16);
+            bool ok = mbar_wait(q_ready, 0, limit);  // Q hi (shared) and Q lo (tensor memory) written
+            if (warp == 1 || warp == 14) {
+                const bool hi = warp == 1;
+                const uint32_t d = tbase + (hi ? C::T_S : C::T_S2), tq = tbase + C::T_Q;
+                const uint64_t a0 = tc_desc(smem_u32(qhi), 128, D * 16);
+                for (int c = 0; c < NC && ok; ++c) {
+                    const int kb = c & 1;
+                    if (!mbar_wait(k_ready + kb, (c >> 1) & 1, limit) || (c >= 1 && !mbar_wait(s_free, (c - 1) & 1, limit))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // descriptors built once; a 16-dim step moves the start address by 256
+                    // bytes, i.e. 16 in the descriptor's address field
+                    const uint64_t b0 = tc_desc(smem_u32(khat(kb, 0)), 128, D * 16);
+                    if (hi) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    tc_mma_ss(d, a0 + 16 * ks, b0 + 16 * ks, IDESC_S2, ks > 0 ? 1 : 0);
-                    tc_mma_ts(d, tq + ks * 8, b0 + 16 * ks, IDESC_S, 1);
+                        for (int ks = 0; ks < D / 16; ++ks) tc_mma_ss(d, a0 + 16 * ks, b0 + 16 * ks, IDESC_S2, ks > 0 ? 1 : 0);
+                        tc_commit(s_done + kb);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) tc_mma_ts(d, tq + ks * 8, b0 + 16 * ks, IDESC_S, ks > 0 ? 1 : 0);
+                        tc_commit(s_done_b + kb);
+                    }
                 }
-                tc_commit(s_done + kb);
-                return true;
-            };
-            ok = mbar_wait(q_ready, 0, limit);  // Q hi (shared) and Q lo (tensor memory) written
-            if (NC > 0 && ok) ok = issue_s(0);
-            for (int c = 0; c < NC && ok; ++c) {
-                if (c + 1 < NC && !issue_s(c + 1)) {
-                    ok = false;
-                    break;
-                }
-                const int pb = c & 1;
-                if (!mbar_wait(p_ready + pb, (c >> 1) & 1, limit) || !mbar_wait(v_ready, c & 1, limit)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+            } else {
                 const uint64_t vh0 = tc_desc(smem_u32(vhat(0)), 128, NK * 16);
                 const uint64_t vl0 = tc_desc(smem_u32(vhat(C::V_LO ? 1 : 0)), 128, NK * 16);
+                for (int c = 0; c < NC && ok; ++c) {
+                    if (!mbar_wait(p_ready, c & 1, limit) || !mbar_wait(v_ready, c & 1, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < NK / 16; ++kk) {
-                    const uint32_t ph = tbase + C::T_P + pb * NK + kk * 8, pl = ph + NK / 2;
-                    tc_mma_ts(tbase + C::T_O, ph, vh0 + 16 * kk, IDESC_O, (c > 0 || kk > 0) ? 1 : 0);
-                    if constexpr (C::V_LO) tc_mma_ts(tbase + C::T_O, ph, vl0 + 16 * kk, IDESC_O, 1);
-                    tc_mma_ts(tbase + C::T_O, pl, vh0 + 16 * kk, IDESC_O, 1);
+                    for (int kk = 0; kk < NK / 16; ++kk) {
+                        const uint32_t ph = tbase + C::T_P + kk * 8, pl = ph + NK / 2;
+                        tc_mma_ts(tbase + C::T_O, ph, vh0 + 16 * kk, IDESC_O, (c > 0 || kk > 0) ? 1 : 0);
+                        if constexpr (C::V_LO) tc_mma_ts(tbase + C::T_O, ph, vl0 + 16 * kk, IDESC_O, 1);
+                        tc_mma_ts(tbase + C::T_O, pl, vh0 + 16 * kk, IDESC_O, 1);
+                    }
+                    tc_commit(pv_done);
                 }
-                tc_commit(pv_done);
             }
             if (!ok) {
                 atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
@@ -416,7 +410,7 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
             (void)mbar_wait(drain, 0);
         }
         __syncwarp();
-    } else if (warp >= 6) {
+    } else if (warp >= 6) {  // warps 6 .. 13
         // ---------------- converters: codes -> K^, V^ ----------------
         // Order K^(0), K^(1), V^(0), K^(2), V^(1), ...: K^(c + 1) is ready while the softmax
         // of chunk c runs, and V^(c) (one buffer) waits only for O += P(c - 1) V^(c - 1).
@@ -448,7 +442,10 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
             const uint8_t *kcs = st, *kss = st + 2 * (C::KC + C::VC), *vss = kss + 2 * C::KS;
             const int nvalid = nvalid_of(c);
             bool okc = mbar_wait(full + slot, use & 1, limit);
-            if (c >= 2) okc = mbar_wait(s_done + kb, ((c >> 1) - 1) & 1, limit) && okc;
+            if (c >= 2) {  // both S streams of chunk c - 2 have read this K^ buffer
+                okc = mbar_wait(s_done + kb, ((c >> 1) - 1) & 1, limit) && okc;
+                okc = mbar_wait(s_done_b + kb, ((c >> 1) - 1) & 1, limit) && okc;
+            }
             // the chunk's exponents (largest scale of its valid keys), found by every converter
             // warp on its own
             constexpr float cmaxk = KT == KVQ_Q8_0 ? 127.f : 8.f, cmaxv = VT == KVQ_Q8_0 ? 127.f : 8.f;
@@ -691,6 +688,7 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
         for (int c = 0; c < NC; ++c) {
             const int kb = c & 1;
             bool okc = mbar_wait(s_done + kb, (c >> 1) & 1, limit);
+            okc = mbar_wait(s_done_b + kb, (c >> 1) & 1, limit) && okc;
             okc = mbar_wait(e_ready + (c & 3), (c >> 2) & 1, limit) && okc;
             okc = __all_sync(0xffffffffu, okc);
             tc_fence_after();
@@ -700,16 +698,21 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
             float s[32], mx = -CUDART_INF_F;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {  // 16 keys at a time
-                uint32_t a[16];
-                tc_ld16(trow + C::T_S + 16 * h2, a);
-                if constexpr (C::K_LO) {  // S = (Q hi K^ hi + Q lo K^ hi) + Q hi K^ lo
+                uint32_t a[16];  // S = Q hi K^ hi + Q lo K^ hi (S2) + Q hi K^ lo
+                {
+                    uint32_t a2[16];
+                    tc_ld16(trow + C::T_S + 16 * h2, a);
+                    tc_ld16(trow + C::T_S2 + 16 * h2, a2);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(a2[j]));
+                }
+                if constexpr (C::K_LO) {
                     uint32_t b[16];
                     tc_ld16(trow + C::T_S + NK + 16 * h2, b);
                     tc_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(b[j]));
-                } else {
-                    tc_wait_ld();
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -739,7 +742,7 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
                 l_acc += p0 + p1;
                 split_hi_lo(p0 * fv, p1 * fv, phw[u], plw[u]);
             }
-            // O and the P buffer of chunk c - 2 are free once O += P(c - 1) V^(c - 1) is done
+            // O and the P buffer are free once O += P(c - 1) V^(c - 1) is done
             if (c >= 1) okc = mbar_wait(pv_done, (c - 1) & 1, limit) && okc;
             okc = __all_sync(0xffffffffu, okc);
             tc_fence_after();
@@ -754,12 +757,12 @@ __global__ void __launch_bounds__(TcCfg<KT, VT, NS>::THREADS, 1) verify_tc_kerne
                     tc_st16(trow + C::T_O + k0, o);
                 }
             }
-            tc_st16(trow + C::T_P + kb * NK, phw);
-            tc_st16(trow + C::T_P + kb * NK + NK / 2, plw);
+            tc_st16(trow + C::T_P, phw);  // one P buffer: P(c - 1) V^ has completed
+            tc_st16(trow + C::T_P + NK / 2, plw);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_ready + kb);
+            if (lane == 0) mbar_arrive(p_ready);
             if (!okc) ok = false;
         }
         // epilogue: the row's split triple (o unnormalised, m natural log, l)
