@@ -778,8 +778,9 @@ __device__ __forceinline__ void stamp(const DecodeParams &sp, int k) {
 }
 
 // The decode of one CTA: split `split` of this launch's cache (blockIdx.y = KV head,
-// blockIdx.z = sequence x row group).
-template <int KT, int VT, int NS, bool MQ, int TW_ = 0>
+// blockIdx.z = sequence x row group).  MERGE false: the caller runs the split merge (the
+// two-region kernel, so that its two bodies share one copy of the merge code).
+template <int KT, int VT, int NS, bool MQ, int TW_ = 0, bool MERGE = true>
 __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fused, const int split) {
     using C = Cfg<KT, VT, NS, TW_>;
     constexpr int TPW = C::TPW;
@@ -1273,7 +1274,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     }
     // A CTA that timed out still takes its merge arrivals, so the arrival counters of the
     // workspace end at zero once every CTA of the launch has finished.
-    if (!fused || single) return;
+    if (!fused || single || !MERGE) return;
 
     const size_t unit = (static_cast<size_t>(bseq) * p.Hkv + h) * p.QG + qg;
     split_merge(p, p.merge_slots ? p.merge_slots : ns, p.part_base + split, rows, D, prow0, unit, rmap, s_flag, smem);
@@ -1294,10 +1295,21 @@ __global__ void __launch_bounds__(Cfg<KT, VT, NS>::THREADS, Cfg<KT, VT, NS>::MIN
     dual_kernel(const DecodeParams pw, const DecodeParams pt, const int nw) {
     constexpr int TWW = Cfg<KT, VT, NS>::TW;  // the window body runs with the tail's warp count
     static_assert(Cfg<KVQ_F16, KVQ_F16, NS, TWW>::THREADS == Cfg<KT, VT, NS>::THREADS, "one block size");
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_flag;
     if (static_cast<int>(blockIdx.x) < nw)
-        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW>(pw, 1, blockIdx.x);
+        decode_body<KVQ_F16, KVQ_F16, NS, false, TWW, false>(pw, 1, blockIdx.x);
     else
-        decode_body<KT, VT, NS, false>(pt, 1, blockIdx.x - nw);
+        decode_body<KT, VT, NS, false, 0, false>(pt, 1, blockIdx.x - nw);
+    // One merge for both regions, after either body: every CTA has published its triple at
+    // slot blockIdx.x (window splits 0 .. nw - 1, tail splits nw ..); the two parameter
+    // sets share the workspace, the outputs and merge_slots.
+    const int bseq = blockIdx.z / pt.QG, qg = blockIdx.z % pt.QG, h = blockIdx.y;
+    const int rows = min(kMaxRowsPerGroup, pt.G - qg * kMaxRowsPerGroup);
+    const size_t prow0 = (static_cast<size_t>(bseq) * pt.Hkv + h) * pt.G + qg * kMaxRowsPerGroup;
+    const size_t unit = (static_cast<size_t>(bseq) * pt.Hkv + h) * pt.QG + qg;
+    split_merge(pt, pt.merge_slots, static_cast<int>(blockIdx.x), rows, NS * kSlice, prow0, unit, RowMap{1, pt.G, pt.Hq, pt.Hkv},
+                s_flag, smem);
 }
 
 constexpr int kMaxDevices = 64;
