@@ -294,10 +294,10 @@ KVQ_API kvq_status kvq_decode_verify(const kvq_cache *cache, const float *q, int
 /*
  * Kernel choice of kvq_decode_verify (process-wide; the result is the same exact attention
  * either way, within the same tolerance).  0 (default): when a (sequence, KV head) has 49
- * to 128 query rows (n_q * Hq / Hkv), all of them form one 128-row tile on the tensor cores
- * with accumulators in tensor memory (tcgen05): each key chunk is dequantised once for all
- * rows; otherwise groups of 8 rows run the register-operand MMA kernel of
- * kvq_decode_attention.  1: always the groups of 8.  2: the 128-row tile whenever the rows
+ * (D = 256) or 33 (D = 128) to 128 query rows (n_q * Hq / Hkv), all of them form one
+ * 128-row tile on the tensor cores with accumulators in tensor memory (tcgen05): each key
+ * chunk is dequantised once for all rows; otherwise groups of 8 rows run the
+ * register-operand MMA kernel of kvq_decode_attention.  1: always the groups of 8.  2: the 128-row tile whenever the rows
  * fit it.  Workspace sizes and automatic split counts follow the choice
  * in force when they are computed: size the workspace after choosing.
  * KVQ_ERR_INVALID_ARG for another value.

@@ -55,17 +55,17 @@ std::atomic<int> g_verify_path{0};
 // Draft verify on the 128-row tensor-memory tile: base types, more than one group of 8 rows
 // and at most 128 rows per (sequence, KV head), unless the caller chose a path.
 // Automatic choice: the 128-row tile costs about the same for any row count, the groups of 8
-// about one single-query pass each; measured on the 65,536-position hybrid layers (D = 256,
-// G = 8), 4 groups (32 rows) were faster on the register-operand kernel and 16 groups (128
-// rows) on the tile, so the tile is taken from 7 groups (49 rows) up.
-constexpr int kVerifyTcMinRows = 6 * kvq::kMaxRowsPerGroup + 1;
+// about one single-query pass each.  Measured crossovers: near 6 groups (48 rows) on the
+// 65,536-position hybrid layers (D = 256) and near 4 groups (32 rows) on the 131,072-position
+// dense layers (D = 128), so the tile is taken from 49 rows at D = 256 and from 33 at D = 128.
+int verify_tc_min_rows(int head_dim) { return (head_dim == 2 * kvq::kSlice ? 6 : 4) * kvq::kMaxRowsPerGroup + 1; }
 
 bool verify_on_tc(const kvq_cache *c, int32_t n_q_heads, int32_t n_q) {
     const int rows = n_q * (n_q_heads / c->desc.n_kv_heads);
     if (rows > kvq::kVerifyTileRows || !kvq::is_base_type(c->desc.type_k) || !kvq::is_base_type(c->desc.type_v))
         return false;
     const int path = g_verify_path.load(std::memory_order_relaxed);
-    return path == 2 || (path == 0 && rows >= kVerifyTcMinRows);
+    return path == 2 || (path == 0 && rows >= verify_tc_min_rows(c->desc.head_dim));
 }
 
 int auto_splits(const kvq_cache *c, int n_q_heads, int *out, int n_q = 1) {
