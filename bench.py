@@ -444,9 +444,9 @@ def run_rotating(kvq, torch, wl, steps, warmup, peak):
 
 def run_window_cell(kvq, torch, wl, window, steps, warmup, peak):
     """Position-axis mixed cache (f16 window of the last `window` tokens + quantised tail):
-    one step = for every layer, kvq_window_append (1 row, evicting the oldest window row
-    into the tail) + kvq_window_decode (both regions in one launch, exact merge); the layers
-    of a step form one CUDA graph."""
+    one step = for every layer, kvq_window_append_decode: the new row into the window (the
+    oldest window row evicted into the tail) and decode over both regions with one exact
+    merge, in one launch; the layers of a step form one CUDA graph."""
     stream = torch.cuda.Stream()
     L, B = wl.layers, wl.batch
     ctx = wl.lengths[0]
@@ -476,8 +476,8 @@ def run_window_cell(kvq, torch, wl, window, steps, warmup, peak):
 
     def step():
         for layer, c in enumerate(caches):
-            c.append(knew[layer], vnew[layer], stream=stream)
-            c.decode(q[layer], scale=wl.scale, out=out[layer], lse=lse[layer], workspace=ws, stream=stream)
+            c.append_decode(knew[layer], vnew[layer], q[layer], scale=wl.scale, out=out[layer], lse=lse[layer],
+                            workspace=ws, stream=stream)
 
     step()
     torch.cuda.synchronize()
@@ -507,8 +507,8 @@ def run_window_cell(kvq, torch, wl, window, steps, warmup, peak):
            "ctx": ctx, "window": window, "steps_per_s": 1000.0 / ms, "ms_per_step": ms,
            "kv_gbs": bytes_step / (ms * 1e-3) / 1e9, "kv_bytes_per_step": bytes_step,
            "pct_hbm_peak": 100.0 * bytes_step / (ms * 1e-3) / 1e9 / peak,
-           "step": "per layer: window append (evict oldest into tail) + one decode over both regions "
-                   "(window and tail splits in one grid, one exact merge)"}
+           "step": "per layer: one launch appends the row (evicting the oldest window row into the tail) "
+                   "and decodes over both regions (window and tail splits in one grid, one exact merge)"}
     if err:
         res["device_error"] = True
     del g

@@ -119,7 +119,7 @@
 extern "C" {
 #endif
 
-#define KVQ_ABI_VERSION 3
+#define KVQ_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define KVQ_API __attribute__((visibility("default")))
@@ -339,6 +339,22 @@ KVQ_API kvq_status kvq_window_workspace_size(const kvq_cache *window, const kvq_
 KVQ_API kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *tail, const float *q,
                                      int32_t n_q_heads, float scale, void *workspace, float *out, float *lse,
                                      void *stream);
+
+/*
+ * One decode step of the window + tail pair: kvq_window_append of k, v followed by
+ * kvq_window_decode of q, with the same arguments, results and errors, in one launch where
+ * the two-region grid is resident at once (one CTA per SM: splits x Hkv x B <= the SM
+ * count) -- the read path's two regions then also take the write path: the window's CTA
+ * that holds the new row's ring slot writes it there before reading that tile, and, once
+ * the window is full, the tail's CTA that holds tail position tail_len first moves the
+ * slot's old row there (quantised from its f16 value) and sets a flag in `workspace` that
+ * the window's CTA waits for (bounded) before it overwrites the slot.  Otherwise the two
+ * calls run one after the other.  `workspace`: kvq_window_workspace_size bytes, zeroed once
+ * (the flags are left at zero).  Same section 5 P2 as above.
+ */
+KVQ_API kvq_status kvq_window_append_decode(kvq_cache *window, kvq_cache *tail, const float *k, const float *v,
+                                            const float *q, int32_t n_q_heads, float scale, void *workspace,
+                                            float *out, float *lse, void *stream);
 
 /*
  * kvq_decode_attention without a caller-provided workspace.  (The pages have no

@@ -72,6 +72,7 @@ def _load():
         "kvq_decode_verify": [vp, vp, i32, i32, ctypes.c_float, i32, vp, vp, vp, vp],
         "kvq_window_workspace_size": [vp, vp, i32, ctypes.POINTER(sz)],
         "kvq_window_decode": [vp, vp, vp, i32, ctypes.c_float, vp, vp, vp, vp],
+        "kvq_window_append_decode": [vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp, vp],
     }
     for name, args in sigs.items():
         fn = getattr(L, name)
@@ -165,6 +166,23 @@ class WindowedCache:
         ws = self.workspace(Hq) if workspace is None else workspace
         _check(lib.kvq_window_decode(self.window.handle, self.tail.handle, _ptr(q), Hq, scale, _ptr(ws), _ptr(out),
                                      _ptr(lse), _stream(stream)), "kvq_window_decode")
+        return out, lse
+
+    def append_decode(self, k, v, q, scale=None, out=None, lse=None, workspace=None, stream=None):
+        """append(k, v) then decode(q) as one step (kvq_window_append_decode): one launch
+        where the two-region grid is resident at once."""
+        for t in (k, v):
+            assert t.dtype == torch.float32 and t.is_contiguous()
+            assert t.numel() == self.batch * self.n_kv_heads * self.head_dim
+        assert q.dtype == torch.float32 and q.is_contiguous() and q.dim() == 3
+        B, Hq, D = q.shape
+        assert B == self.batch and D == self.head_dim
+        scale = 1.0 / math.sqrt(D) if scale is None else scale
+        out = torch.empty_like(q) if out is None else out
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+        ws = self.workspace(Hq) if workspace is None else workspace
+        _check(lib.kvq_window_append_decode(self.window.handle, self.tail.handle, _ptr(k), _ptr(v), _ptr(q), Hq, scale,
+                                            _ptr(ws), _ptr(out), _ptr(lse), _stream(stream)), "kvq_window_append_decode")
         return out, lse
 
     def lengths(self):

@@ -686,10 +686,12 @@ static bool dual_splits(const kvq_cache *window, const kvq_cache *tail, int32_t 
 }
 
 // Workspace of a window + tail decode: one decode workspace, used by the window's decode
-// and then by the tail's (each leaves its counters at zero), and the window's result; or,
-// for the one-launch form, one decode workspace over the splits of both regions.
+// and then by the tail's (each leaves its counters at zero), and the window's result at
+// *res_off; or, for the one-launch form, one decode workspace over the splits of both
+// regions, whichever is larger.  Then the eviction flags of kvq_window_append_decode
+// ([B][Hkv] int32, left at zero) at *flag_off.
 static size_t window_ws(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads, int sw, int stl,
-                        size_t *res_off) {
+                        size_t *res_off, size_t *flag_off = nullptr) {
     const size_t wsz = ws_layout(window, n_q_heads, sw).total, tsz = ws_layout(tail, n_q_heads, stl).total;
     const size_t rows = static_cast<size_t>(window->desc.batch) * n_q_heads;
     *res_off = align256(wsz > tsz ? wsz : tsz);
@@ -699,7 +701,9 @@ static size_t window_ws(const kvq_cache *window, const kvq_cache *tail, int32_t 
         const size_t d = ws_layout(tail, n_q_heads, S).total;
         if (d > total) total = d;
     }
-    return total;
+    total = align256(total);
+    if (flag_off) *flag_off = total;
+    return total + align256(static_cast<size_t>(window->desc.batch) * window->desc.n_kv_heads * 4);
 }
 
 kvq_status kvq_window_workspace_size(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads,
@@ -764,6 +768,73 @@ kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *tail, con
         p.early = track_launch(cs, region[r], nullptr) ? 1 : 0;
         if (kvq::launch_decode(region[r]->desc.type_k, region[r]->desc.type_v, p, true, cs) != cudaSuccess)
             return KVQ_ERR_CUDA;
+    }
+    return KVQ_OK;
+}
+
+kvq_status kvq_window_append_decode(kvq_cache *window, kvq_cache *tail, const float *k, const float *v,
+                                    const float *q, int32_t n_q_heads, float scale, void *workspace, float *out,
+                                    float *lse, void *stream) {
+    kvq_status st = check_window_pair(window, tail);
+    if (st != KVQ_OK) return st;
+    if (!k || !v || !q || !workspace || !out) return KVQ_ERR_INVALID_ARG;
+    int sw = 0, stl = 0;
+    st = window_splits(window, tail, n_q_heads, &sw, &stl);
+    if (st != KVQ_OK) return st;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out) || !aligned16(workspace) ||
+        (lse && !aligned16(lse)))
+        return KVQ_ERR_ALIGNMENT;
+    const int W = window->desc.capacity;
+    for (int b = 0; b < window->desc.batch; ++b)
+        if (window->h_len[b] >= W && static_cast<long long>(tail->h_len[b]) + 1 > tail->desc.capacity)
+            return KVQ_ERR_CAPACITY;
+    auto two_launches = [&]() {
+        kvq_status s2 = kvq_window_append(window, tail, k, v, stream);
+        if (s2 != KVQ_OK) return s2;
+        return kvq_window_decode(window, tail, q, n_q_heads, scale, workspace, out, lse, stream);
+    };
+    int nw = 0, S = 0;
+    // one launch needs one CTA per (split, KV head, sequence): at most 8 query heads per KV head
+    if (n_q_heads / window->desc.n_kv_heads > kvq::kMaxRowsPerGroup || !dual_splits(window, tail, n_q_heads, &nw, &S))
+        return two_launches();
+    size_t res_off = 0, flag_off = 0;
+    window_ws(window, tail, n_q_heads, sw, stl, &res_off, &flag_off);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const WsLayout w = ws_layout(tail, n_q_heads, S);
+    kvq::DecodeParams pr[2] = {base_params(window, q, n_q_heads, scale, nw), base_params(tail, q, n_q_heads, scale, S - nw)};
+    for (int r = 0; r < 2; ++r) {
+        kvq::DecodeParams &p = pr[r];
+        p.out = out;
+        p.lse = lse;
+        set_workspace(p, ws, w);
+        p.part_stride = S;
+        p.part_base = r == 0 ? 0 : nw;
+        p.merge_slots = S;
+        p.win = r + 1;
+        p.wl_len = window->state;
+        p.tl_len = tail->state;
+        p.wl_err = window->state + window->desc.batch + 1;
+        p.tl_err = tail->state + tail->desc.batch + 1;
+        p.wl_cap = W;
+        p.tl_cap = tail->desc.capacity;
+        p.win_k = window->k_mem;
+        p.win_v = window->v_mem;
+        p.evict = reinterpret_cast<int32_t *>(ws + flag_off);
+        p.ticket = window->state + window->desc.batch;  // one ticket for the whole grid
+    }
+    pr[0].k_new = k;
+    pr[0].v_new = v;
+    pr[0].early = pr[1].early = track_launch(cs, window, window, tail, tail) ? 1 : 0;
+    const cudaError_t e =
+        kvq::launch_window_dual(tail->desc.type_k, tail->desc.type_v, window->desc.head_dim, pr[0], pr[1], nw, cs);
+    if (e == cudaErrorCooperativeLaunchTooLarge) return two_launches();  // not resident at once: nothing launched
+    if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    for (int b = 0; b < window->desc.batch; ++b) {
+        if (window->h_len[b] < W)
+            window->h_len[b] += 1;
+        else
+            tail->h_len[b] += 1;
     }
     return KVQ_OK;
 }

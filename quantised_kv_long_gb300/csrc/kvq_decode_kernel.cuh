@@ -389,6 +389,49 @@ __device__ __noinline__ void grid_ticket(const DecodeParams &p, int cap_rows) {
     *p.ticket = 0;
 }
 
+// Two-region append (kvq_window_append_decode): the last CTA of the grid advances, per
+// sequence, the window's length while it fills, then the tail's (its evicted row), or
+// reports KVQ_DEVERR_CAPACITY.  Called by one thread per CTA, once.
+__device__ __noinline__ void window_ticket(const DecodeParams &p) {
+    __threadfence();
+    const int total = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
+    if (atomicAdd(p.ticket, 1) != total - 1) return;
+    __threadfence();
+    for (int b = 0; b < p.B; ++b) {
+        const int Lw = __ldcg(p.wl_len + b), Lt = __ldcg(p.tl_len + b);
+        if (Lw < 0 || Lw > p.wl_cap || Lt < 0)
+            atomicOr(p.wl_err, KVQ_DEVERR_CAPACITY);
+        else if (Lw < p.wl_cap)
+            p.wl_len[b] = Lw + 1;
+        else if (Lt + 1 <= p.tl_cap)
+            p.tl_len[b] = Lt + 1;
+        else
+            atomicOr(p.tl_err, KVQ_DEVERR_CAPACITY);
+    }
+    *p.ticket = 0;
+}
+__device__ __forceinline__ void append_ticket(const DecodeParams &p, int cap_rows) {
+    if (p.win)
+        window_ticket(p);
+    else
+        grid_ticket(p, cap_rows);
+}
+
+// Wait (one thread) until *flag is non-zero, then clear it; reports KVQ_DEVERR_TIMEOUT past
+// `report` SM cycles and gives up after kWaitCycles.
+__device__ __forceinline__ void wait_flag_clear(int32_t *flag, long long report, int32_t *err) {
+    const long long t0 = clock64();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
+        if (v) break;
+        if (clock64() - t0 > kWaitCycles) break;
+        __nanosleep(64);
+    }
+    if (clock64() - t0 > report) atomicOr(err, KVQ_DEVERR_TIMEOUT);
+    atomicExch(flag, 0);
+}
+
 template <int KT, int VT, int NS, int TW_ = 0>
 struct Cfg {
     // tile-warps per 128-value slice: 11 for 128-wide heads with quantised keys (the
@@ -817,10 +860,32 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     }
     int L_old = __ldcg(p.len + bseq);
     L_old = L_old < 0 ? 0 : (L_old > cap_rows ? cap_rows : L_old);
-    // fused append: the new row lands at position L_old and is attended to
-    const bool appending = p.k_new != nullptr;
-    const bool do_app = appending && L_old + 1 <= cap_rows;
-    const int L = do_app ? L_old + 1 : L_old;
+    // fused append: the new row lands at position L_old and is attended to.  Two-region
+    // append: the window's new row lands in ring slot (tail + window length) mod capacity
+    // (the oldest row once the window is full), and a full window's oldest row is moved, as
+    // the tail's new row, to tail position t_len (quantised from its f16 value)
+    const bool appending = p.k_new != nullptr || p.win != 0;
+    bool do_app, win_full = false;
+    int L, app_row = L_old;
+    if (p.win == 0) {
+        do_app = appending && L_old + 1 <= cap_rows;
+        L = do_app ? L_old + 1 : L_old;
+    } else {
+        int Lw = __ldcg(p.wl_len + bseq), Lt = __ldcg(p.tl_len + bseq);
+        Lw = Lw < 0 ? 0 : (Lw > p.wl_cap ? p.wl_cap : Lw);
+        Lt = Lt < 0 ? 0 : (Lt > p.tl_cap ? p.tl_cap : Lt);
+        win_full = Lw >= p.wl_cap;
+        const bool room = !win_full || Lt + 1 <= p.tl_cap;
+        if (p.win == 1) {
+            do_app = room;
+            app_row = static_cast<int>((static_cast<long long>(Lt) + Lw) % p.wl_cap);
+            L = do_app && !win_full ? Lw + 1 : Lw;
+        } else {
+            do_app = win_full && room;
+            app_row = Lt;
+            L = do_app ? Lt + 1 : Lt;
+        }
+    }
     const int T = (L + kTileRows - 1) / kTileRows;
     const int ns = max(1, min(p.n_splits, T));
     const int tps = T > 0 ? (T + ns - 1) / ns : 0;
@@ -836,7 +901,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     if (split >= ns && p.merge_slots == 0) {
         if (early) grid_dep_wait();
         grid_dep_launch();
-        if (appending && threadIdx.x == 0) grid_ticket(p, cap_rows);
+        if (appending && threadIdx.x == 0) append_ticket(p, cap_rows);
         if (!fused) {  // partials mode: splits beyond ns are empty triples
             for (int idx = threadIdx.x; idx < rows * (p.D / 4); idx += blockDim.x) {
                 const int g = idx / (p.D / 4), dq = idx % (p.D / 4);
@@ -864,10 +929,11 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
 
     if (warp == 0) {
         // ---------------- producer ----------------
-        // In fused-append mode the CTA whose split holds the last tile first writes the new
-        // row of its KV head into that tile (all 32 lanes quantise), then copies it in.
-        const bool owner = do_app && t_begin < T && t_end == T;
-        const int app_stage = owner ? (T - 1 - t_begin) / C::TWT : -1;
+        // In fused-append mode the CTA whose split holds the appended row's tile first writes
+        // the row of its KV head into that tile (all 32 lanes quantise), then copies it in.
+        const int app_tile = app_row >> 4;
+        const bool owner = do_app && app_tile >= t_begin && app_tile < t_end;
+        const int app_stage = owner ? (app_tile - t_begin) / C::TWT : -1;
         int issued_use[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) issued_use[i] = -1;
@@ -900,6 +966,33 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             grid_dep_wait();
         }
         grid_dep_launch();
+        if (p.win == 2 && owner) {
+            // The tail's new row is the window's oldest (slot t_len mod capacity), read as f16
+            // and quantised into tail position t_len first of all, so that the window's CTA,
+            // which waits for the flag before it overwrites the slot, is not held up; this
+            // CTA copies that tile in only at its own stage, after this write.
+            const size_t tile = bh_tile + app_tile;
+            const int ws_row = app_row % p.wl_cap;
+            const size_t wtile = (static_cast<size_t>(bseq) * p.Hkv + h) * (p.wl_cap / kTileRows) + (ws_row >> 4);
+#pragma unroll
+            for (int s2 = 0; s2 < NS; ++s2) {
+                const float4 xk = load_f16_row<false>(p.win_k + (wtile * NS + s2) * code_tile_bytes(KVQ_F16), ws_row & 15, lane);
+                const float4 xv = load_f16_row<true>(p.win_v + (wtile * NS + s2) * code_tile_bytes(KVQ_F16), ws_row & 15, lane);
+                quantize_store_vals<KT, false>(xk, const_cast<uint8_t *>(p.k_codes) + tile * C::KC + s2 * code_tile_bytes(KT),
+                                               const_cast<uint8_t *>(p.k_scales) + tile * C::KS + s2 * scale_tile_bytes(KT),
+                                               app_row & 15, lane);
+                quantize_store_vals<VT, true>(xv, const_cast<uint8_t *>(p.v_codes) + tile * C::VC + s2 * code_tile_bytes(VT),
+                                              const_cast<uint8_t *>(p.v_scales) + tile * C::VS + s2 * scale_tile_bytes(VT),
+                                              app_row & 15, lane);
+            }
+            // before the bulk copy (async proxy) of that tile at its stage
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {  // the slot may now be overwritten
+                __threadfence();
+                atomicExch(p.evict + static_cast<size_t>(bseq) * p.Hkv + h, 1);
+            }
+        }
         bool ok = true;
         int slot = k0 == C::STAGES ? 0 : k0, use = k0 == C::STAGES ? 1 : 0;
         for (int k = k0; k < n_stage; ++k) {
@@ -913,9 +1006,13 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
                 ok = false;
                 break;
             }
-            if (k == app_stage) {
-                const size_t tile = bh_tile + (L_old >> 4);
-                const int kt = L_old & 15;
+            if (k == app_stage && p.win != 2) {
+                const size_t tile = bh_tile + app_tile;
+                const int kt = app_row & 15;
+                // a full window's slot is overwritten only once the tail holds its old row
+                if (p.win == 1 && win_full && lane == 0)
+                    wait_flag_clear(p.evict + static_cast<size_t>(bseq) * p.Hkv + h, p.wait_cycles, p.err);
+                __syncwarp();
                 const float *kx = p.k_new + (static_cast<size_t>(bseq) * p.Hkv + h) * p.D;
                 const float *vx = p.v_new + (static_cast<size_t>(bseq) * p.Hkv + h) * p.D;
 #pragma unroll
@@ -939,7 +1036,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
             }
         }
         // the length advance of a fused append, off the consumers' critical path
-        if (appending && lane == 0) grid_ticket(p, cap_rows);
+        if (appending && lane == 0) append_ticket(p, cap_rows);
         if (!ok && lane == 0) {
             s_timeout = 1;
             // let the copies already issued land before the CTA can exit
@@ -1415,6 +1512,8 @@ cudaError_t launch_dual_t(const DecodeParams &pw, const DecodeParams &pt, int nw
     DecodeParams a = pw, b = pt;
     const long long ctas = static_cast<long long>(pt.merge_slots) * pt.Hkv * pt.B * pt.QG;
     a.wide = b.wide = ctas <= static_cast<long long>(occ_cached[dev]) * sms ? 1 : 0;
+    // the two-region append has CTAs wait on one another: only for a grid resident at once
+    if (pw.win && !a.wide) return cudaErrorCooperativeLaunchTooLarge;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pt.merge_slots, pt.Hkv, pt.B * pt.QG);
     cfg.blockDim = dim3(C::THREADS);

@@ -94,13 +94,25 @@ struct DecodeParams {
     // whose merge_slots splits all publish a triple (empty ones too) at part_base + split of
     // part_stride slots per row, merged as one set.
     int merge_slots;
-    // SM clock cycles a pipeline or merge wait may take before it gives up (kWaitCycles
-    // unless the caller set a limit with kvq_set_wait_limit)
+    // SM clock cycles after which a pipeline or merge wait reports KVQ_DEVERR_TIMEOUT
+    // (kWaitCycles unless the caller set a limit with kvq_set_wait_limit)
     long long wait_cycles;
     // optional launch timing: CTA c (linear index < stamp_ctas) writes its %globaltimer at
-    // four points to stamps[4c .. 4c + 3]; nullptr: no stamps
+    // its start and exit to stamps[2c], stamps[2c + 1]; nullptr: no stamps
     unsigned long long *stamps;
     int stamp_ctas;
+    // Window + tail append in the two-region launch (kvq_window_append_decode).  win: 1 in
+    // the window region's parameters, 2 in the tail's, 0 otherwise.  wl_len / tl_len and
+    // wl_err / tl_err: the window's and the tail's lengths and error words; wl_cap / tl_cap
+    // their capacities (rows); win_k / win_v: the window planes, where the tail region reads
+    // the row it evicts; evict: [B][Hkv] flags in the workspace, set by the tail CTA that
+    // has written an evicted row and cleared by the window CTA that then overwrites its slot.
+    // ticket: the window's arrival ticket, shared by both regions.
+    int win;
+    int32_t *wl_len, *tl_len, *wl_err, *tl_err;
+    int wl_cap, tl_cap;
+    const uint8_t *win_k, *win_v;
+    int32_t *evict;
 };
 
 struct AppendParams {

@@ -145,3 +145,108 @@ def test_window_graph_replay(kvq):
         assert cache.window.sync_lengths() == [W] and cache.tail.sync_lengths() == [n - W]
         ref, _ = reference("q8_0", "q4_0", Xk_h[0], Xv_h[0], n, W, qh[0], wl.scale)
         assert np.abs(out[0].cpu().numpy() - ref).max() <= TOL, s
+
+
+def rows_of(wl, kind, B, H, N):
+    return torch.stack([torch.stack([syn.kv_rows(wl, kind, 0, b, h, 0, N) for h in range(H)]) for b in range(B)])
+
+
+@pytest.mark.parametrize("tk,tv,D,G", [("q8_0", "q4_0", 128, 5), ("q8_0", "q8_0", 256, 8), ("q4_0", "q4_0", 128, 4),
+                                    ("f16", "q4_0", 256, 2), ("q4_0", "q8_0", 256, 12)])
+def test_window_append_decode_one_step(kvq, tk, tv, D, G):
+    """kvq_window_append_decode: the write path and the read path of one token in one launch
+    (G <= 8; G = 12 takes the two-launch form).  Every step's output equals, bit for bit,
+    that of a second pair driven by the separate append and decode calls, and matches the
+    oracle at checkpoints; the tail's codes are bit-exact and the window holds token t in
+    slot t mod W."""
+    B, H, W, N = 2, 2, 32, 90
+    wl = syn.Workload("window1", 1, B, H * G, H, D, tk, tv, (N, N), seed=70 + D + G)
+    Xk, Xv = rows_of(wl, syn.KIND_K, B, H, N), rows_of(wl, syn.KIND_V, B, H, N)
+    fused = kvq.WindowedCache(B, H, D, W, 96, tk, tv)
+    split = kvq.WindowedCache(B, H, D, W, 96, tk, tv)
+    ws = fused.workspace(H * G)
+    Xk_h, Xv_h = Xk.cpu().numpy(), Xv.cpu().numpy()
+    checkpoints = {1, 17, W, W + 1, 63, N}
+    for t in range(N):
+        n = t + 1
+        q = syn.queries(wl, 0, step=n)
+        out, lse = fused.append_decode(Xk[:, :, t].contiguous(), Xv[:, :, t].contiguous(), q, scale=wl.scale,
+                                       workspace=ws)
+        split.append(Xk[:, :, t].contiguous(), Xv[:, :, t].contiguous())
+        out2, lse2 = split.decode(q, scale=wl.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2) and torch.equal(lse, lse2), n
+        assert fused.lengths() == ([min(n, W)] * B, [max(0, n - W)] * B)
+        if n not in checkpoints:
+            continue
+        assert fused.window.sync_lengths() == [min(n, W)] * B and fused.tail.sync_lengths() == [max(0, n - W)] * B
+        qh = q.cpu().numpy()
+        for b in range(B):
+            ref, ref_lse = reference(tk, tv, Xk_h[b], Xv_h[b], n, W, qh[b], wl.scale)
+            assert np.abs(out[b].cpu().numpy() - ref).max() <= TOL, (n, b)
+            assert np.abs(lse[b].cpu().numpy() - ref_lse).max() <= TOL, (n, b)
+    assert fused.window.read_error() == 0 and fused.tail.read_error() == 0
+    assert torch.count_nonzero(ws[-256:]) == 0  # the eviction flags are left at zero
+    tkc, tks, tvc, tvs = natural(fused.tail)
+    ok, osk = oracle.quantize(tk, f16_round(Xk_h[:, :, :N - W]))
+    ov, osv = oracle.quantize(tv, f16_round(Xv_h[:, :, :N - W]))
+    assert np.array_equal(tkc[:, :, :N - W], ok) and np.array_equal(tks[:, :, :N - W], osk)
+    assert np.array_equal(tvc[:, :, :N - W], ov) and np.array_equal(tvs[:, :, :N - W], osv)
+    wkc, _, wvc, _ = natural(fused.window)
+    for t in range(N - W, N):
+        assert np.array_equal(wkc[:, :, t % W], oracle.quantize("f16", Xk_h[:, :, t])[0])
+        assert np.array_equal(wvc[:, :, t % W], oracle.quantize("f16", Xv_h[:, :, t])[0])
+
+
+def test_window_append_decode_graph_replay(kvq):
+    """The one-launch step captured once and replayed across the window's fill and its
+    first evictions: lengths, ring slot and eviction flags advance on the device."""
+    B, H, D, G, W = 1, 2, 256, 8, 32
+    N0, steps = 20, 30
+    wl = syn.Workload("window1g", 1, B, H * G, H, D, "q8_0", "q8_0", (N0 + steps,), seed=9)
+    Xk, Xv = rows_of(wl, syn.KIND_K, B, H, N0 + steps), rows_of(wl, syn.KIND_V, B, H, N0 + steps)
+    cache = kvq.WindowedCache(B, H, D, W, 64, "q8_0", "q8_0")
+    for t in range(N0):
+        cache.append(Xk[:, :, t].contiguous(), Xv[:, :, t].contiguous())
+    kn = torch.empty((B, H, D), device="cuda")
+    vn = torch.empty((B, H, D), device="cuda")
+    q = syn.queries(wl, 0)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H * G), device="cuda")
+    ws = cache.workspace(H * G)
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        cache.append_decode(kn, vn, q, scale=wl.scale, out=out, lse=lse, workspace=ws, stream=st)
+    torch.cuda.synchronize()
+    cache.window.sync_lengths()
+    cache.tail.sync_lengths()
+    Xk_h, Xv_h, qh = Xk.cpu().numpy(), Xv.cpu().numpy(), q.cpu().numpy()
+    for s in range(steps):
+        kn.copy_(Xk[:, :, N0 + s])
+        vn.copy_(Xv[:, :, N0 + s])
+        g.replay()
+        torch.cuda.synchronize()
+        n = N0 + s + 1
+        assert cache.window.sync_lengths() == [min(n, W)] and cache.tail.sync_lengths() == [max(0, n - W)]
+        ref, ref_lse = reference("q8_0", "q8_0", Xk_h[0], Xv_h[0], n, W, qh[0], wl.scale)
+        assert np.abs(out[0].cpu().numpy() - ref).max() <= TOL, s
+        assert np.abs(lse[0].cpu().numpy() - ref_lse).max() <= TOL, s
+    assert cache.window.read_error() == 0 and cache.tail.read_error() == 0
+
+
+def test_window_append_decode_capacity(kvq):
+    """A full window with a full tail: refused on the host, nothing written."""
+    B, H, D, W = 1, 2, 128, 16
+    cache = kvq.WindowedCache(B, H, D, W, 32, "q8_0", "q8_0")
+    x = torch.randn((B, H, D), device="cuda")
+    q = torch.randn((B, 2 * H, D), device="cuda")
+    for _ in range(W + 32):
+        cache.append_decode(x, x, q)
+    with pytest.raises(kvq.KvqError) as e:
+        cache.append_decode(x, x, q)
+    assert e.value.status == 3
+    assert cache.lengths() == ([W], [32])
+    torch.cuda.synchronize()
+    assert cache.window.read_error() == 0 and cache.tail.read_error() == 0

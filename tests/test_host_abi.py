@@ -21,7 +21,7 @@ def test_library_exports_every_header_symbol():
     for n in names:
         assert n in exported, n
         assert hasattr(kvq.lib, n)
-    assert kvq.lib.kvq_abi_version() == 3
+    assert kvq.lib.kvq_abi_version() == 4
 
 
 def test_status_strings():
