@@ -350,7 +350,8 @@ KVQ_API kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *t
  * slot's old row there (quantised from its f16 value) and sets a flag in `workspace` that
  * the window's CTA waits for (bounded) before it overwrites the slot.  Otherwise the two
  * calls run one after the other.  `workspace`: kvq_window_workspace_size bytes, zeroed once
- * (the flags are left at zero).  Same section 5 P2 as above.
+ * (the flags are left at zero; zero it again after a wait gave up, i.e. after
+ * KVQ_DEVERR_TIMEOUT from a wait of about two seconds).  Same section 5 P2 as above.
  */
 KVQ_API kvq_status kvq_window_append_decode(kvq_cache *window, kvq_cache *tail, const float *k, const float *v,
                                             const float *q, int32_t n_q_heads, float scale, void *workspace,

@@ -7,6 +7,9 @@ front of a quantised tail ("HAL #582 -- per-layer KV compression study", section
 * Read path: decode over both regions matches the oracle's two-region result (split
   triples of each region, merged by the oracle's exact combine) within 1e-3, through the
   one-launch form (both regions' splits in one grid and one merge) at D = 128 and 256.
+* One step in one launch (kvq_window_append_decode): bit-identical to the separate append
+  and decode, the same pins as above, graph replay across the window's fill and first
+  evictions, capacity refusal, and slow waits reported without losing exactness.
 """
 import numpy as np
 import pytest
@@ -250,3 +253,44 @@ def test_window_append_decode_capacity(kvq):
     assert cache.lengths() == ([W], [32])
     torch.cuda.synchronize()
     assert cache.window.read_error() == 0 and cache.tail.read_error() == 0
+
+
+def test_window_append_decode_wait_reported(kvq):
+    """With a wait limit far below a copy's latency every slow wait of the one-launch step
+    (ring waits, the merge, the window CTA's wait for the evicted row) is reported as
+    KVQ_DEVERR_TIMEOUT and then completed: the step's result is still exact, the lengths
+    advance, the eviction flags end at zero, and the next step with the default limit
+    reports nothing."""
+    B, H, D, G, W, N = 1, 2, 256, 8, 32, 192  # N a multiple of W: the window's slot 0 holds its oldest token
+    wl = syn.Workload("window-timeout", 1, B, H * G, H, D, "q8_0", "q8_0", (N + 2,), seed=62)
+    Xk, Xv = rows_of(wl, syn.KIND_K, B, H, N + 2), rows_of(wl, syn.KIND_V, B, H, N + 2)
+    cache = kvq.WindowedCache(B, H, D, W, 256, "q8_0", "q8_0")
+    # the tail holds evicted tokens, quantised from their f16 values
+    cache.tail.append(Xk[:, :, :N - W].half().float().contiguous(), Xv[:, :, :N - W].half().float().contiguous())
+    cache.window.append(Xk[:, :, N - W:N].contiguous(), Xv[:, :, N - W:N].contiguous())
+    ws = cache.workspace(H * G)
+    q = syn.queries(wl, 0)
+    torch.cuda.synchronize()
+    assert cache.window.read_error() == 0 and cache.tail.read_error() == 0
+    Xk_h, Xv_h, qh = Xk.cpu().numpy(), Xv.cpu().numpy(), q.cpu().numpy()
+    kvq.set_wait_limit(64)
+    try:
+        out, lse = cache.append_decode(Xk[:, :, N].contiguous(), Xv[:, :, N].contiguous(), q, scale=wl.scale,
+                                       workspace=ws)
+    finally:
+        kvq.set_wait_limit(0)
+    torch.cuda.synchronize()
+    assert cache.window.read_error() == kvq.DEVERR_TIMEOUT
+    assert cache.tail.read_error() in (0, kvq.DEVERR_TIMEOUT)
+    assert torch.count_nonzero(ws[-256:]) == 0
+    assert cache.window.sync_lengths() == [W] and cache.tail.sync_lengths() == [N - W + 1]
+    ref, ref_lse = reference("q8_0", "q8_0", Xk_h[0], Xv_h[0], N + 1, W, qh[0], wl.scale)
+    assert np.abs(out[0].cpu().numpy() - ref).max() <= TOL
+    assert np.abs(lse[0].cpu().numpy() - ref_lse).max() <= TOL
+    out, lse = cache.append_decode(Xk[:, :, N + 1].contiguous(), Xv[:, :, N + 1].contiguous(), q, scale=wl.scale,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    assert cache.window.read_error() == 0 and cache.tail.read_error() == 0
+    ref, ref_lse = reference("q8_0", "q8_0", Xk_h[0], Xv_h[0], N + 2, W, qh[0], wl.scale)
+    assert np.abs(out[0].cpu().numpy() - ref).max() <= TOL
+    assert np.abs(lse[0].cpu().numpy() - ref_lse).max() <= TOL
