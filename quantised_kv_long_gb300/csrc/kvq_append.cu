@@ -237,19 +237,46 @@ __device__ __forceinline__ void quantize_block_store(const float (&x)[kBlock], u
 // threads of a tile CTA: one per (K or V, row, block): 2 x 16 x 4
 constexpr int kTileThreads = 2 * kTileRows * (kSlice / kBlock);
 
+// CTAs of the tile kernel per SM: each loops over items; every thread copies its 32 input
+// values of the next item into its own shared-memory slot (asynchronous 16-byte copies)
+// while it quantises the current one, so that every CTA keeps a load in flight without
+// holding it in registers
+constexpr int kTileCtasPerSm = 6;
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
 template <int KT, int VT>
-__global__ void __launch_bounds__(kTileThreads) append_tiles_kernel(const AppendParams p, const int tiles_per_seq) {
+__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) append_tiles_kernel(const AppendParams p,
+                                                                                    const int tiles_per_seq) {
     constexpr int KC = code_tile_bytes(KT), VC = code_tile_bytes(VT);
     constexpr int KS = scale_tile_bytes(KT), VS = scale_tile_bytes(VT);
     constexpr int BYTES = KC + VC + KS + VS;
     __shared__ __align__(16) uint8_t img[BYTES];
+    // each thread's 8 input chunks of 16 bytes, chunk i at place i ^ (thread mod 8), so that
+    // the 8 threads of a 128-bit shared access touch 8 different bank groups
+    __shared__ __align__(16) float4 stage[kTileThreads * (kBlock / 4)];
     __shared__ int s_last;
     const bool is_v = threadIdx.x >= kTileThreads / 2;  // warp-uniform
     const int rb = threadIdx.x % (kTileThreads / 2);
     const int kt = rb >> 2, b = rb & 3;                 // row of the tile, block of the slice
     const int NS = p.D / kSlice;
     const long long items = static_cast<long long>(p.nb) * p.Hkv * NS * tiles_per_seq;
-    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+    float4 *slot = stage + threadIdx.x * (kBlock / 4);
+    const int swz = threadIdx.x & 7;
+    // An item's tile slice (ts), its first position r0, the sequence's length L and this
+    // thread's 32 input values (src: nullptr where its row is not appended); false for an
+    // item with nothing to write (past the append, or a sequence without room, which the
+    // last CTA reports).
+    struct Item {
+        size_t ts;
+        int r0, L;
+        const float4 *src;
+    };
+    auto locate = [&](long long it, Item &m) -> bool {
         const int ti = static_cast<int>(it % tiles_per_seq);
         long long rest = it / tiles_per_seq;
         const int sl = static_cast<int>(rest % NS);
@@ -257,56 +284,84 @@ __global__ void __launch_bounds__(kTileThreads) append_tiles_kernel(const Append
         const int h = static_cast<int>(rest % p.Hkv);
         const int bl = static_cast<int>(rest / p.Hkv);
         const int bseq = p.b0 + bl;
-        const int L = __ldcg(p.len + bseq);
-        if (L < 0 || L + p.n_new > p.cap) continue;  // block-uniform: the last CTA reports it
-        const int tile = (L >> 4) + ti;
-        const int r0 = tile * kTileRows;               // first position of the tile
-        if (r0 >= L + p.n_new) continue;               // past the append
-        const size_t ts = ((static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + tile) * NS + sl;
-        uint8_t *gk = p.k_codes + ts * KC, *gv = p.v_codes + ts * VC;
-        uint8_t *gks = KS ? p.k_scales + ts * KS : nullptr, *gvs = VS ? p.v_scales + ts * VS : nullptr;
-        auto region = [&](int o, uint8_t *&g, int &off) {  // global place of image byte o
-            if (o < KC) { g = gk; off = o; }
-            else if (o < KC + VC) { g = gv; off = o - KC; }
-            else if (o < KC + VC + KS) { g = gks; off = o - KC - VC; }
-            else { g = gvs; off = o - KC - VC - KS; }
-        };
-        const bool partial = r0 < L || r0 + kTileRows > L + p.n_new;
-        __syncthreads();  // the previous item's image has been written out
-        if (partial) {    // keep the rows of the tile that this append does not write
-            for (int o = threadIdx.x * 16; o < BYTES; o += blockDim.x * 16) {
-                uint8_t *g;
-                int off;
-                region(o, g, off);
-                *reinterpret_cast<uint4 *>(img + o) = __ldcg(reinterpret_cast<const uint4 *>(g + off));
-            }
-            __syncthreads();
-        }
-        const int pos = r0 + kt;
-        if (pos >= L && pos < L + p.n_new) {
-            const size_t src = ((static_cast<size_t>(bl) * p.Hkv + h) * p.n_new + (pos - L)) * p.D + sl * kSlice + kBlock * b;
-            const float4 *x4 = reinterpret_cast<const float4 *>((is_v ? p.v : p.k) + src);
-            float x[kBlock];
+        m.L = __ldcg(p.len + bseq);
+        if (m.L < 0 || m.L + p.n_new > p.cap) return false;
+        const int tile = (m.L >> 4) + ti;
+        m.r0 = tile * kTileRows;
+        if (m.r0 >= m.L + p.n_new) return false;
+        m.ts = ((static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + tile) * NS + sl;
+        const int pos = m.r0 + kt;
+        m.src = nullptr;
+        if (pos >= m.L && pos < m.L + p.n_new)
+            m.src = reinterpret_cast<const float4 *>(
+                (is_v ? p.v : p.k) +
+                ((static_cast<size_t>(bl) * p.Hkv + h) * p.n_new + (pos - m.L)) * p.D + sl * kSlice + kBlock * b);
+        return true;
+    };
+    auto prefetch = [&](const float4 *src) {
+#pragma unroll
+        for (int i = 0; i < kBlock / 4; ++i) cp_async16(slot + (i ^ swz), src + i);
+        cp_async_commit();
+    };
+    long long it = blockIdx.x;
+    Item cur{};
+    bool live = it < items && locate(it, cur);
+    if (live && cur.src) prefetch(cur.src);
+    while (it < items) {
+        float x[kBlock];
+        if (live && cur.src) {  // this thread's own slot only: no barrier needed
+            cp_async_wait_all();
 #pragma unroll
             for (int i = 0; i < kBlock / 4; ++i) {
-                const float4 v = __ldcs(x4 + i);
+                const float4 v = slot[i ^ swz];
                 x[4 * i] = v.x;
                 x[4 * i + 1] = v.y;
                 x[4 * i + 2] = v.z;
                 x[4 * i + 3] = v.w;
             }
-            if (!is_v)
-                quantize_block_store<KT, false>(x, img, img + KC + VC, kt, b);
-            else
-                quantize_block_store<VT, true>(x, img + KC, img + KC + VC + KS, kt, b);
         }
-        __syncthreads();
-        for (int o = threadIdx.x * 16; o < BYTES; o += blockDim.x * 16) {
-            uint8_t *g;
-            int off;
-            region(o, g, off);
-            *reinterpret_cast<uint4 *>(g + off) = *reinterpret_cast<const uint4 *>(img + o);
+        // the next item's values are requested before this one is quantised
+        const long long nx = it + gridDim.x;
+        Item nxt{};
+        const bool live_n = nx < items && locate(nx, nxt);
+        if (live_n && nxt.src) prefetch(nxt.src);
+        if (live) {  // block-uniform
+            uint8_t *gk = p.k_codes + cur.ts * KC, *gv = p.v_codes + cur.ts * VC;
+            uint8_t *gks = KS ? p.k_scales + cur.ts * KS : nullptr, *gvs = VS ? p.v_scales + cur.ts * VS : nullptr;
+            auto region = [&](int o, uint8_t *&g, int &off) {  // global place of image byte o
+                if (o < KC) { g = gk; off = o; }
+                else if (o < KC + VC) { g = gv; off = o - KC; }
+                else if (o < KC + VC + KS) { g = gks; off = o - KC - VC; }
+                else { g = gvs; off = o - KC - VC - KS; }
+            };
+            const bool partial = cur.r0 < cur.L || cur.r0 + kTileRows > cur.L + p.n_new;
+            __syncthreads();  // the previous item's image has been written out
+            if (partial) {    // keep the rows of the tile that this append does not write
+                for (int o = threadIdx.x * 16; o < BYTES; o += blockDim.x * 16) {
+                    uint8_t *g;
+                    int off;
+                    region(o, g, off);
+                    *reinterpret_cast<uint4 *>(img + o) = __ldcg(reinterpret_cast<const uint4 *>(g + off));
+                }
+                __syncthreads();
+            }
+            if (cur.src) {
+                if (!is_v)
+                    quantize_block_store<KT, false>(x, img, img + KC + VC, kt, b);
+                else
+                    quantize_block_store<VT, true>(x, img + KC, img + KC + VC + KS, kt, b);
+            }
+            __syncthreads();
+            for (int o = threadIdx.x * 16; o < BYTES; o += blockDim.x * 16) {
+                uint8_t *g;
+                int off;
+                region(o, g, off);
+                *reinterpret_cast<uint4 *>(g + off) = *reinterpret_cast<const uint4 *>(img + o);
+            }
         }
+        it = nx;
+        live = live_n;
+        cur = nxt;
     }
     // the last CTA (all others have read len[] by now) advances the lengths
     __syncthreads();
@@ -337,7 +392,7 @@ cudaError_t launch_append_t(const AppendParams &p, cudaStream_t stream) {
         // most (n_new + 14) / 16 + 1 (L % 16 = 15); items past the append return at once
         const int tiles_per_seq = (p.n_new + kTileRows - 2) / kTileRows + 1;
         const long long items = static_cast<long long>(p.nb) * p.Hkv * (p.D / kSlice) * tiles_per_seq;
-        const long long blocks = items < 12 * 152 ? items : 12 * 152;
+        const long long blocks = items < kTileCtasPerSm * 152 ? items : kTileCtasPerSm * 152;
         append_tiles_kernel<KT, VT><<<static_cast<unsigned>(blocks), kTileThreads, 0, stream>>>(p, tiles_per_seq);
         return cudaGetLastError();
     }
