@@ -294,3 +294,32 @@ def test_window_append_decode_wait_reported(kvq):
     ref, ref_lse = reference("q8_0", "q8_0", Xk_h[0], Xv_h[0], N + 2, W, qh[0], wl.scale)
     assert np.abs(out[0].cpu().numpy() - ref).max() <= TOL
     assert np.abs(lse[0].cpu().numpy() - ref_lse).max() <= TOL
+
+
+def test_window_append_decode_large_grid_two_launches(kvq):
+    """A batch whose two-region grid is larger than one resident wave (8 sequences x 8 KV
+    heads x the tail's splits): the launcher refuses the one-launch form and the call runs
+    the append and the decode as two launches, with the same results and lengths."""
+    B, H, D, G, W, N = 8, 8, 128, 5, 16, 40
+    wl = syn.Workload("window-wide", 1, B, H * G, H, D, "q8_0", "q4_0", (N,) * B, seed=77)
+    Xk, Xv = rows_of(wl, syn.KIND_K, B, H, N), rows_of(wl, syn.KIND_V, B, H, N)
+    fused = kvq.WindowedCache(B, H, D, W, 160, "q8_0", "q4_0")
+    split = kvq.WindowedCache(B, H, D, W, 160, "q8_0", "q4_0")
+    assert fused.tail.auto_splits(H * G) * H * B > 152  # more CTAs than one CTA per SM
+    ws = fused.workspace(H * G)
+    Xk_h, Xv_h = Xk.cpu().numpy(), Xv.cpu().numpy()
+    for t in range(N):
+        q = syn.queries(wl, 0, step=t + 1)
+        out, lse = fused.append_decode(Xk[:, :, t].contiguous(), Xv[:, :, t].contiguous(), q, scale=wl.scale,
+                                       workspace=ws)
+        split.append(Xk[:, :, t].contiguous(), Xv[:, :, t].contiguous())
+        out2, lse2 = split.decode(q, scale=wl.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2) and torch.equal(lse, lse2), t
+    assert fused.window.sync_lengths() == [W] * B and fused.tail.sync_lengths() == [N - W] * B
+    assert fused.window.read_error() == 0 and fused.tail.read_error() == 0
+    qh = q.cpu().numpy()
+    for b in (0, B - 1):
+        ref, ref_lse = reference("q8_0", "q4_0", Xk_h[b], Xv_h[b], N, W, qh[b], wl.scale)
+        assert np.abs(out[b].cpu().numpy() - ref).max() <= TOL, b
+        assert np.abs(lse[b].cpu().numpy() - ref_lse).max() <= TOL, b
