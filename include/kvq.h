@@ -209,8 +209,9 @@ KVQ_API kvq_status kvq_decode_auto_splits(const kvq_cache *cache, int32_t n_q_he
 /* Workspace bytes for kvq_decode_attention with this n_splits (0 = auto).  The workspace
  * holds per-(sequence, KV head, group of 8 query rows) arrival counters at its front,
  * then split and group partials.  Zero it once before its first use; every completed
- * decode leaves the counters at zero, including one whose waits timed out (a CTA that
- * gives up still takes its arrivals).  The counters' places depend on the cache's batch
+ * decode leaves the arrival counts at zero (the low 16 bits of each counter: the one-level
+ * column merge keeps a launch epoch in the bits above), including one whose waits timed
+ * out (a CTA that gives up still arrives).  The counters' places depend on the cache's batch
  * and n_kv_heads and on n_q_heads (and n_q for draft verify) but not on n_splits, so one
  * zeroed workspace serves every split count of those shapes; zero it again before using
  * it for another shape. */
@@ -379,8 +380,9 @@ KVQ_API kvq_status kvq_window_append_decode(kvq_cache *window, kvq_cache *tail, 
  * - All calls share the one array, which keeps the contents of the last call.  The arrival
  *   counters at its front must start at zero: a call clears them (an asynchronous memset
  *   on `stream`, before its kernel) when its counter region reaches past the previous
- *   call's, whose split partials lie beyond that region; otherwise they are zero already,
- *   since every finished decode leaves its counters at zero, and the call skips the clear.
+ *   call's, whose split partials lie beyond that region; otherwise their arrival counts
+ *   are zero already, since every finished decode leaves them at zero, and the call skips
+ *   the clear.
  *   Calls that overlap on the GPU (different streams without ordering, or several host
  *   threads) race on the array and give wrong results.
  */
@@ -428,8 +430,8 @@ KVQ_API kvq_status kvq_select_tier(int64_t cells, int32_t n_layers, int32_t n_kv
  * in the cache's error word and goes on waiting; it gives up only at the default bound,
  * after which its CTA publishes an empty split triple, still takes its merge arrivals and
  * returns.  The 128-row verify tile gives up at the limit itself (its copies in flight land
- * first).  Either way the outputs of that launch are undefined, the workspace counters end
- * at zero and a later call on the same workspace is correct again.  For failure handling
+ * first).  Either way the outputs of that launch are undefined, the workspace's arrival
+ * counts end at zero and a later call on the same workspace is correct again.  For failure handling
  * and its tests: a short limit makes the error word report slow waits on a healthy GPU.
  * KVQ_ERR_INVALID_ARG for a negative value.
  */

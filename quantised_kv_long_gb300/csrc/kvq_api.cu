@@ -154,7 +154,8 @@ struct WsLayout {
 // The arrival counters come first and their places depend only on the unit count
 // (sequences x KV heads x row groups), never on n_splits: a workspace zeroed once serves
 // every split count of the same cache shape and query rows, since each completed decode
-// leaves its counters at zero.  Split and group triples follow.
+// leaves its arrival counts (the low 16 bits of each counter) at zero.  Split and group
+// triples follow.
 WsLayout ws_layout(const kvq_cache *c, int32_t n_q_heads, int32_t splits, int32_t n_q = 1) {
     WsLayout w{};
     const size_t G = n_q_heads / c->desc.n_kv_heads;
@@ -884,8 +885,8 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache *cache, const float *q, 
     if (st != KVQ_OK) return st;
     uint8_t *ws = static_cast<uint8_t *>(base);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // The arrival counters of both merge levels must start at zero; the rest is
-    // overwritten.  Every finished decode leaves its counters at zero, so the clear is
+    // The arrival counts of both merge levels must start at zero; the rest is
+    // overwritten.  Every finished decode leaves them at zero, so the clear is
     // needed only when this call's counter region reaches past the previous call's (whose
     // split triples lie beyond it); skipping it keeps the programmatic launch overlap.
     if (w.part_m > g_noalloc_zero[dev]) {

@@ -123,7 +123,9 @@ __device__ __forceinline__ bool arrive_last(int32_t *counter, int target, int &s
     __threadfence();  // each thread publishes its own writes
     __syncthreads();
     if (threadIdx.x == 0) {
-        const int t = atomicAdd(counter, 1);
+        // the low 16 bits count arrivals (a wide merge of an earlier launch may have left a
+        // launch epoch above them)
+        const int t = atomicAdd(counter, 1) & 0xffff;
         s_flag = (t == target - 1);
     }
     __syncthreads();
@@ -356,15 +358,17 @@ __device__ void merge_cols(const float *po, const float *pm, const float *pl, in
     }
 }
 
-// Wait (thread 0) until the first-arrival count (low 16 bits) of *counter reaches target:
-// 0 within `report` SM cycles, 1 later (reported), 2 not within kWaitCycles (gave up).
-constexpr int kSecondArrival = 1 << 16;
-__device__ __forceinline__ int wait_count(const int32_t *counter, int target, long long report) {
+// Wait (thread 0) until the arrivals of a wide merge are complete: the arrival count (low
+// 16 bits) of *counter reaches target, or its launch epoch (the bits above) is no longer
+// `epoch`.  0 within `report` SM cycles, 1 later (reported), 2 not within kWaitCycles (gave
+// up).
+constexpr int kLaunchEpoch = 1 << 16;
+__device__ __forceinline__ int wait_arrivals(const int32_t *counter, unsigned epoch, int target, long long report) {
     const long long t0 = clock64();
     while (true) {
-        int v;
+        unsigned v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(counter) : "memory");
-        if ((v & 0xffff) >= target) return clock64() - t0 > report ? 1 : 0;
+        if (static_cast<int>(v & 0xffffu) >= target || (v >> 16) != epoch) return clock64() - t0 > report ? 1 : 0;
         if (clock64() - t0 > kWaitCycles) return 2;
         __nanosleep(64);
     }
@@ -753,34 +757,32 @@ __device__ __forceinline__ void split_merge(const DecodeParams &p, int NP, int s
     const long long tbytes = static_cast<long long>(NP) * rows * (D + 2) * 4;
     if (p.wide && tbytes > kWideMinBytes) {
         // the last P arrivals each merge a range of columns once every split has arrived.
-        // The counter holds first arrivals in its low 16 bits and the mergers' second
-        // arrivals from bit 16 on, so that merger roles and the final clear stay exact even
-        // when a merger's wait gave up early and its second arrival came before the others'
-        // first ones: the clear is made by the second arrival that completes both counts
-        // (every non-merger arrives before the first merger does).
+        // The counter holds this launch's arrivals in its low 16 bits and a launch epoch
+        // above them: the last arrival adds one epoch and takes the arrivals back to zero
+        // in one atomic, so that the counter is ready for the next launch without a second
+        // round of arrivals; a merger waits until the arrivals reach NP or the epoch moves.
+        // A merger whose wait gave up merges nothing; the counter ends right either way.
         const int C = rows * (D / 4);
         const int P = max(1, min(min(NP, C), static_cast<int>((tbytes + kWideBytes - 1) / kWideBytes)));
         int32_t *cnt = p.counters + unit;
         __threadfence();  // each thread publishes its own writes
         __syncthreads();
         if (threadIdx.x == 0) {
-            const int t = atomicAdd(cnt, 1) & 0xffff;    // earlier first arrivals
-            int role = t >= NP - P ? t - (NP - P) : -1;  // merger index, or -1
-            const int w = role >= 0 && t != NP - 1 ? wait_count(cnt, NP, p.wait_cycles) : 0;
+            const unsigned old = static_cast<unsigned>(atomicAdd(cnt, 1));
+            const int t = static_cast<int>(old & 0xffffu);  // earlier arrivals of this launch
+            int role = t >= NP - P ? t - (NP - P) : -1;     // merger index, or -1
+            if (t == NP - 1) atomicAdd(cnt, kLaunchEpoch - NP);
+            const int w = role >= 0 && t != NP - 1 ? wait_arrivals(cnt, old >> 16, NP, p.wait_cycles) : 0;
             if (w) atomicOr(p.err, KVQ_DEVERR_TIMEOUT);
-            if (w == 2) role = -2;  // a merger that gave up: no merge, but its second arrival counts
+            if (w == 2) role = -1;  // a merger that gave up: no merge
             s_flag = role;
         }
         __syncthreads();
         const int role = s_flag;
-        if (role == -1) return;
-        if (role >= 0) {
-            __threadfence();
-            merge_cols(p.part_o, p.part_m, p.part_l, p.part_stride, NP, row0, D, role * C / P, (role + 1) * C / P,
-                       p.out, p.lse, rmap, p.ext_out, p.ext_lse, smem);
-            __syncthreads();
-        }
-        if (threadIdx.x == 0 && atomicAdd(cnt, kSecondArrival) == NP + (P - 1) * kSecondArrival) atomicExch(cnt, 0);
+        if (role < 0) return;
+        __threadfence();
+        merge_cols(p.part_o, p.part_m, p.part_l, p.part_stride, NP, row0, D, role * C / P, (role + 1) * C / P, p.out,
+                   p.lse, rmap, p.ext_out, p.ext_lse, smem);
         return;
     }
     if (tbytes <= kDirectMergeBytes) {
