@@ -260,7 +260,7 @@ __device__ void merge_rows(const float *po, const float *pm, const float *pl, in
 // k, k + sg, ... with the same running-maximum rule as merge_rows (a handful of splits per
 // thread, one L2 round trip); the sg partial triples of a column are then combined in
 // shared memory.  Memory for the reduction: 24 bytes per thread at `red`.
-constexpr int kWideMinBytes = kDirectMergeBytes;  // smaller row groups merge in one CTA
+constexpr int kWideMinBytes = 16 * 1024;  // smaller row groups merge in one CTA
 constexpr int kWideBytes = 12 * 1024;     // triple bytes per merging CTA
 constexpr int kWideChunk = 8;
 __device__ void merge_cols(const float *po, const float *pm, const float *pl, int stride, int NP, size_t row0,

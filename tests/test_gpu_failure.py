@@ -66,7 +66,7 @@ def check_sequences(wl, q, out, lse, seqs):
 CASES = {
     # name: (batch, Hq, Hkv, D, K type, V type, lengths, n_splits)
     "one-split": (1, 8, 2, 128, "q8_0", "q4_0", (20000,), 1),
-    "last-arrival": (1, 16, 2, 256, "q8_0", "q8_0", (20000,), 4),
+    "last-arrival": (1, 8, 2, 128, "q8_0", "q4_0", (20000,), 4),  # 8 KB of triples: one CTA merges
     "column-merge": (1, 16, 2, 256, "q8_0", "q8_0", (65536,), 0),
     "two-level": (4, 40, 8, 128, "q8_0", "q4_0", (45000, 44000, 43000, 46000), 40),
 }
