@@ -666,7 +666,8 @@ static kvq_status window_splits(const kvq_cache *window, const kvq_cache *tail, 
 }
 
 // One launch over both regions: the tail's automatic split count S is shared between the
-// regions in proportion to their capacity bytes, at least one each.
+// regions in proportion to their capacity bytes (window bytes weighted, below), at least
+// one each.
 static bool dual_splits(const kvq_cache *window, const kvq_cache *tail, int32_t n_q_heads, int *nw, int *S) {
     if (window->desc.head_dim != kvq::kSlice && window->desc.head_dim != 2 * kvq::kSlice) return false;
     int s = 0;
@@ -678,7 +679,12 @@ static bool dual_splits(const kvq_cache *window, const kvq_cache *tail, int32_t 
                 kvq::scale_tile_bytes(c->desc.type_k) + kvq::scale_tile_bytes(c->desc.type_v)) /
                kvq::kTileRows;
     };
-    const double bw = row_bytes(window) * window->desc.capacity, bt = row_bytes(tail) * tail->desc.capacity;
+    // a window byte weighs 1.75 tail bytes: the f16 body runs with the tail's tile-warp
+    // count and reads twice the bytes per value, and the two bodies share the instruction
+    // cache (measured best against 1.0, 1.25, 1.5, 2.0 and 2.5 on both model shapes)
+    constexpr double kWindowWeight = 1.75;
+    const double bw = kWindowWeight * row_bytes(window) * window->desc.capacity;
+    const double bt = row_bytes(tail) * tail->desc.capacity;
     int w = static_cast<int>(s * bw / (bw + bt) + 0.5);
     w = w < 1 ? 1 : (w > s - 1 ? s - 1 : w);
     *nw = w;
