@@ -238,11 +238,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// Hint: pull [src, src + bytes) into L2 (bytes % 16 == 0, src 16-byte aligned).  No data
-// reaches the SM and nothing waits on it; L2 stays coherent with later writes.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
-}
 
 // 16-byte shared-memory load (ordinary load: the mbarrier waits carry memory clobbers)
 __device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
