@@ -474,6 +474,7 @@ struct Cfg {
     static constexpr int QSM_OFF = KCOR_OFF + NS * 128;
     static constexpr int SMEM = QSM_OFF + NS * 8 * 32 * 16 + 16;
     static constexpr int D = NS * kSlice;
+    static constexpr bool F16_PAIR = KT == KVQ_F16 && VT == KVQ_F16;
     // merge / combine scratch reuses the ring
     static_assert(TW * kMaxRowsPerGroup * D * 4 + 2 * TW * kMaxRowsPerGroup * 4 <= RING, "merge buffer");
 };
@@ -714,6 +715,40 @@ __device__ __forceinline__ void split_range(const DecodeParams &p, int T, int sp
     t1 = min(T, t0 + tps);
 }
 
+// Cache tiles this CTA starts with, pulled into L2 while the previous kernel of the stream
+// drains (called before the programmatic-launch wait): f16 caches only, which read two
+// bytes per value and are bound by HBM; for the quantised ones, whose loop is bound by the
+// consumer warps, the extra early traffic slowed the step.  Only a hint: the length read here
+// may be one append behind and the tiles may still be written; L2 is the coherence point,
+// so later reads see every write either way.  Capped per CTA so that the prefetched set of
+// all CTAs stays well inside L2.
+constexpr int kPrefetchBytes = 384 * 1024;
+template <class C>
+__device__ __noinline__ void prefetch_split(const DecodeParams &p, int bseq, int h, int split, int cap_rows,
+                                            int skip_tiles) {
+    if constexpr (!C::F16_PAIR) return;
+    int L = *reinterpret_cast<const volatile int32_t *>(p.len + bseq);
+    if (p.k_new != nullptr) ++L;
+    L = L < 0 ? 0 : (L > cap_rows ? cap_rows : L);
+    const int T = (L + kTileRows - 1) / kTileRows;
+    const int ns = max(1, min(p.n_splits, T));
+    if (split >= ns || T == 0) return;
+    const int tps = (T + ns - 1) / ns;
+    const int t0 = min(T, split * tps + skip_tiles), t1 = min(T, split * tps + tps);
+    const int nt = min(t1 - t0, kPrefetchBytes / C::TILE - skip_tiles);
+    if (nt <= 0) return;
+    const size_t bt = (static_cast<size_t>(bseq) * p.Hkv + h) * p.cap_tiles + t0;
+    constexpr int kChunk = 32768;
+    auto pf = [](const uint8_t *base, size_t bytes) {
+        for (size_t o = 0; o < bytes; o += kChunk)
+            bulk_prefetch_l2(base + o, static_cast<uint32_t>(min(static_cast<size_t>(kChunk), bytes - o)));
+    };
+    pf(p.k_codes + bt * C::KC, static_cast<size_t>(nt) * C::KC);
+    pf(p.v_codes + bt * C::VC, static_cast<size_t>(nt) * C::VC);
+    if constexpr (C::KS > 0) pf(p.k_scales + bt * C::KS, static_cast<size_t>(nt) * C::KS);
+    if constexpr (C::VS > 0) pf(p.v_scales + bt * C::VS, static_cast<size_t>(nt) * C::VS);
+}
+
 // ---------------- merge of the split triples of one (sequence, KV head, row group) ----------------
 // Called by every CTA of the row group once it has written its triple at slot `slot` of
 // the NP slots (row r, slot s at r * part_stride + s).  Small sets: the last CTA to arrive
@@ -825,7 +860,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
     // CTA releases its dependents only after its own wait, so while a kernel runs its
     // pre-wait part at most one earlier kernel of the stream can still be running.
     const bool early = p.early != 0;
-    if (!early) grid_dep_wait();
+    if (!early) {
+        if (threadIdx.x == 0) prefetch_split<C>(p, bseq, h, split, cap_rows, 0);
+        grid_dep_wait();
+    }
     int L_old = __ldcg(p.len + bseq);
     L_old = L_old < 0 ? 0 : (L_old > cap_rows ? cap_rows : L_old);
     // fused append: the new row lands at position L_old and is attended to.  Two-region
@@ -926,8 +964,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const int fus
         if (early) {
             k0 = min(n_stage, C::STAGES);
             if (app_stage >= 0) k0 = min(k0, app_stage);
-            if (lane == 0)
+            if (lane == 0) {
                 for (int k = 0; k < k0; ++k) issue(k, k, 0);
+                prefetch_split<C>(p, bseq, h, split, cap_rows, k0 * C::TWT);
+            }
             __syncwarp();
             grid_dep_wait();
         }

@@ -229,6 +229,11 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
     return t;
 }
+// Hint: pull [src, src + bytes) into L2 (bytes % 16 == 0, src 16-byte aligned).  No data
+// reaches the SM and nothing waits on it; L2 stays coherent with later writes.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
 // 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes % 16 == 0).
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
