@@ -345,7 +345,9 @@ KVQ_API kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *t
  * One decode step of the window + tail pair: kvq_window_append of k, v followed by
  * kvq_window_decode of q, with the same arguments, results and errors, in one launch where
  * the two-region grid is resident at once (one CTA per SM: splits x Hkv x B <= the SM
- * count) -- the read path's two regions then also take the write path: the window's CTA
+ * count), a KV head has at most 8 query heads and the tail has at least two splits (as
+ * chosen by kvq_decode_auto_splits) -- the read path's two regions then also take the write
+ * path: the window's CTA
  * that holds the new row's ring slot writes it there before reading that tile, and, once
  * the window is full, the tail's CTA that holds tail position tail_len first moves the
  * slot's old row there (quantised from its f16 value) and sets a flag in `workspace` that
