@@ -347,14 +347,13 @@ KVQ_API kvq_status kvq_window_decode(const kvq_cache *window, const kvq_cache *t
  * the two-region grid is resident at once (one CTA per SM: splits x Hkv x B <= the SM
  * count), a KV head has at most 8 query heads and the tail has at least two splits (as
  * chosen by kvq_decode_auto_splits) -- the read path's two regions then also take the write
- * path: the window's CTA
- * that holds the new row's ring slot writes it there before reading that tile, and, once
- * the window is full, the tail's CTA that holds tail position tail_len first moves the
- * slot's old row there (quantised from its f16 value) and sets a flag in `workspace` that
- * the window's CTA waits for (bounded) before it overwrites the slot.  Otherwise the two
- * calls run one after the other.  `workspace`: kvq_window_workspace_size bytes, zeroed once
- * (the flags are left at zero; zero it again after a wait gave up, i.e. after
- * KVQ_DEVERR_TIMEOUT from a wait of about two seconds).  Same section 5 P2 as above.
+ * path: the window's CTA that holds the new row's ring slot writes it there before reading
+ * that tile, and, once the window is full, the tail's CTA that holds tail position tail_len
+ * first moves the slot's old row there (quantised from its f16 value) and sets a flag in
+ * `workspace` that the window's CTA waits for (bounded) before it overwrites the slot.
+ * Otherwise the two calls run one after the other. `workspace`: kvq_window_workspace_size
+ * bytes, zeroed once (the flags are left at zero; zero it again after a wait gave up, i.e.
+ * after KVQ_DEVERR_TIMEOUT from a wait of about two seconds). Same section 5 P2 as above.
  */
 KVQ_API kvq_status kvq_window_append_decode(kvq_cache *window, kvq_cache *tail, const float *k, const float *v,
                                             const float *q, int32_t n_q_heads, float scale, void *workspace,
