@@ -681,11 +681,13 @@ static bool dual_splits(const kvq_cache *window, const kvq_cache *tail, int32_t 
                 kvq::scale_tile_bytes(c->desc.type_k) + kvq::scale_tile_bytes(c->desc.type_v)) /
                kvq::kTileRows;
     };
-    // a window byte weighs 1.75 tail bytes: the f16 body runs with the tail's tile-warp
-    // count and reads twice the bytes per value, and the two bodies share the instruction
-    // cache (measured best against 1.0, 1.25, 1.5, 2.0 and 2.5 on both model shapes)
-    constexpr double kWindowWeight = 1.75;
-    const double bw = kWindowWeight * row_bytes(window) * window->desc.capacity;
+    // a window byte weighs more than a tail byte: the f16 body runs with the tail's
+    // tile-warp count and reads twice the bytes per value, and the two bodies share the
+    // instruction cache.  Weights 1.0 / 1.25 / 1.5 / 1.75 / 2.0 / 2.5 measured 42.8 / 44.9 /
+    // 45.4 / 45.9 / 46.2 / 45.2 % of the copy peak with 256-wide heads and 68.5 / 70.3 /
+    // 70.4 / 70.4 / 67.4 / 67.4 % with 128-wide heads.
+    const double weight = window->desc.head_dim == 2 * kvq::kSlice ? 2.0 : 1.75;
+    const double bw = weight * row_bytes(window) * window->desc.capacity;
     const double bt = row_bytes(tail) * tail->desc.capacity;
     int w = static_cast<int>(s * bw / (bw + bt) + 0.5);
     w = w < 1 ? 1 : (w > s - 1 ? s - 1 : w);
