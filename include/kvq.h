@@ -224,7 +224,8 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache *cache, int32_t n_q
  * NULL.  scale multiplies q.k (e.g. 1/sqrt(D)).  Hq must be a multiple of Hkv.  Keys are
  * split into n_splits contiguous ranges per (sequence, KV head) (0 = auto, else 1..1024);
  * each range is attended with an online softmax in fp32, and the last range to finish
- * merges all ranges ("exact online-softmax combine", HAL #582 section 5 P2).  len == 0
+ * merges all ranges exactly (HAL #582 section 5 P2: softmax partials of ranges combine
+ * without loss).  len == 0
  * gives out = 0 and lse = -inf.  One kernel launch.
  */
 KVQ_API kvq_status kvq_decode_attention(const kvq_cache *cache, const float *q, int32_t n_q_heads,

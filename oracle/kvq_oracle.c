@@ -12,7 +12,7 @@
  *     "HAL #582 -- per-layer KV compression study", section 1 (size model table:
  *     q8_0/q8_0 = 102 KiB/token = 8.5 bits per value, q4_0/q4_0 = 54 KiB/token =
  *     4.5 bits per value, f16 = 192 KiB/token).  The rounding rules are the plain
- *     reading of "GGML-style q8_0 and q4_0 blocks of 32 values with an f16 scale":
+ *     reading of GGML-style q8_0 and q4_0 blocks, 32 values sharing one f16 scale:
  *       q8_0:  d = amax/127, codes round-half-away(x * (1/d)) in [-127, 127];
  *       q4_0:  m = the value of largest magnitude (first one on ties), d = m/-8,
  *              codes min(15, trunc(x * (1/d) + 8.5)) in [0, 15], two per byte
@@ -26,8 +26,8 @@
  *     reader to reproduce it: "logit-identical" / real_frac = 0 in HAL #582
  *     section 3b (finding 2) and section 5 (P0 note).
  *
- *   - The split-softmax merge ("exact online-softmax combine", HAL #582 section 5,
- *     P2 read path) in fp64.
+ *   - The split-softmax merge (HAL #582 section 5, P2 read path: partials of key ranges
+ *     combined without loss) in fp64.
  *
  *   - q4_1, q5_0, q5_1 (the further scalar types of the same study, section 5 P0 note
  *     and the P1 ladder, which prices q5_1 at 24 bytes per 32 values).  The pages name

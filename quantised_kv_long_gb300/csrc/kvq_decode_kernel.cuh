@@ -4,7 +4,8 @@
 // Method: single-token grouped-query decode attention with the keys of each (sequence,
 // KV head) split into contiguous ranges; each range is attended with an online softmax
 // in fp32 and the ranges are merged exactly ("HAL #582 -- per-layer KV compression
-// study", section 5 P2 read path: "exact online-softmax combine").  The K/V blocks are
+// study", section 5 P2 read path: the softmax partials of ranges combine without loss).
+// The K/V blocks are
 // dequantised in registers while they are read, which is the cure the same study
 // (section 3b, finding 2) gives for a quantised reader that was kernel-bound: throughput
 // has to follow the bytes moved.

@@ -3,7 +3,7 @@
 //
 // Method: the same exact attention as kvq_decode_verify ("HAL #582 -- per-layer KV
 // compression study", section 5 P0: the typed reader serves decode batches of up to 16
-// query rows; section 5 P2: exact online-softmax combine of key ranges).  With up to 128
+// query rows; section 5 P2: softmax partials of key ranges combine without loss).  With up to 128
 // query rows per KV head the products are real dense tiles, so each key chunk is
 // dequantised once into tensor-core operands and shared by every row, instead of once per
 // group of 8 rows as in the register-operand kernel.

@@ -1,8 +1,8 @@
 // kvq_window_dual.cu -- one decode launch over an f16 window and a quantised tail of the
 // same sequences (dual_kernel in kvq_decode_kernel.cuh): the window's splits and the
 // tail's splits publish their split triples into one set and are merged exactly as one
-// ("HAL #582 -- per-layer KV compression study", section 5 P2 read path: exact
-// online-softmax combine of ranges).  256-wide heads here; 128-wide heads in
+// ("HAL #582 -- per-layer KV compression study", section 5 P2 read path: the softmax
+// partials of the two regions combine without loss).  256-wide heads here; 128-wide heads in
 // kvq_window_dual1.cu (the window body there runs with the tail's tile-warp count, so
 // that both regions share one block size).
 #include "kvq_decode_kernel.cuh"
