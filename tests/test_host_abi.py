@@ -92,6 +92,10 @@ def test_null_pointers_rejected_without_cuda():
     assert kvq.lib.kvq_quantize_append(None, None, None, 0, 1, 1, None) == 1
     assert kvq.lib.kvq_decode_attention(None, None, 4, ctypes.c_float(1.0), 0, None, None, None, None) == 1
     assert kvq.lib.kvq_combine(None, None, None, 1, 1, 128, None, None, None) == 1
+    f1 = ctypes.c_float(1.0)
+    assert kvq.lib.kvq_window_append(None, None, None, None, None) == 1
+    assert kvq.lib.kvq_window_decode(None, None, None, 4, f1, None, None, None, None) == 1
+    assert kvq.lib.kvq_window_append_decode(None, None, None, None, None, 4, f1, None, None, None, None) == 1
     # misaligned pointers are refused before any CUDA call
     fake = ctypes.c_void_p(0x1000)
     bad = ctypes.c_void_p(0x1004)
