@@ -327,12 +327,14 @@ KVQ_API kvq_status kvq_set_verify_path(int32_t path);
  * (window_len + tail_len rows per sequence), written like kvq_decode_attention.  Each
  * region is read by its own typed decode (the read path of section 5 P2) and the output is
  * the exact merge of both regions.  Normally one launch: its first splits read the window,
- * the rest the tail (the split count shared in proportion to the regions' capacity bytes),
- * and all split triples are merged as one set.  Where the tail's split count is below two,
+ * the rest the tail (the split count shared in proportion to the regions' capacity bytes,
+ * a window byte weighted 2 with 256-wide heads and 1.75 with 128-wide ones), and all split
+ * triples are merged as one set.  Where the tail's split count is below two,
  * two launches: the window's decode writes its normalised result into `workspace`, and the
  * tail's final merge takes that result as one more split triple.  `workspace`:
  * kvq_window_workspace_size bytes, zeroed once before its first use (as for
- * kvq_decode_attention).
+ * kvq_decode_attention); it also holds the eviction flags of kvq_window_append_decode
+ * (one int32 per sequence and KV head, at its end).
  */
 KVQ_API kvq_status kvq_window_append(kvq_cache *window, kvq_cache *tail, const float *k, const float *v,
                                      void *stream);
